@@ -1,0 +1,408 @@
+"""Benchmark: sparse-FFN decode tokens/s at batch 1 on one GB300, with the HBM
+roofline fraction of the dominant kernel and the CPU oracle as baseline.
+
+Default workload: the OPT-13B-shaped layer (d=5120, f=20480, predictor r=512,
+fp16 weights, fp32 accumulation), top-k selection at 10% (k=2048), batch 1.
+A step is one token through the whole hot path: predictor (two GEMVs), top-k
+selection, gathered FFN (gate GEMV + ReLU + down AXPY + reduction).  Steps
+rotate over NCOPY independent layer copies and 512 distinct inputs, so each
+copy's touched bytes are evicted from L2 by the other copies before reuse.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas: the path has no exchange step); value = all ranks' steps / max time.
+--impl reference times the CPU oracle (the only reference this method has) on
+rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-FFN decode tokens/s at batch 1 and effective HBM GB/s vs GB300 peak"
+
+WORKLOADS = {
+    # name: d, f, r, dtype, glu, rho (profile), mode, share (k or threshold quantile)
+    "opt13b-topk10": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.10),
+    "opt13b-topk5": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.05),
+    "opt13b-topk20": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.20),
+    "opt13b-thr10": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="threshold", share=0.10),
+    "tiny-relu-topk10": dict(d=512, f=2048, r=64, dt=0, glu=False, rho=0.10, mode="topk", share=0.10),
+}
+NCOPY = 8
+NX = 200
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=2000)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="opt13b-topk10", choices=sorted(WORKLOADS))
+    p.add_argument("--cpu-sample-s", type=float, default=12.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            m = json.load(fh)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.dev = dev_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def src_sha(path):
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def profile_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since the capture; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            t = json.load(fh)
+        e = t[kernel][workload]
+        if e["source_sha"] != src_sha(os.path.join(ROOT, e["source"])):
+            return None
+        return e["traffic_bytes"]
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def build_copies(W, torch, cs, synthdev):
+    import synth
+    d, f, r, dt = W["d"], W["f"], W["r"], W["dt"]
+    tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}[dt]
+    sd = 1 / math.sqrt(d)
+    copies = []
+    for l in range(NCOPY):
+        t = {}
+        for name, which, rows, cols in (("w_gate", synth.W_GATE, f, d), ("w_down_t", synth.W_DOWN_T, f, d),
+                                        ("p_down", synth.P_DOWN, r, d), ("p_up", synth.P_UP, f, r)):
+            t[name] = torch.empty((rows, cols), dtype=tdt, device="cuda")
+            synthdev.fill_normal(t[name], 0, synth.tensor_id(l, which), sd)
+        if W["glu"]:
+            t["w_up"] = torch.empty((f, d), dtype=tdt, device="cuda")
+            synthdev.fill_normal(t["w_up"], 0, synth.tensor_id(l, synth.W_UP), sd)
+        t["bias"] = torch.from_numpy(synth.zipf_bias(0, l, f, W["rho"])).cuda()
+        layer = cs.FfnLayer(t["w_gate"], t["w_down_t"], w_up=t.get("w_up"), bias=t["bias"])
+        pred = cs.Predictor(t["p_down"], t["p_up"])
+        copies.append((layer, pred, t))
+    torch.cuda.synchronize()
+    return copies
+
+
+def step_bytes(W, k):
+    """Algorithmic bytes of one step (S8(d)-style accounting): predictor weights,
+    scores written and read, selected rows (+ index and bias), x and y."""
+    d, f, r = W["d"], W["f"], W["r"]
+    e = 4 if W["dt"] == 0 else 2
+    m = 3 if W["glu"] else 2
+    pred = e * (r * d + f * r) + 4 * (d + r) * 2
+    sel = 4 * f + 4 * k
+    ffn = k * (m * d * e + 4 + 4) + 4 * d * 2
+    return pred + sel + ffn, ffn
+
+
+def run_ours(args, W, rank, world):
+    import torch
+    import contextual_sparsity_sparse_gb300 as cs
+    import synth
+    import synth.device as synthdev
+    from contextual_sparsity_sparse_gb300 import build as cb
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    cb.build()
+    synthdev.build()
+    d, f, r = W["d"], W["f"], W["r"]
+    k = synth.ceil_k(f, W["share"])
+    copies = build_copies(W, torch, cs, synthdev)
+    X = torch.from_numpy(synth.x_normal(1000 + rank, NX, d)).cuda()
+    s = torch.cuda.Stream()
+    ws = cs.Workspace(d, f, r, stream=s)
+    scores = torch.empty((1, f), device="cuda")
+    idx = torch.empty((1, f), dtype=torch.int32, device="cuda")
+    cnt = torch.empty(1, dtype=torch.int32, device="cuda")
+    Y = torch.empty((NX, d), device="cuda")
+    if W["mode"] == "topk":
+        params = cs.select_params(cs.CS_SEL_TOPK, k)
+    else:
+        # threshold at the (1 - share) quantile of calibration scores (seed 1)
+        layer0, pred0, _ = copies[0]
+        Xc = torch.from_numpy(synth.x_normal(1, 256, d)).cuda()
+        sc = torch.empty((256, f), device="cuda")
+        cs.cs_predict(pred0, Xc, sc, cs.Workspace(d, f, r, 256))
+        torch.cuda.synchronize()
+        tau = float(torch.quantile(sc.flatten()[:: 7].float(), 1 - W["share"]))
+        params = cs.select_params(cs.CS_SEL_THRESHOLD, 0, tau)
+
+    def one_step(i, with_events=None):
+        layer, pred, _ = copies[i % NCOPY]
+        x = X[i % NX: i % NX + 1]
+        cs.cs_predict(pred, x, scores, ws, stream=s)
+        cs.cs_select(scores, params, idx, cnt, stream=s)
+        if with_events is not None:
+            with_events[0].record(s)
+        cs.cs_sparse_ffn(layer, x, idx, cnt, Y[i % NX: i % NX + 1], ws, stream=s)
+        if with_events is not None:
+            with_events[1].record(s)
+
+    # graph of NB steps (launch overhead out of the timed region)
+    NB = 200
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(3):
+            one_step(i)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(NB):
+                one_step(i)
+    K = max(NB, (args.steps // NB) * NB)
+    Wm = max(3 * NB, (args.warmup // NB) * NB)
+    with torch.cuda.stream(s):
+        for _ in range(Wm // NB):
+            g.replay()
+    s.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk = Clocks(dev)
+    clk.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(K // NB):
+            g.replay()
+    e1.record(s)
+    e1.synchronize()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    assert cs.cs_get_device_error(ws, stream=s) == 0
+
+    # roofline pass: the same steps with event records around each FFN call
+    def timing_event():
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:  # older torch: no event-record nodes in graphs
+            return None
+    ev = [(timing_event(), timing_event()) for _ in range(NB)]
+    if ev[0][0] is None:
+        raise RuntimeError("torch.cuda.Event(external=True) is required for the roofline pass")
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g2, stream=s):
+            for i in range(NB):
+                one_step(i, ev[i])
+    ffn_ms = []
+    with torch.cuda.stream(s):
+        for rep in range(max(1, K // NB // 4)):
+            g2.replay()
+            s.synchronize()
+            ffn_ms += [a.elapsed_time(b) for a, b in ev]
+    ffn_avg_s = statistics.mean(ffn_ms) / 1e3
+
+    # e2e: through the public API with pinned host buffers, copies in the timed region
+    KE = min(K, 2000)
+    xh = torch.from_numpy(synth.x_normal(2000 + rank, 64, d)).pin_memory()
+    yh = torch.empty((64, d)).pin_memory()
+    xd = torch.empty((1, d), device="cuda")
+    yd = torch.empty((1, d), device="cuda")
+
+    def e2e_step(i):
+        layer, pred, _ = copies[i % NCOPY]
+        xd.copy_(xh[i % 64: i % 64 + 1], non_blocking=True)
+        cs.cs_predict(pred, xd, scores, ws, stream=s)
+        cs.cs_select(scores, params, idx, cnt, stream=s)
+        cs.cs_sparse_ffn(layer, xd, idx, cnt, yd, ws, stream=s)
+        yh[i % 64: i % 64 + 1].copy_(yd, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for i in range(50):
+            e2e_step(i)
+    s.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for i in range(KE):
+            e2e_step(i)
+    s.synchronize()
+    e2e_s = time.perf_counter() - t0
+
+    total_b, ffn_b = step_bytes(W, k)
+    hbm, src = peaks()
+    step_s = ms / 1e3 / K
+    ffn_gbs = ffn_b / ffn_avg_s / 1e9
+    res = {
+        "metric": METRIC, "value": world * K / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "d": d, "f": f, "r": r, "k": k if W["mode"] == "topk" else None,
+                   "selection": W["mode"], "weights": {0: "f32", 1: "f16", 2: "bf16"}[W["dt"]],
+                   "accumulate": "f32", "batch": 1, "global_batch": world, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {NCOPY} layer copies ({NCOPY * (2 * f * d + r * d + f * r) * (4 if W['dt'] == 0 else 2) / 1e9:.2f} GB) and {NX} inputs rotate; 7 other steps ({7 * total_b / 1e6:.0f} MB) run between uses of a copy",
+                   "step": "cs_predict + cs_select + cs_sparse_ffn, graph of 200 steps"},
+        "clocks": clocks,
+        "gpu_launches": 5 * K,
+        "roofline": {"bound": "hbm", "kernel": "cs_sparse_ffn (gather + fixed-order reduce)",
+                     "achieved": ffn_gbs, "peak": hbm, "unit": "GB/s", "frac": ffn_gbs / hbm,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
+                     "bytes_per_launch": ffn_b, "avg_launch_us": ffn_avg_s * 1e6,
+                     "traffic": profile_traffic("ffn_gather_kernel", args.workload)},
+        "step_roofline": {"bytes_per_step": total_b, "achieved": total_b / step_s / 1e9, "peak": hbm,
+                          "frac": total_b / step_s / 1e9 / hbm, "unit": "GB/s"},
+        "e2e": {"value": world * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * d,
+                "d2h_bytes_per_step": 4 * d, "steps": KE,
+                "how": "Python binding per step: pinned H2D of x, cs_predict, cs_select, cs_sparse_ffn, D2H of y; wall clock"},
+    }
+    return res, copies
+
+
+def oracle_step_inputs(W, layer_index=0):
+    import numpy as np
+    import oracle
+    import synth
+    d, f, r, dt = W["d"], W["f"], W["r"], W["dt"]
+    sd = 1 / math.sqrt(d)
+    mk = lambda which, rows, cols: synth.normal_matrix(0, synth.tensor_id(layer_index, which), rows, cols, sd, dt)
+    L = oracle.Layer(d, f, dt, mk(synth.W_GATE, f, d), mk(synth.W_DOWN_T, f, d),
+                     w_up=mk(synth.W_UP, f, d) if W["glu"] else None,
+                     bias=synth.zipf_bias(0, layer_index, f, W["rho"]))
+    P = oracle.Predictor(d, r, f, dt, mk(synth.P_DOWN, r, d), mk(synth.P_UP, f, r))
+    return L, P
+
+
+def time_oracle(W, budget_s, max_steps=None):
+    """Time the oracle's decode step (predict, select, gathered FFN) on the host."""
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    L, P = oracle_step_inputs(W)
+    k = synth.ceil_k(W["f"], W["share"])
+    X = synth.x_normal(3000, 64, W["d"])
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _, s = oracle.predict(P, X[n % 64])
+        s32 = s.astype(np.float32)
+        if W["mode"] == "topk":
+            sel = oracle.select_topk(s32, k)
+        else:
+            if n == 0:  # threshold at the (1 - share) quantile of the oracle's own scores
+                tau = np.float32(np.quantile(s32, 1 - W["share"]))
+            sel = oracle.select_threshold(s32, tau)
+        oracle.ffn(L, X[n % 64], sel)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps and n >= max_steps):
+            break
+    return n, el, oracle.threads()
+
+
+def main():
+    args = parse()
+    W = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        n, el, cores = time_oracle(W, budget_s=1e9, max_steps=max(1, args.warmup))
+        n, el, cores = time_oracle(W, budget_s=1e9, max_steps=max(1, args.steps))
+        v = n / el
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * el / n, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "d": W["d"], "f": W["f"], "r": W["r"]},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} decode steps (predict, select, gathered FFN) of the workload, fp64 CPU oracle"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res, _ = run_ours(args, W, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, el, cores = time_oracle(W, args.cpu_sample_s)
+        res["cpu_baseline"] = {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "sample": f"{n} decode steps of the workload in {el:.1f} s (fp64 CPU oracle, {cores} threads)"}
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+"""Python binding of the contextual-sparsity sparse FFN library (libcs.so).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  The functions carry the
+C ABI's names (include/cs.h) and raise :class:`CsError` on a non-OK status.
+There is no fallback: if libcs.so is missing, importing the binding's loader
+raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+CS_F32, CS_F16, CS_BF16 = 0, 1, 2
+CS_SEL_TOPK, CS_SEL_THRESHOLD, CS_SEL_EXACT = 0, 1, 2
+CS_STACK_SEQUENTIAL, CS_STACK_LOOKAHEAD = 0, 1
+CS_DEVERR_INDEX, CS_DEVERR_COUNT, CS_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+
+_TORCH_DT = {torch.float32: CS_F32, torch.float16: CS_F16, torch.bfloat16: CS_BF16}
+
+# every symbol include/cs.h declares
+EXPORTS = ["cs_version", "cs_status_string", "cs_last_error", "cs_workspace_size",
+           "cs_workspace_init", "cs_get_device_error", "cs_pack_transpose", "cs_predict",
+           "cs_select", "cs_sparse_ffn", "cs_exact_ffn", "cs_union_mask", "cs_decode_stack",
+           "cs_stack_release"]
+
+
+class CsError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+class _Pred(C.Structure):
+    _fields_ = [("d", C.c_int), ("r", C.c_int), ("f", C.c_int), ("dtype", C.c_int),
+                ("ld_down", C.c_int), ("ld_up", C.c_int), ("p_down", C.c_void_p),
+                ("p_up", C.c_void_p)]
+
+
+class _Layer(C.Structure):
+    _fields_ = [("d", C.c_int), ("f", C.c_int), ("dtype", C.c_int), ("ld", C.c_int),
+                ("w_gate", C.c_void_p), ("w_up", C.c_void_p), ("w_down_t", C.c_void_p),
+                ("bias", C.c_void_p)]
+
+
+class _Sel(C.Structure):
+    _fields_ = [("mode", C.c_int), ("k", C.c_int), ("tau", C.c_float)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libcs.so (built by ``build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise ImportError(f"CUDA library {path} is missing; run "
+                                  "contextual_sparsity_sparse_gb300.build.build() first")
+            L = C.CDLL(path)
+            P, I, S, U = C.c_void_p, C.c_int, C.c_size_t, C.c_uint32
+            L.cs_version.restype = C.c_char_p
+            L.cs_status_string.argtypes = [I]
+            L.cs_status_string.restype = C.c_char_p
+            L.cs_last_error.restype = C.c_char_p
+            L.cs_workspace_size.argtypes = [I, I, I, I]
+            L.cs_workspace_size.restype = S
+            L.cs_workspace_init.argtypes = [P, S, P]
+            L.cs_get_device_error.argtypes = [P, P, I, C.POINTER(U)]
+            L.cs_pack_transpose.argtypes = [P, I, I, I, I, P, I, I, P]
+            L.cs_predict.argtypes = [C.POINTER(_Pred), P, I, P, P, S, P]
+            L.cs_select.argtypes = [P, I, I, C.POINTER(_Sel), P, P, P, P, S, P]
+            L.cs_sparse_ffn.argtypes = [C.POINTER(_Layer), P, I, P, P, P, P, S, P]
+            L.cs_exact_ffn.argtypes = [C.POINTER(_Layer), P, P, P, P, P, P, P, S, P]
+            L.cs_union_mask.argtypes = [P, I, I, P, P, P, P, S, P]
+            L.cs_decode_stack.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), I, P, C.c_float,
+                                          C.POINTER(_Sel), I, P, P, P, S, P, P]
+            for name in ("cs_workspace_init", "cs_get_device_error", "cs_pack_transpose",
+                         "cs_predict", "cs_select", "cs_sparse_ffn", "cs_exact_ffn",
+                         "cs_union_mask", "cs_decode_stack", "cs_stack_release"):
+                getattr(L, name).restype = I
+            _lib = L
+    return _lib
+
+
+def _check(status):
+    if status != 0:
+        L = lib()
+        raise CsError(status, f"{L.cs_status_string(status).decode()}: {L.cs_last_error().decode()}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+def _dt(t):
+    return _TORCH_DT[t.dtype]
+
+
+class Predictor:
+    """p_down [r, ld_down], p_up [f, ld_up]; d is the used width of p_down."""
+
+    def __init__(self, p_down, p_up, d=None, r=None):
+        self.p_down, self.p_up = p_down, p_up
+        self.r, ldd = p_down.shape
+        self.f, ldu = p_up.shape
+        self.d = int(d if d is not None else ldd)
+        if r is not None and r != self.r:
+            raise ValueError("r does not match p_down")
+        self.c = _Pred(self.d, self.r, self.f, _dt(p_down), ldd, ldu, _ptr(p_down), _ptr(p_up))
+
+
+class FfnLayer:
+    """Neuron-major layer: w_gate, w_up, w_down_t are [f, ld]; d is the used
+    width (default ld).  w_up None gives the gate-only ReLU FFN."""
+
+    def __init__(self, w_gate, w_down_t, w_up=None, bias=None, d=None):
+        self.w_gate, self.w_down_t, self.w_up, self.bias = w_gate, w_down_t, w_up, bias
+        self.f, ld = w_gate.shape
+        self.d = int(d if d is not None else ld)
+        self.c = _Layer(self.d, self.f, _dt(w_gate), ld, _ptr(w_gate), _ptr(w_up), _ptr(w_down_t),
+                        _ptr(bias))
+
+
+def select_params(mode, k=0, tau=0.0):
+    return _Sel(int(mode), int(k), float(tau))
+
+
+class Workspace:
+    """Device workspace sized by cs_workspace_size and initialised once."""
+
+    def __init__(self, d, f, r, B=1, device=None, stream=None):
+        n = lib().cs_workspace_size(int(d), int(f), int(r), int(B))
+        if n == 0:
+            raise ValueError("bad workspace dimensions")
+        self.nbytes = n
+        self.buf = torch.empty(n + 256, dtype=torch.uint8, device=device or "cuda")
+        base = self.buf.data_ptr()
+        self.ptr = (base + 255) & ~255
+        _check(lib().cs_workspace_init(self.ptr, self.nbytes, _stream(stream)))
+
+
+def cs_version() -> str:
+    return lib().cs_version().decode()
+
+
+def cs_workspace_size(d, f, r, B=1) -> int:
+    return int(lib().cs_workspace_size(int(d), int(f), int(r), int(B)))
+
+
+def cs_get_device_error(ws: Workspace, stream=None, clear=False) -> int:
+    v = C.c_uint32(0)
+    _check(lib().cs_get_device_error(ws.ptr, _stream(stream), int(bool(clear)), C.byref(v)))
+    return v.value
+
+
+def cs_pack_transpose(src, dst, rows=None, cols=None, stream=None):
+    """dst[c, r] = src[r, c] (with dtype conversion).  src [rows, ld_src],
+    dst [cols, ld_dst]."""
+    rows = src.shape[0] if rows is None else rows
+    cols = src.shape[1] if cols is None else cols
+    _check(lib().cs_pack_transpose(_ptr(src), _dt(src), int(rows), int(cols), src.shape[1],
+                                   _ptr(dst), _dt(dst), dst.shape[1], _stream(stream)))
+
+
+def cs_predict(pred: Predictor, x, scores, ws: Workspace, stream=None):
+    B = x.shape[0] if x.dim() == 2 else 1
+    _check(lib().cs_predict(C.byref(pred.c), _ptr(x), B, _ptr(scores), ws.ptr, ws.nbytes,
+                            _stream(stream)))
+
+
+def cs_select(scores, params, idx, count, mask=None, ws: Workspace | None = None, stream=None):
+    B, f = (scores.shape if scores.dim() == 2 else (1, scores.shape[0]))
+    _check(lib().cs_select(_ptr(scores), B, f, C.byref(params), _ptr(idx), _ptr(count),
+                           _ptr(mask), ws.ptr if ws else None, ws.nbytes if ws else 0,
+                           _stream(stream)))
+
+
+def cs_sparse_ffn(layer: FfnLayer, x, idx, count, y, ws: Workspace, stream=None):
+    B = x.shape[0] if x.dim() == 2 else 1
+    _check(lib().cs_sparse_ffn(C.byref(layer.c), _ptr(x), B, _ptr(idx), _ptr(count), _ptr(y),
+                               ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def cs_exact_ffn(layer: FfnLayer, x, preact, idx, count, y, ws: Workspace, mask=None, stream=None):
+    _check(lib().cs_exact_ffn(C.byref(layer.c), _ptr(x), _ptr(preact), _ptr(idx), _ptr(count),
+                              _ptr(mask), _ptr(y), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def cs_union_mask(masks, f, umask, uidx, ucount, ws: Workspace | None = None, stream=None):
+    B = masks.shape[0]
+    _check(lib().cs_union_mask(_ptr(masks), B, int(f), _ptr(umask), _ptr(uidx), _ptr(ucount),
+                               ws.ptr if ws else None, ws.nbytes if ws else 0, _stream(stream)))
+
+
+def cs_decode_stack(layers, preds, x, resid_scale, params, mode, ws: Workspace, s_main=None,
+                    s_pred=None, trace_count=None, trace_idx=None):
+    L = len(layers)
+    larr = (_Layer * L)(*[l.c for l in layers])
+    parr = (_Pred * L)(*[p.c for p in preds]) if preds is not None else None
+    sp = None if s_pred is None else _stream(s_pred)
+    _check(lib().cs_decode_stack(larr, parr, L, _ptr(x), float(resid_scale), C.byref(params),
+                                 int(mode), _stream(s_main), sp, ws.ptr, ws.nbytes,
+                                 _ptr(trace_count), _ptr(trace_idx)))
+
+
+def cs_stack_release():
+    _check(lib().cs_stack_release())

@@ -1,0 +1,354 @@
+// Layer stack on the residual stream, with look-ahead prediction.
+//
+// Source: "Contextual Sparsity and Activation Predictors", section "The
+// predictor and its budget": the residual stream changes slowly between
+// blocks (x_{l+1} = x_l + f_l(x_l)), so the sparsity of layer l+1 can be
+// predicted from the input of layer l and the prediction run asynchronously,
+// off the critical path.  Section "When it breaks" notes the approximation is
+// weakest in early layers.
+//
+// GB300 mapping.  Stream P runs predictor + selection of layer l+1 from x_l
+// while stream M runs layer l's gathered FFN, which writes
+// x_{l+1} = x_l + c * FFN_l(x_l) into the other half of a ping-pong pair.
+// Dependencies are CUDA events; the whole L-layer fork/join is captured once
+// into a CUDA graph (per distinct argument set) and replayed, so a decode step
+// costs one graph launch instead of ~4L kernel launches.
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+#include "cs_internal.cuh"
+
+namespace cs {
+int ffn_max_d(cs_dtype t);
+}
+
+using namespace cs;
+
+namespace {
+
+struct StackPlan {
+    const cs_ffn_layer *layers;
+    const cs_predictor *preds;
+    int L, d, f, r;
+    float *x;
+    float scale;
+    cs_select_params sel;
+    cs_stack_mode mode;
+    char *ws;
+    WsLayout lay;
+    int32_t *trace_count, *trace_idx;
+};
+
+struct Bufs {
+    float *xb[2];
+    float *h, *scores, *pre, *part;
+    int32_t *idx_slot[2], *cnt_slot[2];
+    uint32_t *err;
+};
+
+Bufs bufs_of(const StackPlan &p) {
+    Bufs b;
+    b.xb[0] = p.x;
+    b.xb[1] = reinterpret_cast<float *>(p.ws + p.lay.st_x);
+    b.h = reinterpret_cast<float *>(p.ws + p.lay.st_h);
+    b.scores = reinterpret_cast<float *>(p.ws + p.lay.st_scores);
+    b.pre = reinterpret_cast<float *>(p.ws + p.lay.st_pre);
+    b.part = reinterpret_cast<float *>(p.ws + p.lay.part);
+    int32_t *slots = reinterpret_cast<int32_t *>(p.ws + p.lay.st_idx);
+    b.idx_slot[0] = slots;
+    b.idx_slot[1] = slots + p.f;
+    int32_t *cnt = reinterpret_cast<int32_t *>(p.ws + p.lay.st_count);
+    b.cnt_slot[0] = cnt;
+    b.cnt_slot[1] = cnt + 1;
+    b.err = reinterpret_cast<uint32_t *>(p.ws);
+    return b;
+}
+
+void sel_out(const StackPlan &p, const Bufs &b, int l, int32_t **idx, int32_t **cnt) {
+    if (p.trace_idx) *idx = p.trace_idx + (size_t)l * p.f;
+    else *idx = b.idx_slot[l & 1];
+    if (p.trace_count) *cnt = p.trace_count + l;
+    else *cnt = b.cnt_slot[l & 1];
+}
+
+cudaError_t predict_select(const StackPlan &p, const Bufs &b, int l, const float *xin, cudaStream_t s) {
+    const cs_predictor &P = p.preds[l];
+    PredictArgs a;
+    a.d = P.d; a.r = P.r; a.f = P.f; a.B = 1; a.dtype = P.dtype;
+    a.ld_down = P.ld_down; a.ld_up = P.ld_up; a.p_down = P.p_down; a.p_up = P.p_up;
+    a.x = xin; a.h = b.h; a.scores = b.scores;
+    cudaError_t e = launch_predict(a, s);
+    if (e != cudaSuccess) return e;
+    SelectArgs sa;
+    sa.scores = b.scores; sa.B = 1; sa.f = p.f;
+    sa.kind = p.sel.mode == CS_SEL_TOPK ? SEL_TOPK : SEL_THRESHOLD;
+    sa.k = p.sel.k; sa.tau = p.sel.tau;
+    sel_out(p, b, l, &sa.idx, &sa.count);
+    sa.ld_idx = p.f; sa.mask = nullptr;
+    return launch_select(sa, s);
+}
+
+cudaError_t ffn_step(const StackPlan &p, const Bufs &b, int l, const float *xin, float *xout,
+                     const float *preact, cudaStream_t s) {
+    const cs_ffn_layer &Ly = p.layers[l];
+    FfnArgs a;
+    a.d = Ly.d; a.f = Ly.f; a.ld = Ly.ld ? Ly.ld : Ly.d; a.B = 1; a.dtype = Ly.dtype;
+    a.w_gate = Ly.w_gate; a.w_up = Ly.w_up; a.w_down_t = Ly.w_down_t; a.bias = Ly.bias;
+    a.x = xin;
+    int32_t *idx, *cnt;
+    sel_out(p, b, l, &idx, &cnt);
+    a.idx = idx; a.count = cnt;
+    a.preact = preact;
+    a.y = xout; a.resid = xin; a.scale = p.scale;
+    a.err = b.err; a.part = b.part; a.G = p.lay.G; a.dp = p.lay.dp;
+    return launch_ffn(a, s);
+}
+
+cudaError_t exact_step(const StackPlan &p, const Bufs &b, int l, const float *xin, float *xout,
+                       cudaStream_t s) {
+    const cs_ffn_layer &Ly = p.layers[l];
+    PreactArgs pa;
+    pa.d = Ly.d; pa.f = Ly.f; pa.ld = Ly.ld ? Ly.ld : Ly.d; pa.dtype = Ly.dtype;
+    pa.w_gate = Ly.w_gate; pa.bias = Ly.bias; pa.x = xin; pa.pre = b.pre;
+    cudaError_t e = launch_preact(pa, s);
+    if (e != cudaSuccess) return e;
+    SelectArgs sa;
+    sa.scores = b.pre; sa.B = 1; sa.f = p.f; sa.kind = SEL_POSITIVE; sa.k = 0; sa.tau = 0.f;
+    sel_out(p, b, l, &sa.idx, &sa.count);
+    sa.ld_idx = p.f; sa.mask = nullptr;
+    e = launch_select(sa, s);
+    if (e != cudaSuccess) return e;
+    return ffn_step(p, b, l, xin, xout, b.pre, s);
+}
+
+struct Events {
+    std::vector<cudaEvent_t> ev;
+    ~Events() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    }
+    cudaError_t make(int n) {
+        ev.resize(n, nullptr);
+        for (int i = 0; i < n; ++i) {
+            cudaError_t e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+};
+
+#define TRY(x)                                  \
+    do {                                        \
+        cudaError_t e_ = (x);                   \
+        if (e_ != cudaSuccess) return e_;       \
+    } while (0)
+
+// Enqueue the whole stack.  s_pred is only touched in look-ahead mode.
+cudaError_t enqueue_stack(const StackPlan &p, cudaStream_t sm, cudaStream_t sp, Events &E) {
+    const Bufs b = bufs_of(p);
+    const int L = p.L;
+    if (p.sel.mode == CS_SEL_EXACT) {
+        for (int l = 0; l < L; ++l) TRY(exact_step(p, b, l, b.xb[l & 1], b.xb[(l + 1) & 1], sm));
+    } else if (p.mode == CS_STACK_SEQUENTIAL || sp == sm) {
+        if (p.mode == CS_STACK_SEQUENTIAL) {
+            for (int l = 0; l < L; ++l) {
+                TRY(predict_select(p, b, l, b.xb[l & 1], sm));
+                TRY(ffn_step(p, b, l, b.xb[l & 1], b.xb[(l + 1) & 1], nullptr, sm));
+            }
+        } else {
+            // look-ahead semantics on one stream: layer l+1's set from x_l
+            TRY(predict_select(p, b, 0, b.xb[0], sm));
+            for (int l = 0; l < L; ++l) {
+                if (l + 1 < L) TRY(predict_select(p, b, l + 1, b.xb[l & 1], sm));
+                TRY(ffn_step(p, b, l, b.xb[l & 1], b.xb[(l + 1) & 1], nullptr, sm));
+            }
+        }
+    } else {
+        // events: 0 fork, 1 join, 2..2+L sel[l], 2+L..2+2L+1 x[l]
+        TRY(E.make(2 + L + L + 1));
+        cudaEvent_t ev_fork = E.ev[0], ev_join = E.ev[1];
+        auto ev_sel = [&](int l) { return E.ev[2 + l]; };
+        auto ev_x = [&](int l) { return E.ev[2 + L + l]; };
+        TRY(cudaEventRecord(ev_fork, sm));
+        TRY(cudaStreamWaitEvent(sp, ev_fork, 0));
+        TRY(predict_select(p, b, 0, b.xb[0], sp));
+        TRY(cudaEventRecord(ev_sel(0), sp));
+        for (int l = 0; l < L; ++l) {
+            if (l + 1 < L) {
+                if (l > 0) TRY(cudaStreamWaitEvent(sp, ev_x(l), 0));
+                TRY(predict_select(p, b, l + 1, b.xb[l & 1], sp));
+                TRY(cudaEventRecord(ev_sel(l + 1), sp));
+            }
+            TRY(cudaStreamWaitEvent(sm, ev_sel(l), 0));
+            TRY(ffn_step(p, b, l, b.xb[l & 1], b.xb[(l + 1) & 1], nullptr, sm));
+            TRY(cudaEventRecord(ev_x(l + 1), sm));
+        }
+        TRY(cudaEventRecord(ev_join, sp));
+        TRY(cudaStreamWaitEvent(sm, ev_join, 0));
+    }
+    if (L & 1)
+        TRY(cudaMemcpyAsync(p.x, b.xb[1], sizeof(float) * (size_t)p.d, cudaMemcpyDeviceToDevice, sm));
+    return cudaSuccess;
+}
+
+struct CacheEntry {
+    cudaGraphExec_t exec = nullptr;
+    int device = -1;
+};
+
+std::mutex g_mu;
+std::unordered_map<std::string, CacheEntry> g_cache;
+constexpr size_t kMaxCached = 64;
+
+std::string plan_key(const StackPlan &p, cudaStream_t sp, int dev) {
+    std::string k;
+    auto put = [&](const void *v, size_t n) { k.append(static_cast<const char *>(v), n); };
+    put(&dev, sizeof dev);
+    put(&p.L, sizeof p.L);
+    put(p.layers, sizeof(cs_ffn_layer) * p.L);
+    if (p.sel.mode != CS_SEL_EXACT) put(p.preds, sizeof(cs_predictor) * p.L);
+    put(&p.x, sizeof p.x);
+    put(&p.scale, sizeof p.scale);
+    put(&p.sel, sizeof p.sel);
+    put(&p.mode, sizeof p.mode);
+    put(&p.ws, sizeof p.ws);
+    put(&p.trace_count, sizeof p.trace_count);
+    put(&p.trace_idx, sizeof p.trace_idx);
+    const bool same = sp == nullptr;
+    put(&same, sizeof same);
+    return k;
+}
+
+void clear_cache_locked() {
+    for (auto &kv : g_cache)
+        if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    g_cache.clear();
+}
+
+}  // namespace
+
+extern "C" {
+
+cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds, int L, float *x,
+                          float resid_scale, const cs_select_params *params, cs_stack_mode mode,
+                          cs_stream_t s_main, cs_stream_t s_pred, void *ws, size_t ws_bytes,
+                          int32_t *trace_count, int32_t *trace_idx) {
+    if (L < 1 || !layers || !params || !x || (reinterpret_cast<uintptr_t>(x) & 3u)) {
+        set_error("cs_decode_stack: L >= 1, layers, params and x are required");
+        return CS_ERR_INVALID;
+    }
+    if (params->mode != CS_SEL_TOPK && params->mode != CS_SEL_THRESHOLD && params->mode != CS_SEL_EXACT) {
+        set_error("cs_decode_stack: bad selection mode");
+        return CS_ERR_INVALID;
+    }
+    if (mode != CS_STACK_SEQUENTIAL && mode != CS_STACK_LOOKAHEAD) {
+        set_error("cs_decode_stack: bad stack mode");
+        return CS_ERR_INVALID;
+    }
+    const bool exact = params->mode == CS_SEL_EXACT;
+    if (!exact && !preds) {
+        set_error("cs_decode_stack: predictors are required unless the selection is exact");
+        return CS_ERR_INVALID;
+    }
+    const int d = layers[0].d, f = layers[0].f, r = exact ? 1 : preds[0].r;
+    const cs_dtype dt = layers[0].dtype;
+    for (int l = 0; l < L; ++l) {
+        const cs_ffn_layer &Ly = layers[l];
+        const int ld = Ly.ld ? Ly.ld : Ly.d;
+        const size_t es = dtype_size(Ly.dtype);
+        if (Ly.d != d || Ly.f != f || Ly.dtype != dt || ld < d || (ld * es) % 16 ||
+            !Ly.w_gate || !Ly.w_down_t || (reinterpret_cast<uintptr_t>(Ly.w_gate) & 15u) ||
+            (reinterpret_cast<uintptr_t>(Ly.w_down_t) & 15u) || (reinterpret_cast<uintptr_t>(Ly.w_up) & 15u)) {
+            set_error("cs_decode_stack: layer %d has a different shape or an invalid layout", l);
+            return CS_ERR_INVALID;
+        }
+        if (!exact) {
+            const cs_predictor &P = preds[l];
+            const int ldd = P.ld_down ? P.ld_down : P.d, ldu = P.ld_up ? P.ld_up : P.r;
+            const size_t ep = dtype_size(P.dtype);
+            if (P.d != d || P.f != f || P.r != r || !P.p_down || !P.p_up || ldd < d || ldu < r ||
+                (ldd * ep) % 16 || (ldu * ep) % 16 || (reinterpret_cast<uintptr_t>(P.p_down) & 15u) ||
+                (reinterpret_cast<uintptr_t>(P.p_up) & 15u) || P.r > 8192 ||
+                (P.dtype != CS_F32 && P.dtype != CS_F16 && P.dtype != CS_BF16)) {
+                set_error("cs_decode_stack: predictor %d does not match the layers or is invalid", l);
+                return CS_ERR_INVALID;
+            }
+        }
+    }
+    if (d > ffn_max_d(dt) || f > kSelectMaxF) {
+        set_error("cs_decode_stack: d=%d or f=%d beyond the supported maximum", d, f);
+        return CS_ERR_UNSUPPORTED;
+    }
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) {
+        set_error("cs_decode_stack: workspace is null or not 256-byte aligned");
+        return CS_ERR_WORKSPACE;
+    }
+    StackPlan p;
+    p.layers = layers; p.preds = preds; p.L = L; p.d = d; p.f = f; p.r = r;
+    p.x = x; p.scale = resid_scale; p.sel = *params; p.mode = mode;
+    p.ws = static_cast<char *>(ws);
+    p.lay = ws_layout(d, f, r, 1, device_sm_count());
+    p.trace_count = trace_count; p.trace_idx = trace_idx;
+    if (ws_bytes < p.lay.total) {
+        set_error("cs_decode_stack: workspace too small: %zu bytes given, %zu needed", ws_bytes, p.lay.total);
+        return CS_ERR_WORKSPACE;
+    }
+
+    cudaStream_t sm = (cudaStream_t)s_main;
+    cudaStream_t sp = (cudaStream_t)s_pred;
+    const bool two = mode == CS_STACK_LOOKAHEAD && !exact && sp && sp != sm;
+
+    // Caller is capturing: enqueue into the caller's graph.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (sm) {
+        cudaError_t e = cudaStreamIsCapturing(sm, &cap);
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(capture query)");
+    }
+    if (cap == cudaStreamCaptureStatusActive || !sm) {
+        Events E;
+        cudaError_t e = enqueue_stack(p, sm, two ? sp : sm, E);
+        return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_decode_stack(enqueue)");
+    }
+
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const std::string key = plan_key(p, two ? sp : nullptr, dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_cache.find(key);
+    if (it == g_cache.end()) {
+        if (g_cache.size() >= kMaxCached) clear_cache_locked();
+        cudaGraph_t graph = nullptr;
+        cudaError_t e = cudaStreamBeginCapture(sm, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(begin capture)");
+        cudaError_t ee;
+        {
+            Events E;
+            ee = enqueue_stack(p, sm, two ? sp : sm, E);
+            e = cudaStreamEndCapture(sm, &graph);
+        }
+        if (ee != cudaSuccess) {
+            if (graph) cudaGraphDestroy(graph);
+            return cuda_fail(ee, "cs_decode_stack(capture)");
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(end capture)");
+        CacheEntry ce;
+        ce.device = dev;
+        e = cudaGraphInstantiate(&ce.exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(instantiate)");
+        it = g_cache.emplace(key, ce).first;
+    }
+    cudaError_t e = cudaGraphLaunch(it->second.exec, sm);
+    return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_decode_stack(launch)");
+}
+
+cs_status cs_stack_release(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    clear_cache_locked();
+    return CS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,125 @@
+// Batch union of active-neuron masks, and the neuron-major layout packer.
+//
+// Union source: "Contextual Sparsity and Activation Predictors", section "When
+// it breaks": the tokens of a batch have different active sets and the layer
+// must read their union.  umask = OR over tokens; uidx = set bits ascending.
+// One CTA: each thread ORs a contiguous run of words, a block scan places the
+// run's ids.
+//
+// Packer source: "Contextual Sparsity: Activation-Aware LLM Inference and the
+// Deja Vu Paradigm", section "Kernel-Level Implementation" (indexing into the
+// row-major down projection breaks coalescing): W_down [d, f] is transposed
+// to neuron-major rows, 32x32 tiles through shared memory.
+#include <utility>
+
+#include "cs_internal.cuh"
+
+namespace cs {
+
+namespace {
+
+constexpr int kUnionThreads = 1024;
+
+__global__ void __launch_bounds__(kUnionThreads)
+union_kernel(const uint32_t *__restrict__ masks, int B, int f, uint32_t *__restrict__ umask,
+             int32_t *__restrict__ uidx, int32_t *__restrict__ ucount) {
+    __shared__ int wsum[32];
+    const int tid = threadIdx.x;
+    const int words = (f + 31) >> 5;
+    const int E = (words + kUnionThreads - 1) / kUnionThreads;
+    const int beg = min(tid * E, words), end = min(beg + E, words);
+    const uint32_t tail = (f & 31) ? ((1u << (f & 31)) - 1u) : 0xffffffffu;
+    pdl_wait();
+    int n = 0;
+    for (int w = beg; w < end; ++w) {
+        uint32_t u = 0;
+        for (int b = 0; b < B; ++b) u |= masks[(size_t)b * words + w];
+        if (w == words - 1) u &= tail;
+        n += __popc(u);
+    }
+    int total;
+    int pos = block_excl_scan(n, wsum, &total);
+    for (int w = beg; w < end; ++w) {
+        uint32_t u = 0;
+        for (int b = 0; b < B; ++b) u |= masks[(size_t)b * words + w];
+        if (w == words - 1) u &= tail;
+        umask[w] = u;
+        while (u) {
+            const int bit = __ffs(u) - 1;
+            uidx[pos++] = w * 32 + bit;
+            u &= u - 1;
+        }
+    }
+    if (tid == 0) *ucount = total;
+}
+
+template <typename S> __device__ __forceinline__ float load_as_float(const void *p, size_t i);
+template <> __device__ __forceinline__ float load_as_float<float>(const void *p, size_t i) {
+    return static_cast<const float *>(p)[i];
+}
+template <> __device__ __forceinline__ float load_as_float<__half>(const void *p, size_t i) {
+    return __half2float(static_cast<const __half *>(p)[i]);
+}
+template <> __device__ __forceinline__ float load_as_float<__nv_bfloat16>(const void *p, size_t i) {
+    return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
+}
+
+template <typename D> __device__ __forceinline__ void store_from_float(void *p, size_t i, float v);
+template <> __device__ __forceinline__ void store_from_float<float>(void *p, size_t i, float v) {
+    static_cast<float *>(p)[i] = v;
+}
+template <> __device__ __forceinline__ void store_from_float<__half>(void *p, size_t i, float v) {
+    static_cast<__half *>(p)[i] = __float2half_rn(v);
+}
+template <> __device__ __forceinline__ void store_from_float<__nv_bfloat16>(void *p, size_t i, float v) {
+    static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
+}
+
+template <typename S, typename D>
+__global__ void __launch_bounds__(256)
+transpose_kernel(const void *__restrict__ src, int rows, int cols, int ld_src, void *__restrict__ dst,
+                 int ld_dst) {
+    __shared__ float tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    pdl_wait();
+    for (int yy = ty; yy < 32; yy += 8) {
+        const int r = r0 + yy, c = c0 + tx;
+        tile[yy][tx] = (r < rows && c < cols) ? load_as_float<S>(src, (size_t)r * ld_src + c) : 0.f;
+    }
+    __syncthreads();
+    for (int yy = ty; yy < 32; yy += 8) {
+        const int c = c0 + yy, r = r0 + tx;  // dst row = source column
+        if (c < cols && r < rows) store_from_float<D>(dst, (size_t)c * ld_dst + r, tile[tx][yy]);
+    }
+}
+
+template <typename S>
+cudaError_t pick_dst(const void *src, int rows, int cols, int ld_src, void *dst, cs_dtype dt, int ld_dst,
+                     cudaStream_t s) {
+    dim3 g((cols + 31) / 32, (rows + 31) / 32);
+    const bool pdl = pdl_enabled();
+    switch (dt) {
+    case CS_F32: return launch(transpose_kernel<S, float>, g, dim3(256), 0, s, pdl, src, rows, cols, ld_src, dst, ld_dst);
+    case CS_F16: return launch(transpose_kernel<S, __half>, g, dim3(256), 0, s, pdl, src, rows, cols, ld_src, dst, ld_dst);
+    default: return launch(transpose_kernel<S, __nv_bfloat16>, g, dim3(256), 0, s, pdl, src, rows, cols, ld_src, dst, ld_dst);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_union(const UnionArgs &a, cudaStream_t s) {
+    return launch(union_kernel, dim3(1), dim3(kUnionThreads), 0, s, pdl_enabled(), a.masks, a.B, a.f,
+                  a.umask, a.uidx, a.ucount);
+}
+
+cudaError_t launch_transpose(const void *src, cs_dtype st, int rows, int cols, int ld_src, void *dst,
+                             cs_dtype dt, int ld_dst, cudaStream_t s) {
+    switch (st) {
+    case CS_F32: return pick_dst<float>(src, rows, cols, ld_src, dst, dt, ld_dst, s);
+    case CS_F16: return pick_dst<__half>(src, rows, cols, ld_src, dst, dt, ld_dst, s);
+    default: return pick_dst<__nv_bfloat16>(src, rows, cols, ld_src, dst, dt, ld_dst, s);
+    }
+}
+
+}  // namespace cs

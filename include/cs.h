@@ -1,0 +1,241 @@
+/*
+ * cs.h -- C ABI of the contextual-sparsity sparse FFN library (GB300, sm_103a).
+ *
+ * The method (sources are web pages, cited by title and section):
+ *  [P1] "Contextual Sparsity and Activation Predictors"
+ *  [P2] "Contextual Sparsity: Activation-Aware LLM Inference and the Deja Vu
+ *       Paradigm"
+ *  [P3] "Activation sparsity" (wikillm concept page)
+ *
+ * A per-layer low-rank predictor scores every FFN neuron; a top-k or threshold
+ * selection turns the scores into an ascending list of active neurons; only
+ * those neurons' gate (and up) rows and their columns of W_down are read:
+ *     y = sum_{j in A} relu(w_gate_j . x + b_j) * (w_up_j . x) * W_down[:, j].
+ *
+ * Conventions for every call
+ *  - Pointers named as device buffers must be device memory of the current
+ *    CUDA device (cudaMalloc / torch).  Struct headers are host memory.  The
+ *    caller owns every buffer; the library allocates nothing on these calls.
+ *  - Calls are asynchronous and stream-ordered on the stream given (NULL =
+ *    legacy default stream).  CS_OK means "validated and enqueued".
+ *  - Argument errors are reported synchronously and nothing is enqueued.
+ *    Errors found on the device (an index out of range, a bad count) set bits
+ *    in the workspace error word (see cs_get_device_error); the kernels skip
+ *    or clamp the offending item instead of dereferencing it.
+ *  - Weights are neuron-major: row j of w_gate, w_up and w_down_t belongs to
+ *    neuron j (w_down_t is W_down transposed, so each neuron's down vector is
+ *    a contiguous row).  Rows have a stride of `ld` elements; ld * elem_size
+ *    must be a multiple of 16 bytes and every base pointer 16-byte aligned.
+ *    Padding elements beyond d are never used.
+ *  - x, scores, pre-activations and y are fp32; weights are fp32, fp16 or
+ *    bf16; all dot products accumulate in fp32.
+ *  - No exception crosses this boundary.  Thread safety: calls on different
+ *    workspaces may run concurrently; one workspace serves one stream at a
+ *    time.
+ */
+#ifndef CS_H
+#define CS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *cs_stream_t; /* the same type as cudaStream_t */
+
+typedef enum cs_status {
+    CS_OK = 0,
+    CS_ERR_INVALID = 1,     /* bad argument; nothing was enqueued              */
+    CS_ERR_CUDA = 2,        /* a CUDA runtime call failed (see cs_last_error)  */
+    CS_ERR_UNSUPPORTED = 3, /* valid, but outside what this build handles      */
+    CS_ERR_TIMEOUT = 4,     /* a bounded device wait gave up                   */
+    CS_ERR_WORKSPACE = 5    /* workspace missing, misaligned or too small      */
+} cs_status;
+
+/* Bits of the device error word (cs_get_device_error). */
+#define CS_DEVERR_INDEX   0x1u /* a neuron id outside [0, f) was skipped        */
+#define CS_DEVERR_COUNT   0x2u /* a count outside [0, f] was clamped            */
+#define CS_DEVERR_TIMEOUT 0x4u /* a bounded wait inside a kernel gave up        */
+
+typedef enum cs_dtype { CS_F32 = 0, CS_F16 = 1, CS_BF16 = 2 } cs_dtype;
+
+typedef enum cs_sel_mode {
+    CS_SEL_TOPK = 0,      /* the k best scores, lower id wins ties [P2 "The Prediction Problem"] */
+    CS_SEL_THRESHOLD = 1, /* scores >= tau [P3 "Implementation sketch", predict_active]          */
+    CS_SEL_EXACT = 2      /* gate pre-activation > 0, no predictor [P1, first section]           */
+} cs_sel_mode;
+
+typedef enum cs_stack_mode {
+    CS_STACK_SEQUENTIAL = 0, /* layer l's set predicted from x_l                             */
+    CS_STACK_LOOKAHEAD = 1   /* layer l+1's set predicted from x_l on a second stream [P1]    */
+} cs_stack_mode;
+
+/*
+ * Low-rank predictor of one layer, [P2] "The Prediction Problem"
+ * (SparsityPredictor): scores = P_up relu(P_down x), both maps bias-free.
+ * The page's final sigmoid is monotone and is not applied: scores are logits.
+ *   p_down: [r, ld_down] device, row i = i-th bottleneck unit (ld_down >= d)
+ *   p_up:   [f, ld_up]   device, row j = neuron j (ld_up >= r)
+ * ld_* = 0 means dense rows (d and r).
+ */
+typedef struct cs_predictor {
+    int d, r, f;
+    cs_dtype dtype;
+    int ld_down, ld_up;
+    const void *p_down;
+    const void *p_up;
+} cs_predictor;
+
+/*
+ * One FFN layer, neuron-major.  w_up == NULL gives the ReLU FFN
+ * (a_j = relu(g_j)); otherwise the ReLUfied gated FFN of [P2] "The SiLU/GELU
+ * Challenge: TurboSparse" (a_j = relu(g_j) * (w_up_j . x)).  g_j = w_gate_j . x
+ * + bias_j (bias may be NULL).  All three matrices share dtype and ld.
+ */
+typedef struct cs_ffn_layer {
+    int d, f;
+    cs_dtype dtype;
+    int ld;
+    const void *w_gate;   /* [f, ld] device                       */
+    const void *w_up;     /* [f, ld] device or NULL               */
+    const void *w_down_t; /* [f, ld] device; row j = W_down[:, j] */
+    const float *bias;    /* [f] device fp32 or NULL              */
+} cs_ffn_layer;
+
+/* Selection: k for CS_SEL_TOPK (clamped to [0, f]); tau for CS_SEL_THRESHOLD. */
+typedef struct cs_select_params {
+    cs_sel_mode mode;
+    int k;
+    float tau;
+} cs_select_params;
+
+/* ------------------------------------------------------------ utilities */
+
+const char *cs_version(void);
+const char *cs_status_string(cs_status s);
+/* Text of the last error on this host thread ("" if none). */
+const char *cs_last_error(void);
+
+/*
+ * Workspace bytes for calls with model width d, f neurons, predictor rank r
+ * and up to B tokens per call, on the current device (the size depends on its
+ * SM count).  One workspace serves every call below, including
+ * cs_decode_stack.  The workspace is caller-owned device memory, 256-byte
+ * aligned, and must be initialised once with cs_workspace_init.
+ */
+size_t cs_workspace_size(int d, int f, int r, int B);
+cs_status cs_workspace_init(void *ws, size_t ws_bytes, cs_stream_t stream);
+
+/*
+ * Reads (and with clear != 0 also resets) the device error word.  Waits for
+ * `stream`; this is the only call that synchronises.
+ */
+cs_status cs_get_device_error(void *ws, cs_stream_t stream, int clear, uint32_t *code_out);
+
+/*
+ * Layout step: dst[c, r] = src[r, c] with dtype conversion (round to nearest
+ * even).  Turns a user's W_down [d, f] into w_down_t [f, ld_dst].  src is
+ * [rows, ld_src], dst is [cols, ld_dst]; both device.  Neuron-major rows
+ * keep each neuron's data contiguous ([P2] "Kernel-Level Implementation":
+ * indexing into row-major weights breaks coalescing).
+ */
+cs_status cs_pack_transpose(const void *src, cs_dtype src_dtype, int rows, int cols, int ld_src,
+                            void *dst, cs_dtype dst_dtype, int ld_dst, cs_stream_t stream);
+
+/* ------------------------------------------------------------- hot path */
+
+/*
+ * Predictor, [P2] "The Prediction Problem": scores[b, j] = sum_i P_up[j, i] *
+ * relu(sum_t P_down[i, t] x[b, t]).
+ *   x:      [B, d] fp32 device;   scores: [B, f] fp32 device (output).
+ * B >= 1.
+ */
+cs_status cs_predict(const cs_predictor *pred, const float *x, int B, float *scores,
+                     void *ws, size_t ws_bytes, cs_stream_t stream);
+
+/*
+ * Selection per token row, [P2] "The Prediction Problem" (top-k) and [P3]
+ * "Implementation sketch" (threshold).
+ *   scores: [B, f] fp32 device.
+ *   idx:    [B, f] int32 device (output): row b holds count[b] ascending ids.
+ *   count:  [B] int32 device (output).
+ *   mask:   [B, ceil(f/32)] uint32 device or NULL (output): bit j%32 of word
+ *           j/32 set iff j selected.
+ * TOPK: the min(k, f) best scores; higher score first, equal scores by lower
+ * id, -0 == +0, NaN below every number.  THRESHOLD: {j : s_j >= tau}, NaN
+ * never passes.  mode CS_SEL_EXACT is not a score selection: use
+ * cs_exact_ffn.  f <= 65536.
+ */
+cs_status cs_select(const float *scores, int B, int f, const cs_select_params *params,
+                    int32_t *idx, int32_t *count, uint32_t *mask,
+                    void *ws, size_t ws_bytes, cs_stream_t stream);
+
+/*
+ * Gathered sparse FFN, [P2] "The Prediction Problem" (sparse_mlp_forward):
+ * for every token b, y[b] = sum_{m < count} a_{b, idx[m]} * w_down_t[idx[m], :]
+ * with a_{b,j} = relu(w_gate_j . x_b + bias_j) (* w_up_j . x_b).  All B tokens
+ * use the same list (batch union semantics, [P1] "When it breaks").
+ *   x: [B, d] fp32 device;  y: [B, d] fp32 device (output, may not alias x).
+ *   idx: [>= count] int32 device, ascending;  count: int32 device scalar.
+ * The list stays on the device; no host synchronisation.  The reduction over
+ * neurons runs in a fixed order, so results are bit-reproducible.
+ */
+cs_status cs_sparse_ffn(const cs_ffn_layer *layer, const float *x, int B, const int32_t *idx,
+                        const int32_t *count, float *y, void *ws, size_t ws_bytes,
+                        cs_stream_t stream);
+
+/*
+ * Exact-mask FFN for one token ([P1] first section: knowing which neurons are
+ * inactive means computing every gate row).  Computes all pre-activations
+ * g_j = w_gate_j . x + bias_j, selects A = {j : g_j > 0}, then
+ * y = sum_{j in A} relu(g_j) (* w_up_j . x) w_down_t[j, :].
+ *   preact: [f] fp32 device (output);  idx: [f] int32 device (output);
+ *   count: int32 device (output);  mask: [ceil(f/32)] uint32 device or NULL;
+ *   y: [d] fp32 device (output).
+ */
+cs_status cs_exact_ffn(const cs_ffn_layer *layer, const float *x, float *preact, int32_t *idx,
+                       int32_t *count, uint32_t *mask, float *y,
+                       void *ws, size_t ws_bytes, cs_stream_t stream);
+
+/*
+ * Batch union, [P1] "When it breaks": umask = OR of the B token masks;
+ * uidx = its set bits ascending; ucount = |U|.
+ *   masks: [B, ceil(f/32)] uint32 device;  umask: [ceil(f/32)] uint32 device;
+ *   uidx: [f] int32 device;  ucount: int32 device scalar.
+ * Bits at positions >= f in the last word are ignored.
+ */
+cs_status cs_union_mask(const uint32_t *masks, int B, int f, uint32_t *umask, int32_t *uidx,
+                        int32_t *ucount, void *ws, size_t ws_bytes, cs_stream_t stream);
+
+/*
+ * Layer stack on the residual stream, [P1] "The predictor and its budget":
+ * x_{l+1} = x_l + resid_scale * FFN_l(x_l, A_l) for l = 0..L-1, batch 1.
+ *   SEQUENTIAL: A_l = select(P_l(x_l)).
+ *   LOOKAHEAD:  A_l = select(P_l(x_{l-1})) (A_0 from x_0): the predictor and
+ *               selection of layer l+1 run on s_pred while layer l's FFN runs
+ *               on s_main.
+ *   params->mode == CS_SEL_EXACT: A_l = {j : g_j > 0} at x_l; preds unused.
+ *   x: [d] fp32 device, input x_0 and output x_L.
+ *   layers, preds: host arrays of L structs (same d, f, r and dtype).
+ *   trace_count: [L] int32 device or NULL; trace_idx: [L, f] int32 device or
+ *   NULL -- per-layer selected counts and ascending ids.
+ * The whole sequence is captured into a CUDA graph on the first call for a
+ * given set of arguments and replayed afterwards (unless s_main is already
+ * capturing, in which case the kernels are enqueued into the caller's
+ * capture).  The workspace must hold cs_workspace_size(d, f, r, 1) bytes.
+ */
+cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds, int L, float *x,
+                          float resid_scale, const cs_select_params *params, cs_stack_mode mode,
+                          cs_stream_t s_main, cs_stream_t s_pred, void *ws, size_t ws_bytes,
+                          int32_t *trace_count, int32_t *trace_idx);
+
+/* Drops every cached stack graph (waits for nothing; call when idle). */
+cs_status cs_stack_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CS_H */

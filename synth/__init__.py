@@ -124,9 +124,10 @@ def storage_to_f64(a: np.ndarray, dtype: int) -> np.ndarray:
     return np.asarray(a).astype(np.float64)
 
 
-def normal_matrix(seed: int, tid: int, rows: int, cols: int, std: float, dtype: int,
-                  row_ids=None, chunk: int = 1 << 22) -> np.ndarray:
-    """Rows of a [rows, cols] N(0, std^2) tensor in storage dtype.
+def normal_matrix_np(seed: int, tid: int, rows: int, cols: int, std: float, dtype: int,
+                     row_ids=None, chunk: int = 1 << 22) -> np.ndarray:
+    """Rows of a [rows, cols] N(0, std^2) tensor in storage dtype (numpy, the
+    readable definition; ``normal_matrix`` is the fast C twin).
 
     ``row_ids`` selects a subset of rows (default all); the values of a row do
     not depend on which other rows are drawn.
@@ -265,3 +266,67 @@ def bool_from_bits(words: np.ndarray, f: int) -> np.ndarray:
 def ceil_k(f: int, frac: float) -> int:
     """k for an active share: ceil(frac * f) (recall-first rounding)."""
     return int(math.ceil(frac * f - 1e-9))
+
+
+# ----------------------------------------------------------------------------
+# fast host twin (synth_host.c, gcc + OpenMP)
+# ----------------------------------------------------------------------------
+import ctypes as _C
+import os as _os
+import subprocess as _sp
+import threading as _th
+
+_HERE = _os.path.dirname(_os.path.abspath(__file__))
+_HOST_SRC = _os.path.join(_HERE, "synth_host.c")
+_HOST_LIB = _os.path.join(_HERE, "_build", "libsynthhost.so")
+_host_lock = _th.Lock()
+_host = None
+
+
+def build_host(force: bool = False) -> str:
+    _os.makedirs(_os.path.dirname(_HOST_LIB), exist_ok=True)
+    if (not force and _os.path.exists(_HOST_LIB)
+            and _os.path.getmtime(_HOST_LIB) >= _os.path.getmtime(_HOST_SRC)):
+        return _HOST_LIB
+    tmp = _HOST_LIB + f".tmp{_os.getpid()}"
+    _sp.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+             _HOST_SRC, "-o", tmp], check=True)
+    _os.replace(tmp, _HOST_LIB)
+    return _HOST_LIB
+
+
+def _host_lib():
+    global _host
+    with _host_lock:
+        if _host is None:
+            L = _C.CDLL(build_host())
+            L.synth_host_fill.argtypes = [_C.c_void_p, _C.c_int, _C.c_void_p, _C.c_int64,
+                                          _C.c_int64, _C.c_int64, _C.c_uint64, _C.c_float]
+            L.synth_host_fill.restype = None
+            L.synth_host_key.argtypes = [_C.c_uint64, _C.c_uint64]
+            L.synth_host_key.restype = _C.c_uint64
+            _host = L
+    return _host
+
+
+_NP_DT = {F32: np.float32, F16: np.float16, BF16: np.uint16}
+
+
+def normal_matrix(seed: int, tid: int, rows: int, cols: int, std: float, dtype: int,
+                  row_ids=None, ld: int | None = None) -> np.ndarray:
+    """Same values as ``normal_matrix_np`` (C twin): rows of a [rows, cols]
+    N(0, std^2) tensor, optionally padded with zero columns to ``ld``."""
+    ld = cols if ld is None else int(ld)
+    if row_ids is None:
+        ids = None
+        n = rows
+    else:
+        ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+        if ids.size and (ids.min() < 0 or ids.max() >= rows):
+            raise IndexError("row id out of range")
+        n = ids.size
+    out = np.empty((n, ld), dtype=_NP_DT[dtype])
+    key = int(stream_key(seed, tid))
+    _host_lib().synth_host_fill(out.ctypes.data, int(dtype), None if ids is None else ids.ctypes.data,
+                                n, int(cols), ld, key, float(weight_scale(std)))
+    return out

@@ -1,0 +1,127 @@
+"""Shared helpers for the GPU parity tests: build the same synthetic layer on
+the host (oracle inputs, from synth's C twin) and on the device (uploaded),
+and compare results."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+import synth
+
+TOL = 2e-3  # max |gpu - oracle| / max |oracle| on scores and y
+
+
+def rel_err(gpu, ref):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.abs(ref).max()
+    if den == 0:
+        return float(np.abs(gpu).max())
+    return float(np.abs(gpu - ref).max() / den)
+
+
+def torch_dtype(dt):
+    import torch
+    return {synth.F32: torch.float32, synth.F16: torch.float16, synth.BF16: torch.bfloat16}[dt]
+
+
+def upload(arr, dt):
+    """numpy storage array -> CUDA tensor of the storage dtype."""
+    import torch
+    if dt == synth.BF16:
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
+
+
+def pad_ld(d, dt):
+    """Smallest row stride >= d whose byte size is a multiple of 16."""
+    per = 16 // synth.DTYPE_BYTES[dt]
+    return (d + per - 1) // per * per
+
+
+class HostLayer:
+    """One synthetic layer + predictor, as host arrays (storage form)."""
+
+    def __init__(self, d, f, r, dt, glu=False, seed=0, layer=0, rho=0.1, ld=None, bias=True):
+        self.d, self.f, self.r, self.dt, self.glu = d, f, r, dt, glu
+        self.ld = ld or pad_ld(d, dt)
+        self.ldr = pad_ld(r, dt) if r else 0
+        sd = 1 / math.sqrt(d)
+        mk = lambda w, rows, cols, ld: synth.normal_matrix(seed, synth.tensor_id(layer, w), rows, cols, sd, dt, ld=ld)
+        self.w_gate = mk(synth.W_GATE, f, d, self.ld)
+        self.w_down_t = mk(synth.W_DOWN_T, f, d, self.ld)
+        self.w_up = mk(synth.W_UP, f, d, self.ld) if glu else None
+        self.bias = synth.zipf_bias(seed, layer, f, rho) if bias else None
+        if r:
+            self.p_down = mk(synth.P_DOWN, r, d, self.ld)
+            self.p_up = mk(synth.P_UP, f, r, self.ldr)
+
+    def oracle_layer(self):
+        return oracle.Layer(self.d, self.f, self.dt, self.w_gate, self.w_down_t, w_up=self.w_up,
+                            bias=self.bias, ld=self.ld)
+
+    def oracle_pred(self):
+        return oracle.Predictor(self.d, self.r, self.f, self.dt, self.p_down, self.p_up,
+                                ld_down=self.ld, ld_up=self.ldr)
+
+    def device(self):
+        import torch
+        import contextual_sparsity_sparse_gb300 as cs
+        t = {k: upload(getattr(self, k), self.dt) for k in ("w_gate", "w_down_t")}
+        t["w_up"] = upload(self.w_up, self.dt) if self.glu else None
+        t["bias"] = torch.from_numpy(self.bias).cuda() if self.bias is not None else None
+        layer = cs.FfnLayer(t["w_gate"], t["w_down_t"], w_up=t["w_up"], bias=t["bias"], d=self.d)
+        pred = None
+        if self.r:
+            pd, pu = upload(self.p_down, self.dt), upload(self.p_up, self.dt)
+            pred = cs.Predictor(pd, pu, d=self.d)
+            pred.keep = (pd, pu)
+        layer.keep = t
+        return layer, pred
+
+
+def score_bounds(P: HostLayer, x):
+    """Oracle scores and a bound on |fp32 GPU score - exact score|.
+
+    The GPU sums every dot product in fp32 along chains of at most ~64
+    dependent roundings (per-thread runs, warp shuffles, a fixed cross-warp
+    order), so |error| <= 64 u sum|terms| per GEMV (u = 2^-24), plus the
+    propagated bottleneck error, plus the final fp32 rounding of the score.
+    """
+    x = np.asarray(x, np.float64)
+    pd = synth.storage_to_f64(P.p_down, P.dt)[:, :P.d]
+    pu = synth.storage_to_f64(P.p_up, P.dt)[:, :P.r]
+    h, s = oracle.predict(P.oracle_pred(), x)
+    g = 64 * 2.0 ** -24
+    dh = g * (np.abs(pd) @ np.abs(x))
+    eps = g * (np.abs(pu) @ np.abs(h)) + np.abs(pu) @ dh + 2.0 ** -24 * np.abs(s)
+    return s, eps
+
+
+def pick_k_with_gap(s, eps, k0, span=64):
+    """A k near k0 whose boundary is decided beyond rounding: the k-th and
+    (k+1)-th largest scores differ by more than both error bounds."""
+    order = np.argsort(-s, kind="stable")
+    for dk in range(span):
+        for k in (k0 + dk, k0 - dk):
+            if 0 < k < s.size:
+                a, b = order[k - 1], order[k]
+                if s[a] - s[b] > eps[a] + eps[b]:
+                    return k
+    raise AssertionError("no decidable k near k0")
+
+
+def pick_tau_with_gap(s, eps, q):
+    """A threshold near the q-quantile with no score within its error bound."""
+    srt = np.sort(s)
+    i0 = int(q * s.size)
+    order = np.argsort(s, kind="stable")
+    for di in range(s.size):
+        for i in (i0 + di, i0 - di):
+            if 0 < i < s.size:
+                lo, hi = order[i - 1], order[i]
+                if s[hi] - s[lo] > 2 * (eps[lo] + eps[hi]):
+                    return np.float32((s[lo] + s[hi]) / 2)
+    raise AssertionError("no decidable threshold")

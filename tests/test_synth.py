@@ -64,3 +64,17 @@ def test_ceil_k():
     assert synth.ceil_k(2048, 0.10) == 205
     assert [synth.ceil_k(20480, r) for r in (0.05, 0.10, 0.20)] == [1024, 2048, 4096]
     assert synth.ceil_k(28672, 0.10) == 2868 and synth.ceil_k(28672, 0.15) == 4301
+
+
+def test_c_twin_matches_numpy_definition():
+    rng = np.random.default_rng(7)
+    for dt in (synth.F32, synth.F16, synth.BF16):
+        for rows, cols in ((1, 1), (37, 53), (8, 512)):
+            a = synth.normal_matrix_np(11, 3, rows, cols, 0.7, dt)
+            b = synth.normal_matrix(11, 3, rows, cols, 0.7, dt)
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+        ids = rng.integers(0, 400, size=17)
+        a = synth.normal_matrix_np(2, 9, 400, 72, 0.1, dt, row_ids=ids)
+        b = synth.normal_matrix(2, 9, 400, 72, 0.1, dt, row_ids=ids, ld=80)
+        assert np.array_equal(a.view(np.uint8), b[:, :72].copy().view(np.uint8))
+        assert not b[:, 72:].view(np.uint8).any()
