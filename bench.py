@@ -203,7 +203,7 @@ def run_ours(args, W, rank, world):
         layer, pred, _ = copies[i % NCOPY]
         x = X[i % NX: i % NX + 1]
         cs.cs_predict(pred, x, scores, ws, stream=s)
-        cs.cs_select(scores, params, idx, cnt, stream=s)
+        cs.cs_select(scores, params, idx, cnt, ws=ws, stream=s)
         if with_events is not None:
             with_events[0].record(s)
         cs.cs_sparse_ffn(layer, x, idx, cnt, Y[i % NX: i % NX + 1], ws, stream=s)
@@ -284,7 +284,7 @@ def run_ours(args, W, rank, world):
         layer, pred, _ = copies[i % NCOPY]
         xd.copy_(xh[i % 64: i % 64 + 1], non_blocking=True)
         cs.cs_predict(pred, xd, scores, ws, stream=s)
-        cs.cs_select(scores, params, idx, cnt, stream=s)
+        cs.cs_select(scores, params, idx, cnt, ws=ws, stream=s)
         cs.cs_sparse_ffn(layer, xd, idx, cnt, yd, ws, stream=s)
         yh[i % 64: i % 64 + 1].copy_(yd, non_blocking=True)
 

@@ -56,7 +56,7 @@ WsLayout ws_layout(int d, int f, int r, int B, int num_sms) {
     WsLayout L;
     L.G = num_sms > 0 ? num_sms : 1;
     L.dp = (d + 7) & ~7;
-    size_t off = 256;
+    size_t off = kControlBytes;
     L.err = 0;
     L.part = off;      off += align256(sizeof(float) * (size_t)L.G * B * L.dp);
     L.h = off;         off += align256(sizeof(float) * (size_t)B * r);
@@ -112,6 +112,10 @@ cs_status check_layer(const cs_ffn_layer *L, int *ld_out) {
     CS_CHECK(L->w_gate && L->w_down_t, "layer: w_gate and w_down_t are required");
     CS_CHECK(al16(L->w_gate) && al16(L->w_down_t) && al16(L->w_up), "layer: weights must be 16-byte aligned");
     CS_CHECK(!L->bias || al4(L->bias), "layer: bias must be 4-byte aligned");
+    if (L->f > 2048 * (device_sm_count() > 0 ? device_sm_count() : 1)) {
+        set_error("layer: f=%d exceeds the supported maximum (2048 per SM)", L->f);
+        return CS_ERR_UNSUPPORTED;
+    }
     if (L->d > ffn_max_d(L->dtype)) {
         set_error("layer: d=%d exceeds the supported maximum %d", L->d, ffn_max_d(L->dtype));
         return CS_ERR_UNSUPPORTED;
@@ -169,7 +173,11 @@ cs_status cs_workspace_init(void *ws, size_t ws_bytes, cs_stream_t stream) {
         set_error("workspace is null, misaligned or smaller than 256 bytes");
         return CS_ERR_WORKSPACE;
     }
-    cudaError_t e = cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream);
+    if (ws_bytes < kControlBytes) {
+        set_error("workspace smaller than its control region (%zu bytes)", kControlBytes);
+        return CS_ERR_WORKSPACE;
+    }
+    cudaError_t e = cudaMemsetAsync(ws, 0, kControlBytes, (cudaStream_t)stream);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_workspace_init");
 }
 
@@ -217,6 +225,7 @@ cs_status cs_predict(const cs_predictor *pred, const float *x, int B, float *sco
     a.x = x;
     a.h = reinterpret_cast<float *>(static_cast<char *>(ws) + L.h);
     a.scores = scores;
+    a.err = static_cast<uint32_t *>(ws);
     cudaError_t e = launch_predict(a, (cudaStream_t)stream);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_predict");
 }
@@ -289,6 +298,7 @@ cs_status cs_exact_ffn(const cs_ffn_layer *layer, const float *x, float *preact,
     PreactArgs p;
     p.d = layer->d; p.f = layer->f; p.ld = ld; p.dtype = layer->dtype;
     p.w_gate = layer->w_gate; p.bias = layer->bias; p.x = x; p.pre = preact;
+    p.err = static_cast<uint32_t *>(ws);
     cudaError_t e = launch_preact(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "cs_exact_ffn(preact)");
     SelectArgs sa;

@@ -1,25 +1,28 @@
-// Gathered sparse FFN (gate GEMV + activation + down AXPY) and the dense
-// pre-activation GEMV of exact-mask mode.
+// Gathered sparse FFN: gate GEMV + activation + down AXPY over the listed
+// neurons, and the fixed-order reduction of the per-CTA partial sums.
 //
 // Sources: "Contextual Sparsity: Activation-Aware LLM Inference and the Deja
 // Vu Paradigm", section "The Prediction Problem" (sparse_mlp_forward: only
 // the chosen neurons' gate rows and down columns are read) and section
-// "Kernel-Level Implementation" (one warp-uncoalesced thread per neuron in the
-// page's sketch; here every row is moved whole and contiguous); section "The
-// SiLU/GELU Challenge: TurboSparse" for the gated form relu(gate x) * up x.
+// "Kernel-Level Implementation" (the page's sketch gives each neuron to one
+// thread, so a warp's loads hit 32 different rows; here every row is read
+// whole and coalesced); section "The SiLU/GELU Challenge: TurboSparse" for the
+// gated form relu(gate x) * up x.
 //
 // Design.  W_down is stored transposed, so each chosen neuron needs two (or
 // three, gated) contiguous rows of d elements.  A persistent grid of one CTA
-// per SM splits the ascending index list into contiguous chunks.  Thread 0 of
-// each CTA streams the chunk's rows into a ring of shared-memory stages with
-// bulk async copies (TMA engine, completion counted on an mbarrier per
-// stage), so up to ~200 KB per SM is in flight with one issuing thread.  The
-// 512 threads own fixed 16-byte column vectors: they dot the staged gate (and
-// up) rows with x held in registers, combine the per-warp sums through shared
-// memory in a fixed order, apply ReLU (and the up factor), and accumulate
-// a_j * w_down_j into per-thread fp32 registers.  Each CTA writes its partial
-// y; a second kernel adds the G partials per column in a fixed order (and
-// applies the residual epilogue), so y is bit-reproducible run to run.
+// per SM splits the ascending index list into contiguous chunks.  Each of the
+// 256 threads owns fixed 16-byte column vectors of every row, and gathers
+// exactly those vectors of the chunk's rows with per-thread asynchronous
+// copies (cp.async) into its own slots of a shared-memory ring, SG groups of
+// NG neurons ahead.  Because a thread only ever reads the slots it filled,
+// the ring needs no barrier; the one cross-thread step is the gate dot
+// product, whose per-warp sums are combined in a fixed order once per group.
+// x stays in registers; a_j * w_down_j accumulates in fp32 registers.  Each
+// CTA writes its partial y; a second kernel adds the G partials per column in
+// a fixed order (and applies the residual epilogue), so y is bit-reproducible.
+// (One-dimensional bulk copies were measured slower for rows of ~10 KB: each
+// costs a fixed ~0.3 us of the SM's copy engine.)
 #include <utility>
 
 #include "cs_internal.cuh"
@@ -28,11 +31,12 @@ namespace cs {
 
 namespace {
 
-constexpr int kFfnThreads = 512;
-constexpr int kFfnWarps = kFfnThreads / 32;
-constexpr int kMaxStages = 16;
-constexpr int kNg = 4;                    // neurons per reduction group (max)
-constexpr size_t kRingBudget = 220 * 1024;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kNgMax = 4;                 // neurons per group (max)
+constexpr int kStageMax = 16;             // ring slots (ng * sg)
+constexpr size_t kRingBudget = 200 * 1024;
+constexpr int kChunkMax = 2048;           // ids per CTA (f <= kChunkMax * grid)
 
 struct FfnK {
     const uint8_t *w_gate, *w_up, *w_down_t;
@@ -42,36 +46,48 @@ struct FfnK {
     uint32_t *err;
     int d, f, B, dp;
     int ldb;        // row pitch in bytes
-    int rb;         // bytes copied per row (d * elem rounded up to 16)
-    int nst;        // ring stages
-    int ng;         // neurons per group (<= kNg, <= nst / 2 when possible)
-    size_t ring_off;
+    int nvec;       // 16-byte vectors per row
+    int ng;         // neurons per group
+    int sg;         // groups in the ring (2 or 3)
 };
 
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
 template <typename T, int TB, bool GLU, bool PRE, int MAXV>
-__global__ void __launch_bounds__(kFfnThreads, 1) ffn_gather_kernel(const FfnK a) {
+__global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
     constexpr int V = Vec<T>::N;
     constexpr int NROW = (PRE ? 0 : 1) + (GLU ? 1 : 0) + 1;
     constexpr bool DOTS = !PRE || GLU;
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    float *red = reinterpret_cast<float *>(smem + 128);  // [warps][kNg][TB][2]
-    int *s_abort = reinterpret_cast<int *>(smem + 128 + sizeof(float) * kFfnWarps * kNg * TB * 2);
-    uint8_t *ring = smem + a.ring_off;
+    extern __shared__ __align__(16) uint4 ring[];  // [slot][NROW][nvec]
+    __shared__ float red[kWarps][kNgMax][TB][2];
+    __shared__ float act[kNgMax][TB];
+    __shared__ float addv[kStageMax];              // bias / pre-activation per slot
+    __shared__ int s_idx[kChunkMax];               // this CTA's ids, staged once
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x, G = gridDim.x;
     const int b0 = blockIdx.y * TB;
-    const int nvec = (a.d + V - 1) / V;
-    const int stage_bytes = NROW * a.rb;
+    const int nvec = a.nvec;
+    const uint32_t row_bytes = (uint32_t)nvec * 16u;
+    const uint32_t slot_bytes = NROW * row_bytes;
+    const uint32_t ring_s = smem_addr(ring);
 
-    if (tid == 0) {
-        for (int s = 0; s < a.nst; ++s) mbar_init(&full[s], 1);
-        *s_abort = 0;
-        mbar_fence_init();
+    // this thread's vectors: byte offsets within a row
+    int voff[MAXV];
+    bool vok[MAXV];
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+        const int v = tid + i * kThreads;
+        vok[i] = v < nvec;
+        voff[i] = v * 16;
     }
-    __syncthreads();
 
+    pdl_launch_dependents();  // one wave: the next kernel may get resident now
     pdl_wait();  // idx, count and x come from earlier kernels
 
     int n = *a.count;
@@ -80,89 +96,114 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_gather_kernel(const FfnK a
         n = n < 0 ? 0 : a.f;
     }
     const int n0 = (int)((long long)n * c / G);
-    const int cnt = (int)((long long)n * (c + 1) / G) - n0;
-    const int32_t *my_idx = a.idx + n0;
-    const uint64_t pol = policy_evict_first();
+    const int cnt = min(kChunkMax, (int)((long long)n * (c + 1) / G) - n0);
+    // stage the chunk's ids so issuing copies never waits on a global load
+    for (int m = tid; m < cnt; m += kThreads) s_idx[m] = __ldg(a.idx + n0 + m);
+    __syncthreads();
+    const int ng = a.ng, sg = a.sg;
+    const int ngroups = (cnt + ng - 1) / ng;
 
-    auto issue = [&](int m) {
-        const int s = m % a.nst;
-        int j = __ldg(my_idx + m);
-        if (j < 0 || j >= a.f) j = 0;  // consumers see the bad id and use a = 0
-        uint8_t *st = ring + (size_t)s * stage_bytes;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-        int r = 0;
-        if (!PRE) bulk_g2s_hint(st + (r++) * a.rb, a.w_gate + (size_t)j * a.ldb, a.rb, &full[s], pol);
-        if (GLU) bulk_g2s_hint(st + (r++) * a.rb, a.w_up + (size_t)j * a.ldb, a.rb, &full[s], pol);
-        bulk_g2s_hint(st + r * a.rb, a.w_down_t + (size_t)j * a.ldb, a.rb, &full[s], pol);
+    // this thread's copies for group g into slots [s0, s0 + ng), plus the
+    // bias of neuron q by lane q of warp 0
+    auto issue = [&](int g, int s0) {
+        if (g < ngroups) {
+            const int gn = min(ng, cnt - g * ng);
+            for (int q = 0; q < gn; ++q) {
+                int j = s_idx[g * ng + q];
+                j = (j >= 0 && j < a.f) ? j : 0;
+                const size_t roff = (size_t)j * (size_t)a.ldb;
+                const uint8_t *gr = a.w_gate + roff;
+                const uint8_t *ur = a.w_up + roff;
+                const uint8_t *dr = a.w_down_t + roff;
+                const uint32_t sb = ring_s + (uint32_t)(s0 + q) * slot_bytes;
+#pragma unroll
+                for (int i = 0; i < MAXV; ++i) {
+                    if (vok[i]) {
+                        uint32_t r = sb + (uint32_t)voff[i];
+                        if (!PRE) { cp16(r, gr + voff[i]); r += row_bytes; }
+                        if (GLU) { cp16(r, ur + voff[i]); r += row_bytes; }
+                        cp16(r, dr + voff[i]);
+                    }
+                }
+                if (warp == 0 && lane == q) {
+                    const float *src = PRE ? a.preact + j : (a.bias ? a.bias + j : nullptr);
+                    if (src) cp4(smem_addr(&addv[s0 + q]), src);
+                    else addv[s0 + q] = 0.f;
+                }
+            }
+        }
+        cp_async_commit();  // always commit, so group counting stays uniform
     };
 
-    int issued = 0;
-    if (tid == 0) {
-        const int first = min(a.nst, cnt);
-        for (int m = 0; m < first; ++m) issue(m);
-        issued = first;
-    }
+    for (int g = 0; g < sg; ++g) issue(g, g * ng);
 
-    // x in registers: thread owns vectors v = tid + i * kFfnThreads
     float xr[TB][MAXV][V];
     float yacc[TB][MAXV][V];
+    const bool xvec = (a.d & 3) == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
 #pragma unroll
     for (int t = 0; t < TB; ++t) {
         const int b = min(b0 + t, a.B - 1);
-        const bool live = b0 + t < a.B;
+        const bool live = DOTS && b0 + t < a.B;
+        const float *xb = a.x + (size_t)b * a.d;
 #pragma unroll
         for (int i = 0; i < MAXV; ++i) {
-            const int v = tid + i * kFfnThreads;
+            const int col0 = (tid + i * kThreads) * V;
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                const int col = v * V + e;
-                xr[t][i][e] = (live && DOTS && v < nvec && col < a.d) ? __ldg(a.x + (size_t)b * a.d + col) : 0.f;
-                yacc[t][i][e] = 0.f;
+            for (int e = 0; e < V; ++e) yacc[t][i][e] = 0.f;
+            if (live && vok[i] && xvec && col0 + V <= a.d) {
+#pragma unroll
+                for (int e = 0; e < V; e += 4) {
+                    const float4 v4 = __ldg(reinterpret_cast<const float4 *>(xb + col0 + e));
+                    xr[t][i][e] = v4.x; xr[t][i][e + 1] = v4.y; xr[t][i][e + 2] = v4.z; xr[t][i][e + 3] = v4.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    xr[t][i][e] = (live && vok[i] && col0 + e < a.d) ? __ldg(xb + col0 + e) : 0.f;
             }
         }
     }
 
-    for (int g0 = 0; g0 < cnt; g0 += a.ng) {
-        const int gn = min(a.ng, cnt - g0);
-        float pg[kNg][TB], pu[kNg][TB];
+    int gs = 0;  // g % sg
+    for (int g = 0; g < ngroups; ++g) {
+        const int gn = min(ng, cnt - g * ng);
+        const int s0 = gs * ng;
+        if (sg == 2) cp_async_wait<1>(); else cp_async_wait<2>();  // group g has landed
+        float pg[kNgMax][TB], pu[kNgMax][TB];
 #pragma unroll
-        for (int q = 0; q < kNg; ++q) {
+        for (int q = 0; q < kNgMax; ++q) {
 #pragma unroll
             for (int t = 0; t < TB; ++t) pg[q][t] = pu[q][t] = 0.f;
-            if (q < gn) {
-                const int m = g0 + q;
-                const int s = m % a.nst;
-                if (!mbar_wait(&full[s], (uint32_t)((m / a.nst) & 1))) {
-                    atomicOr(a.err, CS_DEVERR_TIMEOUT);
-                    *s_abort = 1;
-                }
-                if (DOTS) {
-                    const uint8_t *st = ring + (size_t)s * stage_bytes;
+            if (DOTS && q < gn) {
+                const uint4 *slot = ring + (size_t)(s0 + q) * NROW * nvec;
 #pragma unroll
-                    for (int i = 0; i < MAXV; ++i) {
-                        const int v = tid + i * kFfnThreads;
-                        if (v < nvec) {
-                            const int ne = min(V, a.d - v * V);
-                            if (!PRE) {
-                                float w[V];
-                                unpack<T>(*reinterpret_cast<const uint4 *>(st + v * 16), w);
+                for (int i = 0; i < MAXV; ++i) {
+                    if (vok[i]) {
+                        const int v = tid + i * kThreads;
+                        const int ne = a.d - v * V;  // < V only on a row's last vector
+                        if (!PRE) {
+                            float w[V];
+                            unpack<T>(slot[v], w);
+                            if (ne < V) {
 #pragma unroll
-                                for (int e = 0; e < V; ++e) {
-                                    const float we = e < ne ? w[e] : 0.f;
-#pragma unroll
-                                    for (int t = 0; t < TB; ++t) pg[q][t] = fmaf(we, xr[t][i][e], pg[q][t]);
-                                }
+                                for (int e = 0; e < V; ++e) w[e] = e < ne ? w[e] : 0.f;
                             }
-                            if (GLU) {
-                                float w[V];
-                                unpack<T>(*reinterpret_cast<const uint4 *>(st + (PRE ? 0 : a.rb) + v * 16), w);
 #pragma unroll
-                                for (int e = 0; e < V; ++e) {
-                                    const float we = e < ne ? w[e] : 0.f;
+                            for (int e = 0; e < V; ++e)
 #pragma unroll
-                                    for (int t = 0; t < TB; ++t) pu[q][t] = fmaf(we, xr[t][i][e], pu[q][t]);
-                                }
+                                for (int t = 0; t < TB; ++t) pg[q][t] = fmaf(w[e], xr[t][i][e], pg[q][t]);
+                        }
+                        if (GLU) {
+                            float w[V];
+                            unpack<T>(slot[(PRE ? 0 : 1) * nvec + v], w);
+                            if (ne < V) {
+#pragma unroll
+                                for (int e = 0; e < V; ++e) w[e] = e < ne ? w[e] : 0.f;
                             }
+#pragma unroll
+                            for (int e = 0; e < V; ++e)
+#pragma unroll
+                                for (int t = 0; t < TB; ++t) pu[q][t] = fmaf(w[e], xr[t][i][e], pu[q][t]);
                         }
                     }
                 }
@@ -170,84 +211,72 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_gather_kernel(const FfnK a
         }
         if (DOTS) {
 #pragma unroll
-            for (int q = 0; q < kNg; ++q)
+            for (int q = 0; q < kNgMax; ++q)
 #pragma unroll
                 for (int t = 0; t < TB; ++t) {
                     if (q < gn) {
-                        const float sg = warp_sum(pg[q][t]);
-                        const float su = GLU ? warp_sum(pu[q][t]) : 0.f;
+                        const float sgv = PRE ? 0.f : warp_sum(pg[q][t]);
+                        const float suv = GLU ? warp_sum(pu[q][t]) : 0.f;
                         if (lane == 0) {
-                            red[((warp * kNg + q) * TB + t) * 2 + 0] = sg;
-                            red[((warp * kNg + q) * TB + t) * 2 + 1] = su;
+                            red[warp][q][t][0] = sgv;
+                            red[warp][q][t][1] = suv;
                         }
                     }
                 }
-            __syncthreads();
         }
-        // activations (every thread forms them itself, same fixed order)
-        float act[kNg][TB];
+        __syncthreads();
+        // lane q of warp 0 finishes neuron q (its own bias copy has landed), warps summed in order
+        if (warp == 0 && lane < gn) {
+            const int q = lane;
+            const int j = s_idx[g * ng + q];
+            const bool valid = j >= 0 && j < a.f;
+            const float add = addv[s0 + q];
 #pragma unroll
-        for (int q = 0; q < kNg; ++q) {
+            for (int t = 0; t < TB; ++t) {
+                float gsum = 0.f, usum = 0.f;
+                if (DOTS) {
 #pragma unroll
-            for (int t = 0; t < TB; ++t) act[q][t] = 0.f;
-            if (q < gn) {
-                const int j = __ldg(my_idx + g0 + q);
-                const bool valid = j >= 0 && j < a.f;
-                if (!valid && tid == 0) atomicOr(a.err, CS_DEVERR_INDEX);
-                const int js = valid ? j : 0;
-#pragma unroll
-                for (int t = 0; t < TB; ++t) {
-                    float g = 0.f, u = 0.f;
-                    if (!PRE || GLU) {
-                        for (int w = 0; w < kFfnWarps; ++w) {
-                            g += red[((w * kNg + q) * TB + t) * 2 + 0];
-                            u += red[((w * kNg + q) * TB + t) * 2 + 1];
-                        }
+                    for (int w = 0; w < kWarps; ++w) {
+                        gsum += red[w][q][t][0];
+                        usum += red[w][q][t][1];
                     }
-                    if (PRE) g = __ldg(a.preact + js);
-                    else if (a.bias) g += __ldg(a.bias + js);
-                    float av = fmaxf(g, 0.f);
-                    if (GLU) av *= u;
-                    act[q][t] = valid ? av : 0.f;
                 }
+                const float gv = PRE ? add : gsum + add;
+                float av = fmaxf(gv, 0.f);
+                if (GLU) av *= usum;
+                act[q][t] = valid ? av : 0.f;
             }
+            if (!valid) atomicOr(a.err, CS_DEVERR_INDEX);
         }
+        __syncthreads();
+        float av[kNgMax][TB];
+#pragma unroll
+        for (int q = 0; q < kNgMax; ++q)
+#pragma unroll
+            for (int t = 0; t < TB; ++t) av[q][t] = q < gn ? act[q][t] : 0.f;
         // y += a_j * w_down_j
 #pragma unroll
-        for (int q = 0; q < kNg; ++q) {
+        for (int q = 0; q < kNgMax; ++q) {
             if (q < gn) {
-                const int s = (g0 + q) % a.nst;
-                const uint8_t *dn = ring + (size_t)s * stage_bytes + (NROW - 1) * a.rb;
+                const uint4 *dn = ring + ((size_t)(s0 + q) * NROW + (NROW - 1)) * nvec;
 #pragma unroll
                 for (int i = 0; i < MAXV; ++i) {
-                    const int v = tid + i * kFfnThreads;
-                    if (v < nvec) {
+                    if (vok[i]) {
                         float w[V];
-                        unpack<T>(*reinterpret_cast<const uint4 *>(dn + v * 16), w);
+                        unpack<T>(dn[tid + i * kThreads], w);
 #pragma unroll
                         for (int t = 0; t < TB; ++t)
 #pragma unroll
-                            for (int e = 0; e < V; ++e) yacc[t][i][e] = fmaf(act[q][t], w[e], yacc[t][i][e]);
+                            for (int e = 0; e < V; ++e) yacc[t][i][e] = fmaf(av[q][t], w[e], yacc[t][i][e]);
                     }
                 }
             }
         }
-        __syncthreads();  // stages of this group and red[] are free again
-        if (*s_abort) {
-            if (tid == 0)
-                for (int m = g0 + gn; m < issued; ++m)
-                    mbar_wait(&full[m % a.nst], (uint32_t)((m / a.nst) & 1), 100000000ull);
-            return;
-        }
-        if (tid == 0) {
-            for (int q = 0; q < gn; ++q) {
-                const int m = g0 + q + a.nst;
-                if (m < cnt) { issue(m); issued = m + 1; }
-            }
-        }
+        // this thread's slots of group g are free: refill them with group g + sg
+        issue(g + sg, s0);
+        gs = gs + 1 == sg ? 0 : gs + 1;
     }
-
-    pdl_launch_dependents();
+    cp_async_wait<0>();
 
     // partial y of this CTA
 #pragma unroll
@@ -257,8 +286,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_gather_kernel(const FfnK a
         float *dst = a.part + ((size_t)c * a.B + b) * a.dp;
 #pragma unroll
         for (int i = 0; i < MAXV; ++i) {
-            const int v = tid + i * kFfnThreads;
-            if (v < nvec) {
+            if (vok[i]) {
+                const int v = tid + i * kThreads;
 #pragma unroll
                 for (int e = 0; e < V; e += 4) {
                     float4 o = make_float4(yacc[t][i][e], yacc[t][i][e + 1], yacc[t][i][e + 2], yacc[t][i][e + 3]);
@@ -278,6 +307,7 @@ ffn_reduce_kernel(const float *__restrict__ part, int G, int B, int d, int dp,
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
     const int b = blockIdx.y;
+    pdl_launch_dependents();
     pdl_wait();
     float acc = 0.f;
     if (col < d) {
@@ -297,60 +327,22 @@ ffn_reduce_kernel(const float *__restrict__ part, int G, int B, int d, int dp,
     }
 }
 
-// Exact-mask mode: pre[j] = w_gate_j . x + bias_j for every neuron.
-template <typename T, int RPW>
-__global__ void __launch_bounds__(256)
-preact_kernel(const T *__restrict__ W, int ld, int d, int f, const float *__restrict__ x,
-              const float *__restrict__ bias, float *__restrict__ pre) {
-    constexpr int V = Vec<T>::N;
-    extern __shared__ float xs[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int row0 = (blockIdx.x * 8 + warp) * RPW;
-    const int nvec = (d + V - 1) / V;
-    pdl_wait();
-    for (int i = threadIdx.x; i < nvec * V; i += 256) xs[i] = i < d ? x[i] : 0.f;
-    __syncthreads();
-    float acc[RPW];
-#pragma unroll
-    for (int q = 0; q < RPW; ++q) acc[q] = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-        const int ne = min(V, d - v * V);
-        uint4 raw[RPW];
-#pragma unroll
-        for (int q = 0; q < RPW; ++q) raw[q] = ld_stream(W + (size_t)min(row0 + q, f - 1) * ld + v * V);
-#pragma unroll
-        for (int q = 0; q < RPW; ++q) {
-            float w[V];
-            unpack<T>(raw[q], w);
-#pragma unroll
-            for (int e = 0; e < V; ++e) acc[q] = fmaf(e < ne ? w[e] : 0.f, xs[v * V + e], acc[q]);
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < RPW; ++q) {
-        const float s = warp_sum(acc[q]);
-        const int row = row0 + q;
-        if (lane == 0 && row < f) pre[row] = s + (bias ? bias[row] : 0.f);
-    }
-}
-
-
 template <typename T, int TB, bool GLU, bool PRE, int MAXV>
 cudaError_t run_gather(const FfnArgs &a, FfnK k, size_t smem, cudaStream_t s) {
     auto fn = ffn_gather_kernel<T, TB, GLU, PRE, MAXV>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.G, (a.B + TB - 1) / TB);
-    return launch(fn, grid, dim3(kFfnThreads), smem, s, pdl_enabled(), k);
+    return launch(fn, grid, dim3(kThreads), smem, s, pdl_enabled(), k);
 }
 
 template <typename T, int TB, bool GLU, bool PRE>
 cudaError_t pick_maxv(const FfnArgs &a, const FfnK &k, size_t smem, cudaStream_t s) {
-    constexpr int V = Vec<T>::N;
-    const int nvec = (a.d + V - 1) / V;
-    if (nvec <= kFfnThreads) return run_gather<T, TB, GLU, PRE, 1>(a, k, smem, s);
-    if (nvec <= 2 * kFfnThreads) return run_gather<T, TB, GLU, PRE, 2>(a, k, smem, s);
-    return run_gather<T, TB, GLU, PRE, 4>(a, k, smem, s);
+    if (k.nvec <= kThreads) return run_gather<T, TB, GLU, PRE, 1>(a, k, smem, s);
+    if (k.nvec <= 2 * kThreads) return run_gather<T, TB, GLU, PRE, 2>(a, k, smem, s);
+    if (k.nvec <= 3 * kThreads) return run_gather<T, TB, GLU, PRE, 3>(a, k, smem, s);
+    if (k.nvec <= 4 * kThreads) return run_gather<T, TB, GLU, PRE, 4>(a, k, smem, s);
+    return run_gather<T, TB, GLU, PRE, 8>(a, k, smem, s);
 }
 
 template <typename T, int TB>
@@ -379,17 +371,20 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     k.B = a.B;
     k.dp = a.dp;
     k.ldb = a.ld * esz;
-    k.rb = (a.d * esz + 15) & ~15;
+    k.nvec = (a.d * esz + 15) / 16;
     const int nrow = (a.preact ? 0 : 1) + (a.w_up ? 1 : 0) + 1;
+    const size_t per_neuron = (size_t)nrow * k.nvec * 16;
+    // ring of sg groups of ng neurons: as deep as the budget allows
+    int nst = (int)(kRingBudget / per_neuron);
+    if (nst < 2) return cudaErrorInvalidValue;
+    if (nst >= 3 * kNgMax) { k.ng = kNgMax; k.sg = 3; }
+    else if (nst >= 2 * kNgMax) { k.ng = kNgMax; k.sg = 2; }
+    else if (nst >= 6) { k.ng = 2; k.sg = 3; }
+    else if (nst >= 4) { k.ng = 2; k.sg = 2; }
+    else { k.ng = 1; k.sg = nst >= 3 ? 3 : 2; }
+    static_assert(3 * kNgMax <= kStageMax, "ring slots");
+    const size_t smem = (size_t)k.ng * k.sg * per_neuron;
     const int tb = a.B >= 2 ? 2 : 1;
-    const size_t head = 128 + sizeof(float) * kFfnWarps * kNg * tb * 2 + 16;
-    k.ring_off = (head + 127) & ~size_t(127);
-    int nst = (int)(kRingBudget / ((size_t)nrow * k.rb));
-    nst = nst > kMaxStages ? kMaxStages : nst;
-    if (nst < 1) return cudaErrorInvalidValue;
-    k.nst = nst;
-    k.ng = nst >= 2 * kNg ? kNg : (nst / 2 > 0 ? nst / 2 : 1);
-    const size_t smem = k.ring_off + (size_t)nst * nrow * k.rb;
     cudaError_t e = tb == 2 ? pick_mode<T, 2>(a, k, smem, s) : pick_mode<T, 1>(a, k, smem, s);
     if (e != cudaSuccess) return e;
     dim3 g((a.d + 31) / 32, a.B);
@@ -397,27 +392,12 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
                   static_cast<const float *>(a.part), a.G, a.B, a.d, a.dp, a.resid, a.scale, a.y);
 }
 
-template <typename T>
-cudaError_t run_preact(const PreactArgs &a, cudaStream_t s) {
-    constexpr int RPW = 4;
-    constexpr int V = Vec<T>::N;
-    const int rows_per_cta = 8 * RPW;
-    const size_t smem = sizeof(float) * (size_t)((a.d + V - 1) / V) * V;
-    auto fn = preact_kernel<T, RPW>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    return launch(fn, dim3((a.f + rows_per_cta - 1) / rows_per_cta), dim3(256), smem, s, pdl_enabled(),
-                  static_cast<const T *>(a.w_gate), a.ld, a.d, a.f, a.x, a.bias, a.pre);
-}
-
 }  // namespace
 
 // Largest d (in elements) the gather kernel takes for a dtype.
 int ffn_max_d(cs_dtype t) {
     const int V = t == CS_F32 ? 4 : 8;
-    return 4 * kFfnThreads * V;
+    return 8 * kThreads * V;
 }
 
 cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s) {
@@ -425,14 +405,6 @@ cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s) {
     case CS_F32: return run_ffn<float>(a, s);
     case CS_F16: return run_ffn<__half>(a, s);
     default: return run_ffn<__nv_bfloat16>(a, s);
-    }
-}
-
-cudaError_t launch_preact(const PreactArgs &a, cudaStream_t s) {
-    switch (a.dtype) {
-    case CS_F32: return run_preact<float>(a, s);
-    case CS_F16: return run_preact<__half>(a, s);
-    default: return run_preact<__nv_bfloat16>(a, s);
     }
 }
 

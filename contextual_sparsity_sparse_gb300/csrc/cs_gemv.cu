@@ -1,0 +1,232 @@
+// Streaming GEMVs over contiguous weight rows: the predictor's two maps and
+// the exact-mask pre-activations.
+//
+// Sources: "Contextual Sparsity: Activation-Aware LLM Inference and the Deja
+// Vu Paradigm", section "The Prediction Problem" (SparsityPredictor: a
+// bias-free down map to a small bottleneck, ReLU, a bias-free up map to one
+// score per neuron; the closing sigmoid is monotone and not applied, so scores
+// are logits); "Contextual Sparsity and Activation Predictors", first section
+// (the exact mask needs every gate row: g_j = w_gate_j . x + b_j).
+//
+//   out[b, row] = epi( sum_c W[row, c] * v[b, c] ),  epi = id | relu | +bias
+//
+// Each CTA owns a contiguous block of rows, i.e. one contiguous byte range of
+// W.  Thread 0 streams it into shared memory in chunks of ~40 KB with bulk
+// async copies (one copy per chunk, so the copy engine's fixed per-copy cost
+// is amortised), double-buffered, and issues the first two chunks before
+// waiting on the previous kernel: the weights do not depend on it, only v
+// does.  Warps then reduce whole rows from shared memory with shuffles.
+#include <algorithm>
+#include <utility>
+
+#include "cs_internal.cuh"
+
+namespace cs {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+enum { EPI_NONE = 0, EPI_RELU = 1, EPI_BIAS = 2 };
+
+struct GemvK {
+    const uint8_t *W;
+    int ldb;            // row pitch in bytes (multiple of 16)
+    int ncols;          // used columns
+    int nrows;
+    const float *v;     // [B, ncols]
+    int B;
+    float *out;         // [B, nrows]
+    const float *bias;  // [nrows] (EPI_BIAS)
+    int rows_per_cta;
+    int chunk_rows;
+    uint32_t *err;
+};
+
+template <typename T, int TB, int EPI>
+__global__ void __launch_bounds__(kThreads) stream_gemv_kernel(const GemvK a) {
+    constexpr int V = Vec<T>::N;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[2];
+    const int ncp = (a.ncols + 7) & ~7;
+    float *vs = reinterpret_cast<float *>(smem);                       // [TB][ncp]
+    uint8_t *buf0 = smem + (((size_t)TB * ncp * 4 + 127) & ~size_t(127));
+    const size_t chunk_bytes = (size_t)a.chunk_rows * a.ldb;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = blockIdx.x * a.rows_per_cta;
+    const int r1 = min(a.nrows, r0 + a.rows_per_cta);
+    const int nch = r0 < r1 ? (r1 - r0 + a.chunk_rows - 1) / a.chunk_rows : 0;
+    const int b0 = blockIdx.y * TB;
+    const int nvec = (a.ncols * (int)sizeof(T) + 15) / 16;
+
+    auto issue = [&](int ch) {
+        const int rs = r0 + ch * a.chunk_rows;
+        const int nr = min(a.chunk_rows, r1 - rs);
+        const uint32_t bytes = (uint32_t)nr * (uint32_t)a.ldb;
+        uint8_t *dst = buf0 + (size_t)(ch & 1) * chunk_bytes;
+        mbar_arrive_expect_tx(&full[ch & 1], bytes);
+        bulk_g2s(dst, a.W + (size_t)rs * a.ldb, bytes, &full[ch & 1]);
+    };
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_fence_init();
+        for (int ch = 0; ch < min(2, nch); ++ch) issue(ch);
+    }
+
+    pdl_launch_dependents();  // one wave: the next kernel may start its prologue
+    pdl_wait();               // v comes from the previous kernel
+    const bool v4ok = (a.ncols & 3) == 0 && (reinterpret_cast<uintptr_t>(a.v) & 15) == 0;
+    for (int t = 0; t < TB; ++t) {
+        const int b = b0 + t;
+        float *dst = vs + t * ncp;
+        if (v4ok && b < a.B) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.v + (size_t)b * a.ncols);
+#pragma unroll 8
+            for (int c = tid; c < ncp / 4; c += kThreads)
+                reinterpret_cast<float4 *>(dst)[c] = c * 4 < a.ncols ? __ldg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            for (int c = tid; c < ncp; c += kThreads)
+                dst[c] = (b < a.B && c < a.ncols) ? __ldg(a.v + (size_t)b * a.ncols + c) : 0.f;
+        }
+    }
+    __syncthreads();
+
+    bool ok = true;
+    for (int ch = 0; ch < nch; ++ch) {
+        if (!mbar_wait(&full[ch & 1], (uint32_t)((ch >> 1) & 1))) {
+            if (tid == 0) atomicOr(a.err, CS_DEVERR_TIMEOUT);
+            ok = false;
+        }
+        const uint8_t *buf = buf0 + (size_t)(ch & 1) * chunk_bytes;
+        const int rs = r0 + ch * a.chunk_rows;
+        const int nr = min(a.chunk_rows, r1 - rs);
+        for (int q = warp; q < nr; q += kWarps) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(buf + (size_t)q * a.ldb);
+            float acc[TB];
+#pragma unroll
+            for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+            for (int v = lane; v < nvec; v += 32) {
+                float w[V];
+                unpack<T>(row[v], w);
+                const int ne = a.ncols - v * V;
+                if (ne < V) {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) w[e] = e < ne ? w[e] : 0.f;
+                }
+#pragma unroll
+                for (int t = 0; t < TB; ++t) {
+                    const float *vv = vs + t * ncp + v * V;
+#pragma unroll
+                    for (int e = 0; e < V; e += 4) {
+                        const float4 x4 = *reinterpret_cast<const float4 *>(vv + e);
+                        acc[t] = fmaf(w[e], x4.x, acc[t]);
+                        acc[t] = fmaf(w[e + 1], x4.y, acc[t]);
+                        acc[t] = fmaf(w[e + 2], x4.z, acc[t]);
+                        acc[t] = fmaf(w[e + 3], x4.w, acc[t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < TB; ++t) {
+                float sum = warp_sum(acc[t]);
+                const int b = b0 + t;
+                if (lane == 0 && b < a.B) {
+                    if (EPI == EPI_RELU) sum = fmaxf(sum, 0.f);
+                    if (EPI == EPI_BIAS && a.bias) sum += a.bias[rs + q];
+                    a.out[(size_t)b * a.nrows + rs + q] = sum;
+                }
+            }
+        }
+        __syncthreads();  // the buffer of chunk ch is free
+        if (tid == 0 && ok && ch + 2 < nch) issue(ch + 2);
+    }
+    if (!ok && tid == 0) {
+        // let copies already in flight land before the CTA's memory goes away
+        for (int ch = 0; ch < nch; ++ch) mbar_wait(&full[ch & 1], (uint32_t)((ch >> 1) & 1), 100000000ull);
+    }
+}
+
+template <typename T, int TB, int EPI>
+cudaError_t run_tb(const GemvK &k0, cudaStream_t s) {
+    GemvK k = k0;
+    int sms = device_sm_count();
+    sms = sms < 1 ? 1 : sms;
+    const size_t vbytes = ((size_t)TB * ((k.ncols + 7) & ~7) * 4 + 127) & ~size_t(127);
+    // two CTAs per SM: each gets half of ~220 KB for its vector and two buffers
+    const size_t per_cta = 110 * 1024;
+    size_t chunk_budget = per_cta > vbytes ? (per_cta - vbytes) / 2 : 0;
+    chunk_budget = std::min<size_t>(chunk_budget, 48 * 1024);
+    k.rows_per_cta = std::max(1, (k.nrows + 2 * sms - 1) / (2 * sms));
+    k.chunk_rows = (int)std::max<size_t>(1, chunk_budget / (size_t)k.ldb);
+    k.chunk_rows = std::min(k.chunk_rows, k.rows_per_cta);
+    const size_t smem = vbytes + 2 * (size_t)k.chunk_rows * k.ldb;
+    auto fn = stream_gemv_kernel<T, TB, EPI>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((k.nrows + k.rows_per_cta - 1) / k.rows_per_cta, (k.B + TB - 1) / TB);
+    return launch(fn, grid, dim3(kThreads), smem, s, pdl_enabled(), k);
+}
+
+template <typename T, int EPI>
+cudaError_t run_gemv(const GemvK &k, cudaStream_t s) {
+    // tokens per CTA: as many as fit beside the weight buffers (weights are
+    // re-streamed for each group of TB tokens)
+    const size_t row_f = (size_t)((k.ncols + 7) & ~7) * 4;
+    if (k.B >= 4 && 4 * row_f <= 48 * 1024) return run_tb<T, 4, EPI>(k, s);
+    if (k.B >= 2 && 2 * row_f <= 48 * 1024) return run_tb<T, 2, EPI>(k, s);
+    return run_tb<T, 1, EPI>(k, s);
+}
+
+template <int EPI>
+cudaError_t dispatch(cs_dtype dt, const GemvK &k, cudaStream_t s) {
+    switch (dt) {
+    case CS_F32: return run_gemv<float, EPI>(k, s);
+    case CS_F16: return run_gemv<__half, EPI>(k, s);
+    default: return run_gemv<__nv_bfloat16, EPI>(k, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s) {
+    const size_t es = dtype_size(a.dtype);
+    GemvK k = {};
+    // P1: h[b, i] = relu(sum_t P_down[i, t] x[b, t])
+    k.W = static_cast<const uint8_t *>(a.p_down);
+    k.ldb = (a.ld_down ? a.ld_down : a.d) * (int)es;
+    k.ncols = a.d;
+    k.nrows = a.r;
+    k.v = a.x;
+    k.B = a.B;
+    k.out = a.h;
+    k.err = a.err;
+    cudaError_t e = dispatch<EPI_RELU>(a.dtype, k, s);
+    if (e != cudaSuccess) return e;
+    // P2: s[b, j] = sum_i P_up[j, i] h[b, i]
+    k.W = static_cast<const uint8_t *>(a.p_up);
+    k.ldb = (a.ld_up ? a.ld_up : a.r) * (int)es;
+    k.ncols = a.r;
+    k.nrows = a.f;
+    k.v = a.h;
+    k.out = a.scores;
+    return dispatch<EPI_NONE>(a.dtype, k, s);
+}
+
+cudaError_t launch_preact(const PreactArgs &a, cudaStream_t s) {
+    GemvK k = {};
+    k.W = static_cast<const uint8_t *>(a.w_gate);
+    k.ldb = a.ld * (int)dtype_size(a.dtype);
+    k.ncols = a.d;
+    k.nrows = a.f;
+    k.v = a.x;
+    k.B = 1;
+    k.out = a.pre;
+    k.bias = a.bias;
+    k.err = a.err;
+    return dispatch<EPI_BIAS>(a.dtype, k, s);
+}
+
+}  // namespace cs

@@ -19,6 +19,8 @@ constexpr unsigned kFull = 0xffffffffu;
 // Workspace layout.  The first 256 bytes are control words; the error word is
 // at offset 0.  Every region starts on a 256-byte boundary.
 // ----------------------------------------------------------------------------
+constexpr size_t kControlBytes = 256;
+
 struct WsLayout {
     size_t err = 0;         // uint32 error bits
     size_t part = 0;        // [G, B, dp] fp32 per-CTA partial sums of y
@@ -122,6 +124,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) with id `id` (1..15).
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -163,6 +174,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
 }
+
+// Per-thread asynchronous global -> shared copies (16 bytes, or 4), grouped
+// with commit/wait.  Only the issuing thread's own copies are waited for.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Same, with an L2 eviction-priority policy (evict_first for data read once).
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -258,6 +281,7 @@ struct PredictArgs {
     const float *x;
     float *h;      // [B, r]
     float *scores; // [B, f]
+    uint32_t *err = nullptr;
 };
 cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s);
 
@@ -301,6 +325,7 @@ struct PreactArgs {
     const float *bias;
     const float *x;
     float *pre;
+    uint32_t *err = nullptr;
 };
 cudaError_t launch_preact(const PreactArgs &a, cudaStream_t s);
 

@@ -80,7 +80,7 @@ cudaError_t predict_select(const StackPlan &p, const Bufs &b, int l, const float
     PredictArgs a;
     a.d = P.d; a.r = P.r; a.f = P.f; a.B = 1; a.dtype = P.dtype;
     a.ld_down = P.ld_down; a.ld_up = P.ld_up; a.p_down = P.p_down; a.p_up = P.p_up;
-    a.x = xin; a.h = b.h; a.scores = b.scores;
+    a.x = xin; a.h = b.h; a.scores = b.scores; a.err = b.err;
     cudaError_t e = launch_predict(a, s);
     if (e != cudaSuccess) return e;
     SelectArgs sa;
@@ -113,7 +113,7 @@ cudaError_t exact_step(const StackPlan &p, const Bufs &b, int l, const float *xi
     const cs_ffn_layer &Ly = p.layers[l];
     PreactArgs pa;
     pa.d = Ly.d; pa.f = Ly.f; pa.ld = Ly.ld ? Ly.ld : Ly.d; pa.dtype = Ly.dtype;
-    pa.w_gate = Ly.w_gate; pa.bias = Ly.bias; pa.x = xin; pa.pre = b.pre;
+    pa.w_gate = Ly.w_gate; pa.bias = Ly.bias; pa.x = xin; pa.pre = b.pre; pa.err = b.err;
     cudaError_t e = launch_preact(pa, s);
     if (e != cudaSuccess) return e;
     SelectArgs sa;

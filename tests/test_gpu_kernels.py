@@ -116,6 +116,48 @@ def test_threshold_bit_exact(f):
             assert N[b] == want.size and np.array_equal(I[b, :N[b]], want), (f, tau)
 
 
+COOP_F = [1024, 1057, 2048, 4900, 20480, 32768, 49152]
+
+
+@pytest.mark.parametrize("f", COOP_F)
+def test_topk_single_row_bit_exact(f):
+    """Single rows at large f, every k from 0 to past f, with ties, specials
+    and a coarse quantisation (masses of equal scores), repeated on one
+    workspace."""
+    ws = ws_for(64, f, 8)
+    idx = torch.full((1, f), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mask = torch.zeros((1, (f + 31) // 32), dtype=torch.int32, device="cuda")
+    for variant in range(4):
+        S = synth.score_vector(7 * f + variant, f, ties=f // 3 if variant else 0,
+                               specials=variant == 2, quantize=0.02 if variant == 3 else None)[None]
+        s = torch.from_numpy(S).cuda()
+        for k in sorted({0, 1, 2, f // 10, f // 3, f // 2, f - 1, f, f + 5}):
+            cs.cs_select(s, cs.select_params(cs.CS_SEL_TOPK, k), idx, cnt, mask, ws=ws)
+            want = oracle.select_topk(S[0], k)
+            n = int(cnt.item())
+            assert n == want.size, (f, k, variant)
+            assert np.array_equal(idx.cpu().numpy()[0, :n], want), (f, k, variant)
+            assert np.array_equal(mask.cpu().numpy()[0].view(np.uint32),
+                                  synth.bits_from_bool(np.isin(np.arange(f), want)))
+        for tau in (-np.inf, 0.0, 0.7, np.nan):
+            cs.cs_select(s, cs.select_params(cs.CS_SEL_THRESHOLD, 0, tau), idx, cnt, mask, ws=ws)
+            want = oracle.select_threshold(S[0], tau)
+            n = int(cnt.item())
+            assert n == want.size and np.array_equal(idx.cpu().numpy()[0, :n], want), (f, tau)
+    # a mass of equal scores: the pivot bucket overflows the exact ranking and
+    # the radix fallback resolves it
+    S = np.zeros((1, f), np.float32)
+    S[0, ::7] = 1.0
+    s = torch.from_numpy(S).cuda()
+    for k in (1, f // 7, f // 7 + 1, f // 2, f - 3):
+        cs.cs_select(s, cs.select_params(cs.CS_SEL_TOPK, k), idx, cnt, mask, ws=ws)
+        want = oracle.select_topk(S[0], k)
+        n = int(cnt.item())
+        assert n == want.size and np.array_equal(idx.cpu().numpy()[0, :n], want), (f, k)
+    assert dev_err(ws) == 0
+
+
 def test_select_rejects_bad_args():
     s = torch.zeros((1, 8), device="cuda")
     idx = torch.zeros((1, 8), dtype=torch.int32, device="cuda")

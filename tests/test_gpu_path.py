@@ -33,7 +33,7 @@ def run_step(layer, pred, x, params, f, d, ws):
     cnt = torch.empty(1, dtype=torch.int32, device="cuda")
     y = torch.empty((1, d), device="cuda")
     cs.cs_predict(pred, x, scores, ws)
-    cs.cs_select(scores, params, idx, cnt)
+    cs.cs_select(scores, params, idx, cnt, ws=ws)
     cs.cs_sparse_ffn(layer, x, idx, cnt, y, ws)
     n = int(cnt.item())
     return scores.cpu().numpy()[0], idx.cpu().numpy()[0, :n], y.cpu().numpy()[0]
