@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
     constexpr int NROW = (PRE ? 0 : 1) + (GLU ? 1 : 0) + 1;
     constexpr bool DOTS = !PRE || GLU;
     extern __shared__ __align__(16) uint4 ring[];  // [slot][NROW][nvec]
-    __shared__ float red[kWarps][kNgMax][TB][2];
-    __shared__ float act[kNgMax][TB];
+    __shared__ float red[2][kWarps][kNgMax][TB][2];
+    __shared__ float act[2][kNgMax][TB];
     __shared__ float addv[kStageMax];              // bias / pre-activation per slot
     __shared__ int s_idx[kChunkMax];               // this CTA's ids, staged once
 
@@ -164,23 +164,47 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
         }
     }
 
-    int gs = 0;  // g % sg
-    for (int g = 0; g < ngroups; ++g) {
-        const int gn = min(ng, cnt - g * ng);
+    // Software-pipelined groups: iteration g computes group g's gate (and up)
+    // dot products, then group g-1's down-row AXPY.  Named barriers are split
+    // into arrive / wait: every warp arrives after writing its partial sums
+    // (barrier A) and goes on; warp 0 alone waits on A, finishes the
+    // activations, and arrives on barrier B, which the other warps wait on
+    // only one iteration later, before that group's AXPY.  So no thread waits
+    // on another thread's data for the group it is working on.
+    constexpr int kBarA = 1, kBarB = 3;  // ids 1,2 and 3,4 by group parity
+    int gs = 0;      // ring group of group g
+    int s0_prev = 0, gn_prev = 0;
+    for (int g = 0; g <= ngroups; ++g) {
+        const bool have = g < ngroups;
+        const int gn = have ? min(ng, cnt - g * ng) : 0;
         const int s0 = gs * ng;
-        if (sg == 2) cp_async_wait<1>(); else cp_async_wait<2>();  // group g has landed
-        float pg[kNgMax][TB], pu[kNgMax][TB];
+        const int p = g & 1;
+        if (have) {
+            // this thread's copies for group g have landed (commits so far: sg at
+            // start, then one per iteration from iteration 1)
+            if (g == 0) { if (sg == 2) cp_async_wait<1>(); else cp_async_wait<2>(); }
+            else { if (sg == 2) cp_async_wait<0>(); else cp_async_wait<1>(); }
+            // gate (and up) dot products: one accumulator per (neuron, vector),
+            // all neurons of the group interleaved.  Slots past the group's
+            // last neuron hold stale data whose sums are never used.
+            float pg[kNgMax][TB], pu[kNgMax][TB];
 #pragma unroll
-        for (int q = 0; q < kNgMax; ++q) {
+            for (int q = 0; q < kNgMax; ++q)
 #pragma unroll
-            for (int t = 0; t < TB; ++t) pg[q][t] = pu[q][t] = 0.f;
-            if (DOTS && q < gn) {
-                const uint4 *slot = ring + (size_t)(s0 + q) * NROW * nvec;
+                for (int t = 0; t < TB; ++t) pg[q][t] = pu[q][t] = 0.f;
+            if (DOTS) {
 #pragma unroll
                 for (int i = 0; i < MAXV; ++i) {
-                    if (vok[i]) {
-                        const int v = tid + i * kThreads;
-                        const int ne = a.d - v * V;  // < V only on a row's last vector
+                    if (!vok[i]) continue;
+                    const int v = tid + i * kThreads;
+                    const int ne = a.d - v * V;  // < V only on a row's last vector
+                    float ag[kNgMax][TB], au[kNgMax][TB];
+#pragma unroll
+                    for (int q = 0; q < kNgMax; ++q) {
+                        const uint4 *slot = ring + (size_t)(s0 + q) * NROW * nvec;
+#pragma unroll
+                        for (int t = 0; t < TB; ++t) ag[q][t] = au[q][t] = 0.f;
+                        if (q >= ng) continue;  // ng is uniform: no divergence
                         if (!PRE) {
                             float w[V];
                             unpack<T>(slot[v], w);
@@ -191,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
 #pragma unroll
                             for (int e = 0; e < V; ++e)
 #pragma unroll
-                                for (int t = 0; t < TB; ++t) pg[q][t] = fmaf(w[e], xr[t][i][e], pg[q][t]);
+                                for (int t = 0; t < TB; ++t) ag[q][t] = fmaf(w[e], xr[t][i][e], ag[q][t]);
                         }
                         if (GLU) {
                             float w[V];
@@ -203,77 +227,90 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
 #pragma unroll
                             for (int e = 0; e < V; ++e)
 #pragma unroll
-                                for (int t = 0; t < TB; ++t) pu[q][t] = fmaf(w[e], xr[t][i][e], pu[q][t]);
+                                for (int t = 0; t < TB; ++t) au[q][t] = fmaf(w[e], xr[t][i][e], au[q][t]);
                         }
                     }
+#pragma unroll
+                    for (int q = 0; q < kNgMax; ++q)
+#pragma unroll
+                        for (int t = 0; t < TB; ++t) { pg[q][t] += ag[q][t]; pu[q][t] += au[q][t]; }
                 }
+#pragma unroll
+                for (int q = 0; q < kNgMax; ++q)
+#pragma unroll
+                    for (int t = 0; t < TB; ++t) {
+                        if (q < gn) {
+                            const float sgv = PRE ? 0.f : warp_sum(pg[q][t]);
+                            const float suv = GLU ? warp_sum(pu[q][t]) : 0.f;
+                            if (lane == 0) {
+                                red[p][warp][q][t][0] = sgv;
+                                red[p][warp][q][t][1] = suv;
+                            }
+                        }
+                    }
+            }
+            if (warp != 0) {
+                named_arrive(kBarA + p, kThreads);
+            } else {
+                named_sync(kBarA + p, kThreads);
+                // lane q finishes neuron q (its own bias copy has landed), warps in order
+                if (lane < gn) {
+                    const int q = lane;
+                    const int j = s_idx[g * ng + q];
+                    const bool valid = j >= 0 && j < a.f;
+                    const float add = addv[s0 + q];
+#pragma unroll
+                    for (int t = 0; t < TB; ++t) {
+                        float gsum = 0.f, usum = 0.f;
+                        if (DOTS) {
+#pragma unroll
+                            for (int w = 0; w < kWarps; ++w) {
+                                gsum += red[p][w][q][t][0];
+                                usum += red[p][w][q][t][1];
+                            }
+                        }
+                        const float gv = PRE ? add : gsum + add;
+                        float av = fmaxf(gv, 0.f);
+                        if (GLU) av *= usum;
+                        act[p][q][t] = valid ? av : 0.f;
+                    }
+                    if (!valid) atomicOr(a.err, CS_DEVERR_INDEX);
+                }
+                __syncwarp();
+                named_arrive(kBarB + p, kThreads);
             }
         }
-        if (DOTS) {
+        if (g > 0) {
+            // group g-1: y += a_j * w_down_j
+            const int pp = p ^ 1;
+            if (warp != 0) named_sync(kBarB + pp, kThreads);
+            float av[kNgMax][TB];
 #pragma unroll
             for (int q = 0; q < kNgMax; ++q)
 #pragma unroll
-                for (int t = 0; t < TB; ++t) {
-                    if (q < gn) {
-                        const float sgv = PRE ? 0.f : warp_sum(pg[q][t]);
-                        const float suv = GLU ? warp_sum(pu[q][t]) : 0.f;
-                        if (lane == 0) {
-                            red[warp][q][t][0] = sgv;
-                            red[warp][q][t][1] = suv;
+                for (int t = 0; t < TB; ++t) av[q][t] = q < gn_prev ? act[pp][q][t] : 0.f;
+#pragma unroll
+            for (int q = 0; q < kNgMax; ++q) {
+                if (q < gn_prev) {
+                    const uint4 *dn = ring + ((size_t)(s0_prev + q) * NROW + (NROW - 1)) * nvec;
+#pragma unroll
+                    for (int i = 0; i < MAXV; ++i) {
+                        if (vok[i]) {
+                            float w[V];
+                            unpack<T>(dn[tid + i * kThreads], w);
+#pragma unroll
+                            for (int t = 0; t < TB; ++t)
+#pragma unroll
+                                for (int e = 0; e < V; ++e) yacc[t][i][e] = fmaf(av[q][t], w[e], yacc[t][i][e]);
                         }
                     }
                 }
-        }
-        __syncthreads();
-        // lane q of warp 0 finishes neuron q (its own bias copy has landed), warps summed in order
-        if (warp == 0 && lane < gn) {
-            const int q = lane;
-            const int j = s_idx[g * ng + q];
-            const bool valid = j >= 0 && j < a.f;
-            const float add = addv[s0 + q];
-#pragma unroll
-            for (int t = 0; t < TB; ++t) {
-                float gsum = 0.f, usum = 0.f;
-                if (DOTS) {
-#pragma unroll
-                    for (int w = 0; w < kWarps; ++w) {
-                        gsum += red[w][q][t][0];
-                        usum += red[w][q][t][1];
-                    }
-                }
-                const float gv = PRE ? add : gsum + add;
-                float av = fmaxf(gv, 0.f);
-                if (GLU) av *= usum;
-                act[q][t] = valid ? av : 0.f;
             }
-            if (!valid) atomicOr(a.err, CS_DEVERR_INDEX);
+            // this thread's slots of group g-1 are free: refill them
+            issue(g - 1 + sg, s0_prev);
         }
-        __syncthreads();
-        float av[kNgMax][TB];
-#pragma unroll
-        for (int q = 0; q < kNgMax; ++q)
-#pragma unroll
-            for (int t = 0; t < TB; ++t) av[q][t] = q < gn ? act[q][t] : 0.f;
-        // y += a_j * w_down_j
-#pragma unroll
-        for (int q = 0; q < kNgMax; ++q) {
-            if (q < gn) {
-                const uint4 *dn = ring + ((size_t)(s0 + q) * NROW + (NROW - 1)) * nvec;
-#pragma unroll
-                for (int i = 0; i < MAXV; ++i) {
-                    if (vok[i]) {
-                        float w[V];
-                        unpack<T>(dn[tid + i * kThreads], w);
-#pragma unroll
-                        for (int t = 0; t < TB; ++t)
-#pragma unroll
-                            for (int e = 0; e < V; ++e) yacc[t][i][e] = fmaf(av[q][t], w[e], yacc[t][i][e]);
-                    }
-                }
-            }
-        }
-        // this thread's slots of group g are free: refill them with group g + sg
-        issue(g + sg, s0);
+        s0_prev = s0;
+        gn_prev = gn;
         gs = gs + 1 == sg ? 0 : gs + 1;
     }
     cp_async_wait<0>();
@@ -377,11 +414,12 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     // ring of sg groups of ng neurons: as deep as the budget allows
     int nst = (int)(kRingBudget / per_neuron);
     if (nst < 2) return cudaErrorInvalidValue;
+    // three ring groups keep one group in flight while two are in use
     if (nst >= 3 * kNgMax) { k.ng = kNgMax; k.sg = 3; }
-    else if (nst >= 2 * kNgMax) { k.ng = kNgMax; k.sg = 2; }
+    else if (nst >= 9) { k.ng = 3; k.sg = 3; }
     else if (nst >= 6) { k.ng = 2; k.sg = 3; }
-    else if (nst >= 4) { k.ng = 2; k.sg = 2; }
-    else { k.ng = 1; k.sg = nst >= 3 ? 3 : 2; }
+    else if (nst >= 3) { k.ng = 1; k.sg = 3; }
+    else { k.ng = 1; k.sg = 2; }
     static_assert(3 * kNgMax <= kStageMax, "ring slots");
     const size_t smem = (size_t)k.ng * k.sg * per_neuron;
     const int tb = a.B >= 2 ? 2 : 1;

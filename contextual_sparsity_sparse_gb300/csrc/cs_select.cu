@@ -25,6 +25,7 @@
 // scan over the 32 warps gives (a) the K-ties before each warp, so the lowest
 // ids win, and (b) each warp's output position.  No global atomics and no
 // grid-wide synchronisation: a grid barrier costs microseconds here.
+#include <cstdlib>
 #include <utility>
 
 #include "cs_internal.cuh"
@@ -311,11 +312,372 @@ select_kernel(const float *__restrict__ scores, int f, int kind, int k, float ta
     if (tid == 0) count[b] = s_total;
 }
 
+// ---------------------------------------------------------------------------
+// Cluster variant: one thread-block cluster of kCl CTAs per token row.  CTA r
+// owns the 32-aligned id slice [r*S, (r+1)*S).  The same four steps run with
+// the element work split kCl ways; the CTAs exchange min/max, histogram
+// slices, the pivot bucket's members and their per-CTA counts through
+// distributed shared memory, separated by hardware cluster barriers (no global
+// atomics, no grid-wide barrier).
+// ---------------------------------------------------------------------------
+constexpr int kCl = 8;
+constexpr int kClThreads = 1024;
+constexpr int kClSliceMax = 6144;            // f <= kCl * kClSliceMax
+constexpr int kClBinsPerCta = kBuckets / kCl;
+
+struct ClSmem {
+    float vals[kClSliceMax];
+    uint32_t hist[kBuckets];
+    uint32_t red[kClBinsPerCta];
+    uint32_t ckey[kCandMax];
+    uint32_t cid[kCandMax];
+    uint32_t wtot[32][2];
+    uint32_t loc[kClBinsPerCta];             // a remote bin slice, copied locally
+    float rlo[kCl], rhi[kCl];
+    uint32_t rtot[kCl];
+    int rgt[kCl], req[kCl];
+    float lo, hi;
+    uint32_t slice_total;
+    uint32_t ncand_fill;
+    int cta_gt, cta_eq;
+    uint32_t s_bucket, s_rem, s_ncand, s_pivot;
+    int s_need, s_base, s_eqb, s_total, s_slow;
+};
+
+__device__ __forceinline__ uint32_t cl_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cl_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr(p)), "r"(rank));
+    return out;
+}
+__device__ __forceinline__ uint32_t cl_ld_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float cl_ld_f32(uint32_t addr) { return __uint_as_float(cl_ld_u32(addr)); }
+__device__ __forceinline__ void cl_st_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cl_atom_add(uint32_t addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
+
+__global__ void __launch_bounds__(kClThreads)
+select_cluster_kernel(const float *__restrict__ scores, int f, int kind, int k, float tau,
+                      int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
+                      uint32_t *__restrict__ mask) {
+    extern __shared__ __align__(16) uint8_t dyn[];
+    ClSmem &S = *reinterpret_cast<ClSmem *>(dyn);
+    __shared__ int wsum[32];
+    __shared__ float wred[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cl_rank();
+    const int b = blockIdx.x / kCl;
+    const int words = (f + 31) >> 5;
+    const int SL = (((f + kCl - 1) / kCl) + 31) & ~31;
+    const int beg = min((int)rank * SL, f), end = min(beg + SL, f);
+    const int n_my = end - beg;
+    const float *s = scores + (size_t)b * f;
+    int32_t *out = idx + (size_t)b * ld_idx;
+
+    pdl_launch_dependents();
+    pdl_wait();  // scores come from the previous kernel
+
+    float lo = INFINITY, hi = -INFINITY;
+    for (int j = tid; j < n_my; j += kClThreads) {
+        const float v = __ldg(s + beg + j);
+        S.vals[j] = v;
+        if (v - v == 0.f) { lo = fminf(lo, v); hi = fmaxf(hi, v); }
+    }
+    __syncthreads();  // vals[] is read across threads from here on
+    const int kk = k < 0 ? 0 : (k > f ? f : k);
+    const bool radix = kind == SEL_TOPK && kk > 0 && kk < f;
+    uint32_t pivot = 0u;
+    int need = 0;
+    if (radix) {
+        lo = block_min(lo, wred);
+        hi = block_max(hi, wred);
+        if (tid == 0) { S.lo = lo; S.hi = hi; S.ncand_fill = 0u; }
+        for (int i = tid; i < kBuckets; i += kClThreads) S.hist[i] = 0u;
+        cl_sync();
+        // cluster-wide min / max (every CTA the same): one remote load per CTA
+        if (tid < kCl) {
+            S.rlo[tid] = cl_ld_f32(cl_map(&S.lo, (uint32_t)tid));
+            S.rhi[tid] = cl_ld_f32(cl_map(&S.hi, (uint32_t)tid));
+        }
+        __syncthreads();
+        float smin = INFINITY, smax = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kCl; ++r) { smin = fminf(smin, S.rlo[r]); smax = fmaxf(smax, S.rhi[r]); }
+        const float scale = smax > smin ? (float)(kBuckets - 4) / (smax - smin) : 0.f;
+        for (int j = tid; j < n_my; j += kClThreads) atomicAdd(&S.hist[bucket_of(S.vals[j], smin, scale)], 1u);
+        cl_sync();
+        // reduce-scatter: this CTA sums bins [rank*512, rank*512 + 512) over the cluster
+        uint32_t part = 0;
+        if (tid < kClBinsPerCta) {
+            const int bin = (int)rank * kClBinsPerCta + tid;
+            uint32_t sum = 0;
+            for (uint32_t r = 0; r < kCl; ++r) sum += cl_ld_u32(cl_map(&S.hist[bin], r));
+            S.red[tid] = sum;
+            part = sum;
+        }
+        int tot;
+        block_excl_scan((int)part, wsum, &tot);
+        if (tid == 0) S.slice_total = (uint32_t)tot;
+        cl_sync();
+        // which CTA's bin slice holds the kk-th largest (slices are ordered by
+        // score: the last CTA has the top bins), then which bin
+        if (tid < kCl) S.rtot[tid] = cl_ld_u32(cl_map(&S.slice_total, (uint32_t)tid));
+        __syncthreads();
+        int owner = 0;
+        uint32_t above_owner = 0;
+        {
+            uint32_t run = 0;
+            for (int r = kCl - 1; r >= 0; --r) {
+                if (run + S.rtot[r] >= (uint32_t)kk) { owner = r; break; }
+                run += S.rtot[r];
+            }
+            above_owner = run;
+        }
+        if (tid < kClBinsPerCta) S.loc[tid] = cl_ld_u32(cl_map(&S.red[tid], (uint32_t)owner));
+        __syncthreads();
+        {
+            // suffix counts over the owner's bins: thread t (< 512) holds bin t
+            const uint32_t cb = tid < kClBinsPerCta ? S.loc[tid] : 0u;
+            int tot_unused;
+            // reversed scan: thread t feeds bin (511 - t)
+            const uint32_t rb = tid < kClBinsPerCta ? S.loc[kClBinsPerCta - 1 - tid] : 0u;
+            const int excl = block_excl_scan((int)rb, wsum, &tot_unused);
+            __syncthreads();
+            if (tid < kClBinsPerCta) S.hist[kClBinsPerCta - 1 - tid] = (uint32_t)excl;  // count above bin
+            __syncthreads();
+            if (tid < kClBinsPerCta) {
+                const uint32_t run = above_owner + S.hist[tid];
+                if (run < (uint32_t)kk && run + cb >= (uint32_t)kk) {
+                    S.s_bucket = (uint32_t)(owner * kClBinsPerCta + tid);
+                    S.s_rem = (uint32_t)kk - run;
+                    S.s_ncand = cb;
+                }
+            }
+        }
+        __syncthreads();
+        const int B_ = (int)S.s_bucket;
+        const uint32_t rem = S.s_rem, ncand = S.s_ncand;
+        if (ncand <= (uint32_t)kCandMax) {
+            // every CTA sends its members of bucket B_ to CTA 0
+            const uint32_t fill0 = cl_map(&S.ncand_fill, 0);
+            for (int j = tid; j < n_my; j += kClThreads) {
+                const float v = S.vals[j];
+                if (bucket_of(v, smin, scale) == B_) {
+                    const uint32_t p = cl_atom_add(fill0, 1u);
+                    cl_st_u32(cl_map(&S.ckey[p], 0), score_key(v));
+                    cl_st_u32(cl_map(&S.cid[p], 0), (uint32_t)(beg + j));
+                }
+            }
+            cl_sync();
+            // every CTA copies the members from CTA 0 once, then ranks them
+            // locally: the member of rank rem-1 is the pivot
+            if (rank != 0) {
+                const uint32_t ck0 = cl_map(&S.ckey[0], 0), ci0 = cl_map(&S.cid[0], 0);
+                for (int c = tid; c < (int)ncand; c += kClThreads) {
+                    S.ckey[c] = cl_ld_u32(ck0 + 4u * c);
+                    S.cid[c] = cl_ld_u32(ci0 + 4u * c);
+                }
+            }
+            __syncthreads();
+            for (int c = tid; c < (int)ncand; c += kClThreads) {
+                const uint32_t kc = S.ckey[c], ic = S.cid[c];
+                uint32_t rk = 0;
+                for (int o = 0; o < (int)ncand; ++o) {
+                    const uint32_t ko = S.ckey[o];
+                    rk += (ko > kc) || (ko == kc && S.cid[o] < ic);
+                }
+                if (rk == rem - 1u) S.s_pivot = kc;
+            }
+            __syncthreads();
+            int gtc = 0;
+            for (int c = tid; c < (int)ncand; c += kClThreads) gtc += S.ckey[c] > S.s_pivot;
+            int tot_gt;
+            block_excl_scan(gtc, wsum, &tot_gt);
+            pivot = S.s_pivot;
+            need = (int)rem - tot_gt;
+        } else {
+            // a mass of equal scores: every CTA resolves it alone from the full row
+            // (radix select over the members' exact keys, read from global memory)
+            uint32_t prefix = 0u, pmask = 0u, r_ = rem;
+            uint32_t *h = S.hist;
+            for (int pass = 0; pass < 4; ++pass) {
+                const int shift = 24 - 8 * pass;
+                __syncthreads();
+                if (tid < 256) h[tid] = 0u;
+                __syncthreads();
+                for (int j = tid; j < f; j += kClThreads) {
+                    const float v = __ldg(s + j);
+                    const uint32_t key = score_key(v);
+                    if (bucket_of(v, smin, scale) == B_ && (key & pmask) == prefix)
+                        atomicAdd(&h[(key >> shift) & 255u], 1u);
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    uint32_t run = 0;
+                    for (int dgt = 255; dgt >= 0; --dgt) {
+                        const uint32_t c = h[dgt];
+                        if (run < r_ && run + c >= r_) { S.s_pivot = (uint32_t)dgt; S.s_rem = r_ - run; break; }
+                        run += c;
+                    }
+                }
+                __syncthreads();
+                prefix |= S.s_pivot << shift;
+                pmask |= 255u << shift;
+                r_ = S.s_rem;
+            }
+            pivot = prefix;
+            need = (int)r_;
+        }
+    }
+
+    // compaction of this CTA's slice: warp w owns [w*W, (w+1)*W) within it
+    const int nw = kClThreads / 32;
+    const int WL = (((n_my + nw - 1) / nw) + 31) & ~31;
+    const int wbeg = min(warp * WL, n_my), wend = min(wbeg + WL, n_my);
+    const unsigned lt = (1u << lane) - 1u;
+    auto flags = [&](int jl, bool &gt, bool &eq) {
+        gt = false;
+        eq = false;
+        if (jl >= wend) return;
+        const float v = S.vals[jl];
+        if (kind == SEL_TOPK) {
+            if (kk == f) gt = true;
+            else if (kk > 0) { const uint32_t key = score_key(v); gt = key > pivot; eq = key == pivot; }
+        } else if (kind == SEL_THRESHOLD) {
+            gt = v >= tau;
+        } else {
+            gt = v > 0.f;
+        }
+    };
+    int w_gt = 0, w_eq = 0;
+    for (int base = wbeg; base < wend; base += 32) {
+        bool gt, eq;
+        flags(base + lane, gt, eq);
+        w_gt += __popc(__ballot_sync(kFull, gt));
+        w_eq += __popc(__ballot_sync(kFull, eq));
+    }
+    if (lane == 0) { S.wtot[warp][0] = (uint32_t)w_gt; S.wtot[warp][1] = (uint32_t)w_eq; }
+    __syncthreads();
+    if (tid == 0) {
+        int g_ = 0, e_ = 0;
+        for (int w = 0; w < nw; ++w) { g_ += (int)S.wtot[w][0]; e_ += (int)S.wtot[w][1]; }
+        S.cta_gt = g_;
+        S.cta_eq = e_;
+    }
+    cl_sync();
+    // this CTA's place: ties and selections of the CTAs before it
+    if (tid < kCl) {
+        S.rgt[tid] = (int)cl_ld_u32(cl_map(&S.cta_gt, (uint32_t)tid));
+        S.req[tid] = (int)cl_ld_u32(cl_map(&S.cta_eq, (uint32_t)tid));
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int eqb = 0, selb = 0;
+        for (int r = 0; r < kCl; ++r) {
+            const int take = max(0, min(S.req[r], need - eqb));
+            if (r == (int)rank) { S.s_base = selb; S.s_eqb = eqb; }
+            eqb += S.req[r];
+            selb += S.rgt[r] + take;
+        }
+        S.s_total = selb;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // warp offsets inside the CTA (ties first, so the lowest ids win)
+        const int g_ = (int)S.wtot[lane][0], e_ = (int)S.wtot[lane][1];
+        int eb = e_;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) { const int nn = __shfl_up_sync(kFull, eb, o); if (lane >= o) eb += nn; }
+        eb = eb - e_ + S.s_eqb;
+        const int take = max(0, min(e_, need - eb));
+        const int sel = g_ + take;
+        int sb = sel;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) { const int nn = __shfl_up_sync(kFull, sb, o); if (lane >= o) sb += nn; }
+        S.wtot[lane][0] = (uint32_t)(sb - sel + S.s_base);
+        S.wtot[lane][1] = (uint32_t)eb;
+    }
+    __syncthreads();
+    int pos = (int)S.wtot[warp][0], eq_run = (int)S.wtot[warp][1];
+    for (int base = wbeg; base < wend; base += 32) {
+        bool gt, eq;
+        const int jl = base + lane;
+        flags(jl, gt, eq);
+        const unsigned be = __ballot_sync(kFull, eq);
+        const bool take = gt || (eq && eq_run + __popc(be & lt) < need);
+        const unsigned bs = __ballot_sync(kFull, take);
+        if (take) out[pos + __popc(bs & lt)] = beg + jl;
+        if (mask && lane == 0) mask[(size_t)b * words + ((beg + base) >> 5)] = bs;
+        eq_run += __popc(be);
+        pos += __popc(bs);
+    }
+    if (rank == 0 && tid == 0) count[b] = S.s_total;
+    cl_sync();  // no CTA leaves while another may still read its shared memory
+}
+
 size_t select_smem(int f) { return sizeof(uint32_t) * ((size_t)f + kBuckets); }
+
+bool cluster_select_enabled() {
+    static const bool on = [] {
+        const char *v = getenv("CS_SELECT_CLUSTER");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
 
 }  // namespace
 
+cudaError_t launch_select_cluster(const SelectArgs &a, cudaStream_t s) {
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem = sizeof(ClSmem);
+    if (configured_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCl * a.B);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int n = 1;
+    if (pdl_enabled()) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, select_cluster_kernel, a.scores, a.f, (int)a.kind, a.k, a.tau, a.idx,
+                              a.ld_idx, a.count, a.mask);
+}
+
 cudaError_t launch_select(const SelectArgs &a, cudaStream_t s) {
+    if (a.f >= 2048 && a.f <= kCl * kClSliceMax && cluster_select_enabled()) return launch_select_cluster(a, s);
     static int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
