@@ -30,7 +30,7 @@ _TORCH_DT = {torch.float32: CS_F32, torch.float16: CS_F16, torch.bfloat16: CS_BF
 EXPORTS = ["cs_version", "cs_status_string", "cs_last_error", "cs_workspace_size",
            "cs_workspace_init", "cs_get_device_error", "cs_pack_transpose", "cs_predict",
            "cs_select", "cs_sparse_ffn", "cs_exact_ffn", "cs_union_mask", "cs_decode_stack",
-           "cs_stack_release"]
+           "cs_stack_release", "cs_sparse_ffn_noalloc"]
 
 
 class CsError(RuntimeError):
@@ -86,9 +86,11 @@ def lib():
             L.cs_union_mask.argtypes = [P, I, I, P, P, P, P, S, P]
             L.cs_decode_stack.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), I, P, C.c_float,
                                           C.POINTER(_Sel), I, P, P, P, S, P, P]
+            L.cs_sparse_ffn_noalloc.argtypes = [C.POINTER(_Layer), P, I, P, P, P, P]
             for name in ("cs_workspace_init", "cs_get_device_error", "cs_pack_transpose",
                          "cs_predict", "cs_select", "cs_sparse_ffn", "cs_exact_ffn",
-                         "cs_union_mask", "cs_decode_stack", "cs_stack_release"):
+                         "cs_union_mask", "cs_decode_stack", "cs_stack_release",
+                         "cs_sparse_ffn_noalloc"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -201,6 +203,14 @@ def cs_sparse_ffn(layer: FfnLayer, x, idx, count, y, ws: Workspace, stream=None)
     B = x.shape[0] if x.dim() == 2 else 1
     _check(lib().cs_sparse_ffn(C.byref(layer.c), _ptr(x), B, _ptr(idx), _ptr(count), _ptr(y),
                                ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def cs_sparse_ffn_noalloc(layer: FfnLayer, x, idx, count, y, stream=None):
+    """cs_sparse_ffn without a workspace (see include/cs.h): scratch comes from
+    a fixed array inside the library, so nothing is allocated."""
+    B = x.shape[0] if x.dim() == 2 else 1
+    _check(lib().cs_sparse_ffn_noalloc(C.byref(layer.c), _ptr(x), B, _ptr(idx), _ptr(count),
+                                       _ptr(y), _stream(stream)))
 
 
 def cs_exact_ffn(layer: FfnLayer, x, preact, idx, count, y, ws: Workspace, mask=None, stream=None):

@@ -145,6 +145,8 @@ cs_status check_pred(const cs_predictor *P) {
 
 }  // namespace
 
+cs_status cs::validate_layer(const cs_ffn_layer *layer, int *ld_out) { return check_layer(layer, ld_out); }
+
 extern "C" {
 
 const char *cs_version(void) { return "contextual_sparsity_sparse_gb300 0.1 (sm_103a)"; }

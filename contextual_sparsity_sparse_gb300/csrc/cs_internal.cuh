@@ -344,4 +344,8 @@ cudaError_t launch_union(const UnionArgs &a, cudaStream_t s);
 
 size_t dtype_size(cs_dtype t);
 
+// Host-side checks of a layer descriptor (sets the error text); *ld_out gets
+// the effective row stride.
+cs_status validate_layer(const cs_ffn_layer *layer, int *ld_out);
+
 }  // namespace cs

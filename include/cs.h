@@ -234,6 +234,29 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
 /* Drops every cached stack graph (waits for nothing; call when idle). */
 cs_status cs_stack_release(void);
 
+/*
+ * cs_sparse_ffn without a workspace, for callers that cannot allocate device
+ * memory (for example a plugin running inside a host framework that owns all
+ * device allocations and gives it no allocator, or a path where a cudaMalloc
+ * may not be issued).  The method's sources have no counterpart of this call:
+ * it computes exactly what cs_sparse_ffn computes, with the same arguments
+ * minus the workspace.
+ *
+ * Scratch: a fixed device array inside the library (2^21 fp32 values, 8 MiB,
+ * held by every GPU that loads the library until the process exits).  A call
+ * needs (SM count) * B * roundup(d, 8) values; larger calls return
+ * CS_ERR_UNSUPPORTED without enqueuing anything.  The call allocates nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device), so make that first call before any stream capture begins.
+ * Every call shares the one array and it keeps the last call's contents
+ * (each call rewrites all of what it reads): calls that overlap on the GPU,
+ * on different streams or from different threads, race and must be ordered
+ * by the caller.  Device-side error bits (bad ids, which are skipped as in
+ * cs_sparse_ffn) are not reported by this entry point.
+ */
+cs_status cs_sparse_ffn_noalloc(const cs_ffn_layer *layer, const float *x, int B, const int32_t *idx,
+                                const int32_t *count, float *y, cs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
