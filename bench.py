@@ -40,6 +40,15 @@ WORKLOADS = {
     "opt13b-topk20": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.20),
     "opt13b-thr10": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="threshold", share=0.10),
     "tiny-relu-topk10": dict(d=512, f=2048, r=64, dt=0, glu=False, rho=0.10, mode="topk", share=0.10),
+    # layer stacks: one step = one token through every layer (cs_decode_stack)
+    "opt30b-stack-seq": dict(d=7168, f=28672, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.10,
+                             L=48, stack="seq"),
+    "opt30b-stack-lookahead": dict(d=7168, f=28672, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.10,
+                                   L=48, stack="lookahead"),
+    "llama70b-stack-seq": dict(d=8192, f=28672, r=1024, dt=2, glu=True, rho=0.15, mode="topk", share=0.15,
+                               L=80, stack="seq"),
+    "llama70b-stack-lookahead": dict(d=8192, f=28672, r=1024, dt=2, glu=True, rho=0.15, mode="topk",
+                                     share=0.15, L=80, stack="lookahead"),
 }
 NCOPY = 8
 NX = 200
@@ -328,6 +337,120 @@ def run_ours(args, W, rank, world):
     return res, copies
 
 
+def run_stack(args, W, rank, world):
+    """K tokens through the whole L-layer stack (one cs_decode_stack call each,
+    replaying the library's cached graph), fresh x per token."""
+    import torch
+    import contextual_sparsity_sparse_gb300 as cs
+    import synth
+    import synth.device as synthdev
+    from contextual_sparsity_sparse_gb300 import build as cb
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    cb.build()
+    synthdev.build()
+    d, f, r, L = W["d"], W["f"], W["r"], W["L"]
+    k = synth.ceil_k(f, W["share"])
+    tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}[W["dt"]]
+    sd = 1 / math.sqrt(d)
+    layers, preds, keep = [], [], []
+    for l in range(L):
+        t = {}
+        for name, which, rows, cols in (("w_gate", synth.W_GATE, f, d), ("w_down_t", synth.W_DOWN_T, f, d),
+                                        ("p_down", synth.P_DOWN, r, d), ("p_up", synth.P_UP, f, r)):
+            t[name] = torch.empty((rows, cols), dtype=tdt, device="cuda")
+            synthdev.fill_normal(t[name], 0, synth.tensor_id(l, which), sd)
+        if W["glu"]:
+            t["w_up"] = torch.empty((f, d), dtype=tdt, device="cuda")
+            synthdev.fill_normal(t["w_up"], 0, synth.tensor_id(l, synth.W_UP), sd)
+        t["bias"] = torch.from_numpy(synth.zipf_bias(0, l, f, W["rho"])).cuda()
+        layers.append(cs.FfnLayer(t["w_gate"], t["w_down_t"], w_up=t.get("w_up"), bias=t["bias"]))
+        preds.append(cs.Predictor(t["p_down"], t["p_up"]))
+        keep.append(t)
+    torch.cuda.synchronize()
+    NXS = 64
+    X = torch.from_numpy(synth.x_normal(5000 + rank, NXS, d)).cuda()
+    x = torch.empty(d, device="cuda")
+    sm, sp = torch.cuda.Stream(), torch.cuda.Stream()
+    ws = cs.Workspace(d, f, r, stream=sm)
+    params = cs.select_params(cs.CS_SEL_TOPK, k)
+    mode = cs.CS_STACK_LOOKAHEAD if W["stack"] == "lookahead" else cs.CS_STACK_SEQUENTIAL
+
+    def step(i):
+        x.copy_(X[i % NXS], non_blocking=True)
+        cs.cs_decode_stack(layers, preds, x, 0.1, params, mode, ws, s_main=sm, s_pred=sp)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(sm):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    sm.synchronize()
+    K = max(1, args.steps)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = Clocks(dev)
+    clk.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(sm):
+        e0.record(sm)
+        for i in range(K):
+            step(i)
+        e1.record(sm)
+    e1.synchronize()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    assert cs.cs_get_device_error(ws, stream=sm) == 0
+    # e2e through the API with host buffers
+    KE = min(K, 50)
+    xh = torch.from_numpy(synth.x_normal(6000 + rank, NXS, d)).pin_memory()
+    yh = torch.empty((NXS, d)).pin_memory()
+    with torch.cuda.stream(sm):
+        for i in range(3):
+            x.copy_(xh[i], non_blocking=True)
+            cs.cs_decode_stack(layers, preds, x, 0.1, params, mode, ws, s_main=sm, s_pred=sp)
+            yh[i].copy_(x, non_blocking=True)
+    sm.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(sm):
+        for i in range(KE):
+            x.copy_(xh[i % NXS], non_blocking=True)
+            cs.cs_decode_stack(layers, preds, x, 0.1, params, mode, ws, s_main=sm, s_pred=sp)
+            yh[i % NXS].copy_(x, non_blocking=True)
+    sm.synchronize()
+    e2e_s = time.perf_counter() - t0
+    tot_b, ffn_b = step_bytes(W, k)
+    per_token = L * tot_b
+    hbm, src = peaks()
+    step_s = ms / 1e3 / K
+    return {
+        "metric": METRIC, "value": world * K / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": L, "d": d, "f": f, "r": r, "k": k, "selection": "topk",
+                   "stack": W["stack"], "weights": {0: "f32", 1: "f16", 2: "bf16"}[W["dt"]],
+                   "gated": W["glu"], "accumulate": "f32", "batch": 1, "global_batch": world,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: the stack's weights ({L * (2 + W['glu']) * f * d * (4 if W['dt'] == 0 else 2) / 1e9:.0f} GB) are read once per token",
+                   "step": "one token through every layer: cs_decode_stack (graph replay), fresh x per token"},
+        "clocks": clocks,
+        "gpu_launches": K * L * (5 if W["stack"] else 5),
+        "roofline": {"bound": "hbm", "kernel": "whole decode step (predictor, select, gathered FFN of every layer)",
+                     "achieved": per_token / step_s / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": per_token / step_s / 1e9 / hbm,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)", "bytes_per_launch": per_token,
+                     "avg_launch_us": step_s * 1e6, "traffic": None},
+        "e2e": {"value": world * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * d,
+                "d2h_bytes_per_step": 4 * d, "steps": KE,
+                "how": "per token: pinned H2D of x, cs_decode_stack, D2H of x_L; wall clock"},
+    }
+
+
 def oracle_step_inputs(W, layer_index=0):
     import numpy as np
     import oracle
@@ -379,24 +502,29 @@ def main():
             return
         n, el, cores = time_oracle(W, budget_s=1e9, max_steps=max(1, args.warmup))
         n, el, cores = time_oracle(W, budget_s=1e9, max_steps=max(1, args.steps))
-        v = n / el
+        v = n / el / W.get("L", 1)
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * el / n, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "d": W["d"], "f": W["f"], "r": W["r"]},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{n} decode steps (predict, select, gathered FFN) of the workload, fp64 CPU oracle"},
+                             "sample": f"{n} single-layer decode steps (predict, select, gathered FFN; layer 0) of the workload, fp64 CPU oracle" + (f", scaled to {W['L']} layers" if "L" in W else "")},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
-    res, _ = run_ours(args, W, rank, world)
+    if "L" in W:
+        res = run_stack(args, W, rank, world)
+    else:
+        res, _ = run_ours(args, W, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, el, cores = time_oracle(W, args.cpu_sample_s)
-        res["cpu_baseline"] = {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                               "sample": f"{n} decode steps of the workload in {el:.1f} s (fp64 CPU oracle, {cores} threads)"}
+        L = W.get("L", 1)
+        res["cpu_baseline"] = {"value": n / el / L, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "sample": f"{n} single-layer decode steps (layer 0) in {el:.1f} s, fp64 CPU oracle on {cores} threads"
+                                         + (f", scaled to {L} layers" if L > 1 else "")}
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

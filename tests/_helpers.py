@@ -99,7 +99,7 @@ def score_bounds(P: HostLayer, x):
     h, s = oracle.predict(P.oracle_pred(), x)
     c = 10 * 2.0 ** -24 * 8.0
     dh = c * np.sqrt((pd * pd) @ (x * x))
-    eps = c * np.sqrt((pu * pu) @ (h * h)) + 10 * np.sqrt((pu * pu) @ (dh * dh)) + 2.0 ** -24 * np.abs(s)
+    eps = c * np.sqrt((pu * pu) @ (h * h)) + np.sqrt((pu * pu) @ (dh * dh)) + 2.0 ** -24 * np.abs(s)
     return s, eps
 
 
@@ -128,3 +128,36 @@ def pick_tau_with_gap(s, eps, q):
                 if s[hi] - s[lo] > 2 * (eps[lo] + eps[hi]):
                     return np.float32((s[lo] + s[hi]) / 2)
     raise AssertionError("no decidable threshold")
+
+
+def stack_inputs(L, d, f, r, dt, glu=False, seed=0, rho=0.1):
+    Hs = [HostLayer(d, f, r, dt, glu=glu, seed=seed, layer=l, rho=rho) for l in range(L)]
+    dev = [H.device() for H in Hs]
+    return Hs, [a for a, _ in dev], [b for _, b in dev]
+
+
+def oracle_stack_k(Hs, x0, mode, k0, scale):
+    """A k at which every layer's top-k boundary is decided beyond rounding,
+    with the oracle's output and trace at that k.  x_l comes from the oracle
+    run on the first l layers; the bound is widened for the fp32 drift of the
+    GPU's x_l."""
+    layers = [H.oracle_layer() for H in Hs]
+    preds = [H.oracle_pred() for H in Hs]
+    for k in range(k0, k0 + 64):
+        xs = [np.asarray(x0, np.float64)]
+        for l in range(1, len(Hs)):
+            xs.append(oracle.stack(layers[:l], preds[:l], x0, mode=mode, k=k, resid_scale=scale))
+        ok = True
+        for l, H in enumerate(Hs):
+            xin = xs[l - 1] if (mode == oracle.LOOKAHEAD and l > 0) else xs[l]
+            s, eps = score_bounds(H, xin)
+            eps = 4 * eps + 1e-6 * np.abs(s).max()
+            order = np.argsort(-s, kind="stable")
+            a, b = order[k - 1], order[k]
+            if s[a] - s[b] <= eps[a] + eps[b]:
+                ok = False
+                break
+        if ok:
+            xo, tr = oracle.stack(layers, preds, x0, mode=mode, k=k, resid_scale=scale, trace=True)
+            return k, xo, tr
+    raise AssertionError("no decidable k")
