@@ -12,7 +12,7 @@
 // Design.  W_down is stored transposed, so each chosen neuron needs two (or
 // three, gated) contiguous rows of d elements.  A persistent grid of one CTA
 // per SM splits the ascending index list into contiguous chunks.  Each of the
-// 256 threads owns fixed 16-byte column vectors of every row, and gathers
+// 512 threads owns fixed 16-byte column vectors of every row, and gathers
 // exactly those vectors of the chunk's rows with per-thread asynchronous
 // copies (cp.async) into its own slots of a shared-memory ring, SG groups of
 // NG neurons ahead.  Because a thread only ever reads the slots it filled,
@@ -31,7 +31,7 @@ namespace cs {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kNgMax = 4;                 // neurons per group (max)
 constexpr int kStageMax = 16;             // ring slots (ng * sg)
