@@ -335,32 +335,51 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
     }
 }
 
-// y[b, col] = (resid[b, col] + scale *) sum_{c < G} part[c, b, col], c ascending
-// within each of 8 warps, warps combined in order.
-__global__ void __launch_bounds__(256)
+// y[b, col] = (resid[b, col] + scale *) sum_{c < G} part[c, b, col].  Warp w
+// of 16 adds partials c = w, w + 16, ... in ascending order, every load of a
+// thread in flight at once; the 16 warp sums are then added in warp order, so
+// y is bit-reproducible.  Lane l of a CTA owns columns 2l, 2l + 1 of its
+// 64-column slice.
+constexpr int kRedWarps = 16;
+constexpr int kRedUnroll = 16;   // partials per warp kept in flight (G <= 256 in one pass)
+
+__global__ void __launch_bounds__(kRedWarps * 32)
 ffn_reduce_kernel(const float *__restrict__ part, int G, int B, int d, int dp,
                   const float *__restrict__ resid, float scale, float *__restrict__ y) {
-    __shared__ float red[8][33];
+    __shared__ float2 red[kRedWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int col = blockIdx.x * 32 + lane;
+    const int col = blockIdx.x * 64 + 2 * lane;
     const int b = blockIdx.y;
     pdl_launch_dependents();
     pdl_wait();
-    float acc = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
     if (col < d) {
+        // col + 1 < dp (dp is a multiple of 8), so the pair load stays inside the row
         const float *p = part + (size_t)b * dp + col;
         const size_t stride = (size_t)B * dp;
-#pragma unroll 4
-        for (int cc = warp; cc < G; cc += 8) acc += __ldg(p + cc * stride);
+        float2 t[kRedUnroll];
+#pragma unroll
+        for (int u = 0; u < kRedUnroll; ++u) {
+            const int c = warp + kRedWarps * u;
+            t[u] = c < G ? __ldg(reinterpret_cast<const float2 *>(p + c * stride)) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kRedUnroll; ++u) { acc.x += t[u].x; acc.y += t[u].y; }
+        for (int c = warp + kRedWarps * kRedUnroll; c < G; c += kRedWarps) {
+            const float2 v = __ldg(reinterpret_cast<const float2 *>(p + c * stride));
+            acc.x += v.x;
+            acc.y += v.y;
+        }
     }
     red[warp][lane] = acc;
     __syncthreads();
     if (warp == 0 && col < d) {
-        float s = 0.f;
+        float2 s = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) s += red[w][lane];
+        for (int w = 0; w < kRedWarps; ++w) { s.x += red[w][lane].x; s.y += red[w][lane].y; }
         const size_t o = (size_t)b * d + col;
-        y[o] = resid ? fmaf(scale, s, resid[o]) : s;
+        y[o] = resid ? fmaf(scale, s.x, resid[o]) : s.x;
+        if (col + 1 < d) y[o + 1] = resid ? fmaf(scale, s.y, resid[o + 1]) : s.y;
     }
 }
 
@@ -425,8 +444,8 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     const int tb = a.B >= 2 ? 2 : 1;
     cudaError_t e = tb == 2 ? pick_mode<T, 2>(a, k, smem, s) : pick_mode<T, 1>(a, k, smem, s);
     if (e != cudaSuccess) return e;
-    dim3 g((a.d + 31) / 32, a.B);
-    return launch(ffn_reduce_kernel, g, dim3(256), 0, s, pdl_enabled(),
+    dim3 g((a.d + 63) / 64, a.B);
+    return launch(ffn_reduce_kernel, g, dim3(kRedWarps * 32), 0, s, pdl_enabled(),
                   static_cast<const float *>(a.part), a.G, a.B, a.d, a.dp, a.resid, a.scale, a.y);
 }
 

@@ -7,26 +7,27 @@
 // Activation Predictors", first section (a neuron is active when its gate
 // pre-activation passes the ReLU).
 //
-// One CTA of 1024 threads per token row; the row's scores sit in shared
-// memory.  Ranking: larger score first, equal scores by lower id, -0 == +0,
-// NaN below -inf (as order-preserving 32-bit keys).  Top-k needs the k-th key
-// K and the number of ties at K to take:
-//   1. min / max of the finite scores (block reduction);
+// Ranking: larger score first, equal scores by lower id, -0 == +0, NaN below
+// -inf (as order-preserving 32-bit keys).  Top-k needs the k-th key K and the
+// number of ties at K to take:
+//   1. min / max of the finite scores;
 //   2. a 4096-bucket histogram of a monotone linear map of the score (NaN,
 //      -inf and +inf get their own end buckets), so buckets hold a handful of
 //      scores for any smooth distribution;
 //   3. a suffix scan finds the bucket B holding the k-th score;
-//   4. B's members are ranked exactly against each other (key, then id);
-//      the member of rank k-1 gives K and the number of ties to take.  A
-//      bucket with more than 2048 members (a mass of equal scores) is
-//      resolved instead by a radix select on the exact keys of its members.
-// Compaction is in ascending id order: each warp owns a contiguous range taken
-// 32 ids at a time; warp ballots give in-warp ranks (and the mask words), one
-// scan over the 32 warps gives (a) the K-ties before each warp, so the lowest
-// ids win, and (b) each warp's output position.  No global atomics and no
-// grid-wide synchronisation: a grid barrier costs microseconds here.
-#include <cstdlib>
-#include <utility>
+//   4. B's members are ranked exactly against each other (key, then id); the
+//      member of rank k-1 gives K and the number of ties to take.  A bucket
+//      with more than 64 members (a mass of near-equal scores) is resolved
+//      instead by a radix select on the exact keys of its members.
+// Compaction is in ascending id order: every thread owns a contiguous run of
+// ids, so one exclusive scan of the packed (greater, tie) counts gives each
+// thread its output position and the ties before it (the lowest ids win).
+//
+// Rows of f >= 2048 scores run on a cluster of 8 CTAs (the per-element passes
+// split 8 ways, the CTAs exchanging through distributed shared memory);
+// shorter rows on one CTA.  Neither takes a global atomic or a grid-wide
+// barrier.
+#include <cooperative_groups.h>
 
 #include "cs_internal.cuh"
 
@@ -34,9 +35,7 @@ namespace cs {
 
 namespace {
 
-constexpr int kSelThreads = 1024;
 constexpr int kBuckets = 4096;
-constexpr int kCandMax = 2048;
 
 // Order-preserving key: larger score -> larger key.  -0 is folded onto +0;
 // NaN maps to 0, below the key of -inf (0x007fffff).
@@ -47,195 +46,230 @@ __device__ __forceinline__ uint32_t score_key(float s) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ int bucket_of(float s, float smin, float scale) {
-    if (s != s) return 0;
-    if (s == -INFINITY) return 1;
-    if (s == INFINITY) return kBuckets - 1;
-    const float t = (s - smin) * scale;  // monotone in s
-    int b = (int)t;
-    b = b < 0 ? 0 : (b > kBuckets - 4 ? kBuckets - 4 : b);
-    return 2 + b;
-}
+// ---------------------------------------------------------------------------
+// Row kernel: one CTA of 1024 threads per token row; thread t owns the
+// contiguous ids [t*E, t*E + E), E = ceil(f / 1024) <= ET, held in registers.
+// Every per-element pass is a short register loop and every block-wide step
+// a warp-shuffle reduction or one prefix scan.
+// ---------------------------------------------------------------------------
+constexpr int kRowThreads = 1024;
+constexpr int kCandSmall = 64;
 
-__device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
-
-__device__ __forceinline__ float block_min(float v, float *wred) {
+__device__ __forceinline__ float warp_min(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
-    if ((threadIdx.x & 31) == 0) wred[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = wred[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fminf(r, wred[w]);
-    __syncthreads();
-    return r;
+    return v;
 }
-
-__device__ __forceinline__ float block_max(float v, float *wred) {
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-    if ((threadIdx.x & 31) == 0) wred[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = wred[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, wred[w]);
-    __syncthreads();
-    return r;
+    return v;
+}
+__device__ __forceinline__ int warp_isum(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
 }
 
-__global__ void __launch_bounds__(kSelThreads)
-select_kernel(const float *__restrict__ scores, int f, int kind, int k, float tau,
-              int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
-              uint32_t *__restrict__ mask) {
-    extern __shared__ uint32_t sm[];
-    float *vals = reinterpret_cast<float *>(sm);      // [f] scores
-    uint32_t *hist = sm + f;                           // [kBuckets]; later candidates
-    __shared__ int wsum[32];
-    __shared__ float wred[32];
-    __shared__ uint32_t tots[kSelThreads];
-    __shared__ uint32_t above[kSelThreads];
-    __shared__ uint32_t s_bucket, s_rem, s_pivot, s_need, s_ncand, s_fill;
-
-    const int b = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int words = (f + 31) >> 5;
-    const float *s = scores + (size_t)b * f;
-    int32_t *out = idx + (size_t)b * ld_idx;
-
-    pdl_launch_dependents();  // single CTA: let the consumer kernel get resident
-    pdl_wait();  // scores come from the previous kernel
-
-    float lo = INFINITY, hi = -INFINITY;
-    if ((f & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & 15) == 0) {
-        // all of a thread's 16-byte loads are in flight together
-        const float4 *s4 = reinterpret_cast<const float4 *>(s);
-        float4 *v4 = reinterpret_cast<float4 *>(vals);
-        const int f4 = f >> 2;
-#pragma unroll 8
-        for (int j = tid; j < f4; j += kSelThreads) {
-            const float4 v = __ldg(s4 + j);
-            v4[j] = v;
-            const float e[4] = {v.x, v.y, v.z, v.w};
+// Exclusive prefix sum of one unsigned value per thread (wraps modulo 2^32,
+// so two 16-bit counts packed in one word scan independently).
+__device__ __forceinline__ uint32_t block_excl_scan_u32(uint32_t v, uint32_t *wsum, uint32_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int nw = kRowThreads / 32;
+    uint32_t inc = v;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (e[q] - e[q] == 0.f) { lo = fminf(lo, e[q]); hi = fmaxf(hi, e[q]); }
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t n = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t n = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += n;
         }
-    } else {
-#pragma unroll 8
-        for (int j = tid; j < f; j += kSelThreads) {
-            const float v = __ldg(s + j);
-            vals[j] = v;
-            if (v - v == 0.f) {  // finite
-                lo = fminf(lo, v);
-                hi = fmaxf(hi, v);
-            }
-        }
+        wsum[lane] = w;
     }
     __syncthreads();
+    const uint32_t base = warp > 0 ? wsum[warp - 1] : 0u;
+    *total = wsum[nw - 1];
+    __syncthreads();
+    return base + inc - v;
+}
 
-    uint32_t pivot = 0u;
-    int need = 0;
-    const int kk = k < 0 ? 0 : (k > f ? f : k);
-    if (kind == SEL_TOPK && kk > 0 && kk < f) {
-        const float smin = block_min(lo, wred);
-        const float smax = block_max(hi, wred);
-        const float scale = smax > smin ? (float)(kBuckets - 4) / (smax - smin) : 0.f;
-        for (int i = tid; i < kBuckets; i += kSelThreads) hist[i] = 0u;
-        __syncthreads();
-        for (int j = tid; j < f; j += kSelThreads) atomicAdd(&hist[bucket_of(vals[j], smin, scale)], 1u);
-        __syncthreads();
-        // bucket of the kk-th largest: thread t owns buckets [4t, 4t+4)
-        {
-            constexpr int BPT = kBuckets / kSelThreads;
-            uint32_t cb[BPT], tot = 0;
+// Bucket of a score for the row kernel: NaN 0, -inf 1, +inf kBuckets-1, a
+// finite s 2 + round(clamp(s * scale + off, 0, kBuckets - 4)).  Monotone in s:
+// a correctly rounded fma of a linear map with scale >= 0, a clamp and a
+// round-to-nearest are each non-decreasing.  The rounding adds 1.5 * 2^23,
+// which leaves round(t) in the low mantissa bits (0 <= t < 2^22).
+__device__ __forceinline__ int bucket_fast(float s, float scale, float off) {
+    float t = fmaf(s, scale, off);
+    t = fminf(fmaxf(t, 0.f), (float)(kBuckets - 4));
+    int b = __float_as_int(t + 12582912.f) - 0x4B400000 + 2;
+    b = fabsf(s) == INFINITY ? (s > 0.f ? kBuckets - 1 : 1) : b;
+    return s != s ? 0 : b;
+}
+
+// The ranking of score keys as float comparisons against the pivot's value pv
+// (key(s) > key(p) iff s > p for non-NaN s, p; -0 == +0 either way).  A NaN
+// pivot (key 0) makes every NaN a tie and every other score greater.
+__device__ __forceinline__ void rank_flags(float s, float pv, bool pnan, bool &gt, bool &eq) {
+    const bool snan = s != s;
+    gt = pnan ? !snan : s > pv;
+    eq = pnan ? snan : s == pv;
+}
+
+template <int ET, int KIND>
+__global__ void __launch_bounds__(kRowThreads, 1)
+select_row_kernel(const float *__restrict__ scores, int f, int k, float tau,
+                  int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
+                  uint32_t *__restrict__ mask) {
+    __shared__ __align__(16) uint32_t hist[kBuckets];
+    __shared__ uint32_t ckey[kCandSmall], cid[kCandSmall];
+    __shared__ float wlo[32], whi[32];
+    __shared__ uint32_t usum[32];
+    __shared__ uint32_t s_bucket, s_rem, s_ncand, s_fill, s_pivot, s_need;
+    __shared__ uint32_t bits[kSelectMaxF / 32];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x;
+    const float *s = scores + (size_t)b * f;
+    int32_t *out = idx + (size_t)b * ld_idx;
+    const int words = (f + 31) >> 5;
+    const int E = (f + kRowThreads - 1) / kRowThreads;
+    const int j0 = tid * E;
+    const int ne = max(0, min(E, f - j0));
+
+    if (tid == 0) s_fill = 0u;
+    if (mask)
+        for (int w = tid; w < words; w += kRowThreads) bits[w] = 0u;
+
+    pdl_launch_dependents();  // single CTA: let the consumer kernel get resident
+    pdl_wait();               // scores come from the previous kernel
+
+    float v[ET];
+    const bool vec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & 15) == 0;
 #pragma unroll
-            for (int q = 0; q < BPT; ++q) { cb[q] = hist[tid * BPT + q]; tot += cb[q]; }
-            // count of members in buckets above this thread's: a scan in
-            // reversed thread order, handed back to the owning thread
-            tots[tid] = tot;
-            __syncthreads();
-            int total_unused;
-            const int excl = block_excl_scan((int)tots[kSelThreads - 1 - tid], wsum, &total_unused);
-            above[kSelThreads - 1 - tid] = (uint32_t)excl;
-            __syncthreads();
-            uint32_t run = above[tid];
-            const uint32_t rem = (uint32_t)kk;
-#pragma unroll
-            for (int q = BPT - 1; q >= 0; --q) {
-                if (run < rem && run + cb[q] >= rem) {
-                    s_bucket = (uint32_t)(tid * BPT + q);
-                    s_rem = rem - run;
-                    s_ncand = cb[q];
-                }
-                run += cb[q];
-            }
-            __syncthreads();
-        }
-        const int B_ = (int)s_bucket;
-        const uint32_t rem = s_rem;       // how many of bucket B_ are taken (>= 1)
-        const uint32_t ncand = s_ncand;
-        if (ncand <= (uint32_t)kCandMax) {
-            // gather bucket B_'s members as (key, id), rank them exactly
-            uint32_t *ckey = hist;                 // [kCandMax]
-            uint32_t *cid = hist + kCandMax;       // [kCandMax]
-            if (tid == 0) s_fill = 0u;
-            __syncthreads();
-            for (int j = tid; j < f; j += kSelThreads) {
-                const float v = vals[j];
-                if (bucket_of(v, smin, scale) == B_) {
-                    const uint32_t p = atomicAdd(&s_fill, 1u);
-                    ckey[p] = score_key(v);
-                    cid[p] = (uint32_t)j;
-                }
-            }
-            __syncthreads();
-            for (int c = tid; c < (int)ncand; c += kSelThreads) {
-                const uint32_t kc = ckey[c], ic = cid[c];
-                uint32_t rank = 0;
-                for (int o = 0; o < (int)ncand; ++o) {
-                    const uint32_t ko = ckey[o];
-                    rank += (ko > kc) || (ko == kc && cid[o] < ic);
-                }
-                if (rank == rem - 1u) s_pivot = kc;
-            }
-            __syncthreads();
-            // ties at the pivot that rank inside the top kk
-            int gtc = 0;
-            for (int c = tid; c < (int)ncand; c += kSelThreads) gtc += ckey[c] > s_pivot;
-            int tot_gt;
-            block_excl_scan(gtc, wsum, &tot_gt);
-            pivot = s_pivot;
-            need = (int)rem - tot_gt;
+    for (int q = 0; q < ET; q += 4) {
+        if (vec && q + 4 <= ne) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(s + j0 + q));
+            v[q] = t.x; v[q + 1] = t.y; v[q + 2] = t.z; v[q + 3] = t.w;
         } else {
-            // a mass of near-equal scores: radix select on the members' keys
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[q + e] = q + e < ne ? __ldg(s + j0 + q + e) : 0.f;
+        }
+    }
+
+    const int kk = k < 0 ? 0 : (k > f ? f : k);
+    float pv = 0.f;      // pivot value (top-k)
+    bool pnan = false;   // pivot is NaN
+    int need = 0;        // ties at the pivot to take, lowest ids first
+    if (KIND == SEL_TOPK && kk > 0 && kk < f) {
+        float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < ET; ++e)
+            if (e < ne && fabsf(v[e]) < INFINITY) { lo = fminf(lo, v[e]); hi = fmaxf(hi, v[e]); }
+        lo = warp_min(lo);
+        hi = warp_max(hi);
+        if (lane == 0) { wlo[warp] = lo; whi[warp] = hi; }
+        reinterpret_cast<uint4 *>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+        const float smin = warp_min(wlo[lane]), smax = warp_max(whi[lane]);
+        const float scale = smax > smin ? (float)(kBuckets - 4) / (smax - smin) : 0.f;
+        const float off = -smin * scale;
+#pragma unroll
+        for (int e = 0; e < ET; ++e)
+            if (e < ne) atomicAdd(&hist[bucket_fast(v[e], scale, off)], 1u);
+        __syncthreads();
+        // thread t owns bins [4t, 4t + 4); members above them = total - prefix - own
+        static_assert(kBuckets == 4 * kRowThreads, "four bins per thread");
+        const uint4 hb = reinterpret_cast<const uint4 *>(hist)[tid];
+        const uint32_t cb[4] = {hb.x, hb.y, hb.z, hb.w};
+        const uint32_t own = hb.x + hb.y + hb.z + hb.w;
+        uint32_t total;
+        const uint32_t pre = block_excl_scan_u32(own, usum, &total);
+        uint32_t run = total - pre - own;
+#pragma unroll
+        for (int q = 3; q >= 0; --q) {
+            if (run < (uint32_t)kk && run + cb[q] >= (uint32_t)kk) {
+                s_bucket = (uint32_t)(4 * tid + q);
+                s_rem = (uint32_t)kk - run;
+                s_ncand = cb[q];
+            }
+            run += cb[q];
+        }
+        __syncthreads();
+        const int B_ = (int)s_bucket;
+        const uint32_t rem = s_rem, ncand = s_ncand;
+        uint32_t pkey;
+        if (ncand <= (uint32_t)kCandSmall) {
+            // the bucket's members, ranked exactly (key descending, id ascending)
+#pragma unroll
+            for (int e = 0; e < ET; ++e) {
+                if (e < ne && bucket_fast(v[e], scale, off) == B_) {
+                    const uint32_t p = atomicAdd(&s_fill, 1u);
+                    ckey[p] = score_key(v[e]);
+                    cid[p] = (uint32_t)(j0 + e);
+                }
+            }
+            __syncthreads();
+            // warp w ranks members w, w + 32, ...: lanes split the comparisons
+            for (int c = warp; c < (int)ncand; c += kRowThreads / 32) {
+                const uint32_t kc = ckey[c], ic = cid[c];
+                int rk = 0, gt = 0;
+                for (int o = lane; o < (int)ncand; o += 32) {
+                    const uint32_t ko = ckey[o];
+                    rk += (ko > kc) || (ko == kc && cid[o] < ic);
+                    gt += ko > kc;
+                }
+                rk = warp_isum(rk);
+                gt = warp_isum(gt);
+                if (lane == 0 && rk == (int)rem - 1) {
+                    s_pivot = kc;
+                    s_need = rem - (uint32_t)gt;
+                }
+            }
+            __syncthreads();
+            pkey = s_pivot;
+            need = (int)s_need;
+        } else {
+            // a crowded bucket (near-equal scores): radix select over its
+            // members' exact keys, eight bits at a time
             uint32_t prefix = 0u, pmask = 0u, r_ = rem;
-            uint32_t *h = hist;  // 256 bins
             for (int pass = 0; pass < 4; ++pass) {
                 const int shift = 24 - 8 * pass;
-                if (tid < 256) h[tid] = 0u;
+                if (tid < 256) hist[tid] = 0u;
                 __syncthreads();
-                for (int j = tid; j < f; j += kSelThreads) {
-                    const float v = vals[j];
-                    const uint32_t key = score_key(v);
-                    if (bucket_of(v, smin, scale) == B_ && (key & pmask) == prefix)
-                        atomicAdd(&h[(key >> shift) & 255u], 1u);
+#pragma unroll
+                for (int e = 0; e < ET; ++e) {
+                    if (e < ne && bucket_fast(v[e], scale, off) == B_) {
+                        const uint32_t key = score_key(v[e]);
+                        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+                    }
                 }
                 __syncthreads();
-                if (tid < 256) {
-                    // bins from the top: thread t looks at digit 255 - t
-                    const uint32_t c = h[255 - tid];
-                    uint32_t inc = c;
+                if (warp == 0) {
+                    // lane l holds digits 255 - 8l - i, i = 0..7 (descending)
+                    uint32_t c8[8], sum = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) { c8[i] = hist[255 - 8 * lane - i]; sum += c8[i]; }
+                    uint32_t inc = sum;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
                         const uint32_t nn = __shfl_up_sync(kFull, inc, o);
                         if (lane >= o) inc += nn;
                     }
-                    if (lane == 31) wsum[tid >> 5] = (int)inc;
-                    named_sync(1, 256);
-                    uint32_t base_ = 0;
-                    for (int w = 0; w < (tid >> 5); ++w) base_ += (uint32_t)wsum[w];
-                    const uint32_t ge = base_ + inc, gt = ge - c;
-                    if (ge >= r_ && gt < r_) {
-                        s_pivot = 255u - (uint32_t)tid;
-                        s_need = r_ - gt;
+                    uint32_t run8 = inc - sum;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (run8 < r_ && run8 + c8[i] >= r_) {
+                            s_pivot = (uint32_t)(255 - 8 * lane - i);
+                            s_need = r_ - run8;
+                        }
+                        run8 += c8[i];
                     }
                 }
                 __syncthreads();
@@ -244,420 +278,436 @@ select_kernel(const float *__restrict__ scores, int f, int kind, int k, float ta
                 r_ = s_need;
                 __syncthreads();
             }
-            pivot = prefix;
+            pkey = prefix;
             need = (int)r_;
         }
+        // back from the key to the value (keys of -0 and NaN never arise here
+        // except key 0, a NaN pivot)
+        pnan = pkey == 0u;
+        pv = __uint_as_float((pkey & 0x80000000u) ? (pkey & 0x7fffffffu) : ~pkey);
     }
 
-    // compaction: warp w owns ids [w*S, (w+1)*S), S a multiple of 32, taken
-    // 32 at a time; ballots give in-warp ranks and, directly, the mask words
-    const int nw = kSelThreads / 32;
-    const int S = (((f + nw - 1) / nw) + 31) & ~31;
-    const int wbeg = min(warp_id() * S, f), wend = min(wbeg + S, f);
-    const unsigned lt = (1u << lane) - 1u;
-    auto flags = [&](int j, bool &gt, bool &eq) {
-        gt = false;
-        eq = false;
-        if (j >= wend) return;
-        const float v = vals[j];
-        if (kind == SEL_TOPK) {
-            if (kk == f) gt = true;
-            else if (kk > 0) { const uint32_t key = score_key(v); gt = key > pivot; eq = key == pivot; }
-        } else if (kind == SEL_THRESHOLD) {
-            gt = v >= tau;
+    // compaction: packed (greater, tie) counts of this thread's chunk -> one scan
+    auto flags = [&](float x, bool &gt, bool &eq) {
+        if (KIND == SEL_TOPK) {
+            if (kk == f) { gt = true; eq = false; }
+            else if (kk == 0) { gt = false; eq = false; }
+            else rank_flags(x, pv, pnan, gt, eq);
+        } else if (KIND == SEL_THRESHOLD) {
+            gt = x >= tau;
+            eq = false;
         } else {
-            gt = v > 0.f;
+            gt = x > 0.f;
+            eq = false;
         }
     };
-    int w_gt = 0, w_eq = 0;
-    for (int base = wbeg; base < wend; base += 32) {
-        bool gt, eq;
-        flags(base + lane, gt, eq);
-        w_gt += __popc(__ballot_sync(kFull, gt));
-        w_eq += __popc(__ballot_sync(kFull, eq));
-    }
-    // per-warp totals -> exclusive prefixes (ties first: the lowest ids win)
-    __shared__ int s_eqb[32], s_selb[32], s_total;
-    if (lane == 0) { tots[warp_id()] = (uint32_t)w_gt; above[warp_id()] = (uint32_t)w_eq; }
-    __syncthreads();
-    if (warp_id() == 0) {
-        const int g_ = (int)tots[lane], e_ = (int)above[lane];
-        int eb = e_;
+    uint32_t cg = 0, ce = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) { const int nn = __shfl_up_sync(kFull, eb, o); if (lane >= o) eb += nn; }
-        eb -= e_;                                   // ties in earlier warps
-        const int take = max(0, min(e_, need - eb));
-        const int sel = g_ + take;
-        int sb = sel;
+    for (int e = 0; e < ET; ++e) {
+        if (e < ne) {
+            bool gt, eq;
+            flags(v[e], gt, eq);
+            cg += gt;
+            ce += eq;
+        }
+    }
+    // f <= kSelectMaxF < 2^16: both block totals fit their 16-bit halves
+    static_assert(kSelectMaxF < 65536, "packed counts");
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan_u32((cg << 16) | ce, usum, &tot);
+    int eq_run = (int)(ex & 0xffffu);
+    int pos = (int)(ex >> 16) + min(eq_run, need);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) { const int nn = __shfl_up_sync(kFull, sb, o); if (lane >= o) sb += nn; }
-        s_eqb[lane] = eb;
-        s_selb[lane] = sb - sel;
-        if (lane == 31) s_total = sb;
+    for (int e = 0; e < ET; ++e) {
+        if (e < ne) {
+            bool gt, eq;
+            flags(v[e], gt, eq);
+            const bool take = gt || (eq && eq_run < need);
+            eq_run += eq;
+            if (take) {
+                const int j = j0 + e;
+                out[pos++] = j;
+                if (mask) atomicOr(&bits[j >> 5], 1u << (j & 31));
+            }
+        }
     }
-    __syncthreads();
-    int eq_run = s_eqb[warp_id()], pos = s_selb[warp_id()];
-    for (int base = wbeg; base < wend; base += 32) {
-        bool gt, eq;
-        const int j = base + lane;
-        flags(j, gt, eq);
-        const unsigned be = __ballot_sync(kFull, eq);
-        const bool take = gt || (eq && eq_run + __popc(be & lt) < need);
-        const unsigned bs = __ballot_sync(kFull, take);
-        if (take) out[pos + __popc(bs & lt)] = j;
-        if (mask && lane == 0) mask[(size_t)b * words + (base >> 5)] = bs;
-        eq_run += __popc(be);
-        pos += __popc(bs);
+    if (tid == kRowThreads - 1) count[b] = (int)(tot >> 16) + min((int)(tot & 0xffffu), need);
+    if (mask) {
+        __syncthreads();
+        for (int w = tid; w < words; w += kRowThreads) mask[(size_t)b * words + w] = bits[w];
     }
-    if (tid == 0) count[b] = s_total;
 }
 
 // ---------------------------------------------------------------------------
-// Cluster variant: one thread-block cluster of kCl CTAs per token row.  CTA r
-// owns the 32-aligned id slice [r*S, (r+1)*S).  The same four steps run with
-// the element work split kCl ways; the CTAs exchange min/max, histogram
-// slices, the pivot bucket's members and their per-CTA counts through
-// distributed shared memory, separated by hardware cluster barriers (no global
-// atomics, no grid-wide barrier).
+// Cluster row kernel: one cluster of kCl CTAs x 256 threads per token row.
+// CTA r owns the 32-aligned id slice [r*SL, r*SL + SL); thread t of it the
+// contiguous ids [t*E, t*E + E) of that slice, in registers.  The four steps
+// of the row kernel run with the per-element passes split kCl ways.  Small
+// data is pushed into every CTA's shared memory before a cluster barrier, so
+// that after it each CTA finds it locally: min / max, per-slice histogram
+// totals, the pivot bucket's members, and the (greater, tie) totals behind the
+// output offsets.  The one pull is the pivot slice's 512 bins from every CTA
+// (all loads in flight together).  Four cluster barriers in all; no shared
+// memory is touched remotely after the last one, so CTAs may leave at once.
 // ---------------------------------------------------------------------------
 constexpr int kCl = 8;
-constexpr int kClThreads = 1024;
-constexpr int kClSliceMax = 6144;            // f <= kCl * kClSliceMax
-constexpr int kClBinsPerCta = kBuckets / kCl;
+constexpr int kClT = 256;
+constexpr int kClW = kClT / 32;
+constexpr int kClBins = kBuckets / kCl;     // bins per CTA slice
+constexpr int kClMaxSlice = kSelectMaxF / kCl;
+static_assert(kClW == kCl, "warp w of a CTA handles histogram slice w");
 
 struct ClSmem {
-    float vals[kClSliceMax];
-    uint32_t hist[kBuckets];
-    uint32_t red[kClBinsPerCta];
-    uint32_t ckey[kCandMax];
-    uint32_t cid[kCandMax];
-    uint32_t wtot[32][2];
-    uint32_t loc[kClBinsPerCta];             // a remote bin slice, copied locally
-    float rlo[kCl], rhi[kCl];
-    uint32_t rtot[kCl];
-    int rgt[kCl], req[kCl];
-    float lo, hi;
-    uint32_t slice_total;
-    uint32_t ncand_fill;
-    int cta_gt, cta_eq;
-    uint32_t s_bucket, s_rem, s_ncand, s_pivot;
-    int s_need, s_base, s_eqb, s_total, s_slow;
+    uint32_t hist[kBuckets];                  // local histogram
+    uint32_t ptot[kCl][kCl];                // [source CTA][slice] partial slice totals
+    float plo[kCl], phi[kCl];               // min / max from each CTA
+    uint32_t ckey[kCl][kCandSmall];          // [source CTA] pivot-bucket members
+    uint32_t cid[kCl][kCandSmall];
+    uint32_t ccnt[kCl];
+    uint32_t pgt[kCl], peq[kCl];            // (greater, tie) totals from each CTA
+    uint32_t lkey[kCandSmall], lid[kCandSmall];
+    uint32_t rhist[256];                      // radix digits (crowded bucket)
+    uint32_t akey[kCandSmall], aid[kCandSmall];
+    uint32_t bits[kClMaxSlice / 32];
+    uint32_t usum[32];
+    float wlo[kClW], whi[kClW];
+    uint32_t nfill;
+    uint32_t bucket, rem, ncand, pivot, need;
 };
 
-__device__ __forceinline__ uint32_t cl_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cl_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// address of the same shared variable in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
-    uint32_t out;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr(p)), "r"(rank));
-    return out;
-}
-__device__ __forceinline__ uint32_t cl_ld_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float cl_ld_f32(uint32_t addr) { return __uint_as_float(cl_ld_u32(addr)); }
-__device__ __forceinline__ void cl_st_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t cl_atom_add(uint32_t addr, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-    return old;
+// Exclusive scan over a 256-thread block (unsigned, wraps modulo 2^32).
+__device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t *wsum, uint32_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t n = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    const uint32_t wv = lane < kClW ? wsum[lane] : 0u;
+    uint32_t w = wv;
+#pragma unroll
+    for (int o = 1; o < kClW; o <<= 1) {
+        const uint32_t n = __shfl_up_sync(kFull, w, o);
+        if (lane >= o) w += n;
+    }
+    const uint32_t wex = __shfl_sync(kFull, w - wv, warp);
+    *total = __shfl_sync(kFull, w, kClW - 1);
+    __syncthreads();
+    return wex + inc - v;
 }
 
-__global__ void __launch_bounds__(kClThreads)
-select_cluster_kernel(const float *__restrict__ scores, int f, int kind, int k, float tau,
-                      int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
-                      uint32_t *__restrict__ mask) {
-    extern __shared__ __align__(16) uint8_t dyn[];
-    ClSmem &S = *reinterpret_cast<ClSmem *>(dyn);
-    __shared__ int wsum[32];
-    __shared__ float wred[32];
+template <int ET, int KIND>
+__global__ void __launch_bounds__(kClT, 1)
+select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
+                 int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
+                 uint32_t *__restrict__ mask) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    __shared__ __align__(16) ClSmem S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t rank = cl_rank();
+    const int rank = (int)cl.block_rank();
     const int b = blockIdx.x / kCl;
-    const int words = (f + 31) >> 5;
-    const int SL = (((f + kCl - 1) / kCl) + 31) & ~31;
-    const int beg = min((int)rank * SL, f), end = min(beg + SL, f);
-    const int n_my = end - beg;
     const float *s = scores + (size_t)b * f;
     int32_t *out = idx + (size_t)b * ld_idx;
+    const int words = (f + 31) >> 5;
+    const int SL = (((f + kCl - 1) / kCl) + 31) & ~31;
+    const int beg = min(rank * SL, f), n_my = min(SL, f - beg);
+    const int E = (SL + kClT - 1) / kClT;
+    const int j0 = tid * E;                      // within the slice
+    const int ne = max(0, min(E, n_my - j0));
+
+    // Zero what peers add into before the first barrier; nothing here reads
+    // the scores, so it runs ahead of the wait.
+#pragma unroll
+    for (int i = tid; i < kBuckets / 4; i += kClT) reinterpret_cast<uint4 *>(S.hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (mask)
+        for (int w = tid; w < SL / 32; w += kClT) S.bits[w] = 0u;
+    if (tid == 0) S.nfill = 0u;
 
     pdl_launch_dependents();
     pdl_wait();  // scores come from the previous kernel
 
-    float lo = INFINITY, hi = -INFINITY;
-    for (int j = tid; j < n_my; j += kClThreads) {
-        const float v = __ldg(s + beg + j);
-        S.vals[j] = v;
-        if (v - v == 0.f) { lo = fminf(lo, v); hi = fmaxf(hi, v); }
-    }
-    __syncthreads();  // vals[] is read across threads from here on
-    const int kk = k < 0 ? 0 : (k > f ? f : k);
-    const bool radix = kind == SEL_TOPK && kk > 0 && kk < f;
-    uint32_t pivot = 0u;
-    int need = 0;
-    if (radix) {
-        lo = block_min(lo, wred);
-        hi = block_max(hi, wred);
-        if (tid == 0) { S.lo = lo; S.hi = hi; S.ncand_fill = 0u; }
-        for (int i = tid; i < kBuckets; i += kClThreads) S.hist[i] = 0u;
-        cl_sync();
-        // cluster-wide min / max (every CTA the same): one remote load per CTA
-        if (tid < kCl) {
-            S.rlo[tid] = cl_ld_f32(cl_map(&S.lo, (uint32_t)tid));
-            S.rhi[tid] = cl_ld_f32(cl_map(&S.hi, (uint32_t)tid));
-        }
-        __syncthreads();
-        float smin = INFINITY, smax = -INFINITY;
+    float v[ET];
+    const bool vec = (E & 3) == 0 && ((reinterpret_cast<uintptr_t>(s) + 4u * (uint32_t)beg) & 15) == 0;
 #pragma unroll
-        for (int r = 0; r < kCl; ++r) { smin = fminf(smin, S.rlo[r]); smax = fmaxf(smax, S.rhi[r]); }
-        const float scale = smax > smin ? (float)(kBuckets - 4) / (smax - smin) : 0.f;
-        for (int j = tid; j < n_my; j += kClThreads) atomicAdd(&S.hist[bucket_of(S.vals[j], smin, scale)], 1u);
-        cl_sync();
-        // reduce-scatter: this CTA sums bins [rank*512, rank*512 + 512) over the cluster
-        uint32_t part = 0;
-        if (tid < kClBinsPerCta) {
-            const int bin = (int)rank * kClBinsPerCta + tid;
-            uint32_t sum = 0;
-            for (uint32_t r = 0; r < kCl; ++r) sum += cl_ld_u32(cl_map(&S.hist[bin], r));
-            S.red[tid] = sum;
-            part = sum;
-        }
-        int tot;
-        block_excl_scan((int)part, wsum, &tot);
-        if (tid == 0) S.slice_total = (uint32_t)tot;
-        cl_sync();
-        // which CTA's bin slice holds the kk-th largest (slices are ordered by
-        // score: the last CTA has the top bins), then which bin
-        if (tid < kCl) S.rtot[tid] = cl_ld_u32(cl_map(&S.slice_total, (uint32_t)tid));
-        __syncthreads();
-        int owner = 0;
-        uint32_t above_owner = 0;
-        {
-            uint32_t run = 0;
-            for (int r = kCl - 1; r >= 0; --r) {
-                if (run + S.rtot[r] >= (uint32_t)kk) { owner = r; break; }
-                run += S.rtot[r];
-            }
-            above_owner = run;
-        }
-        if (tid < kClBinsPerCta) S.loc[tid] = cl_ld_u32(cl_map(&S.red[tid], (uint32_t)owner));
-        __syncthreads();
-        {
-            // suffix counts over the owner's bins: thread t (< 512) holds bin t
-            const uint32_t cb = tid < kClBinsPerCta ? S.loc[tid] : 0u;
-            int tot_unused;
-            // reversed scan: thread t feeds bin (511 - t)
-            const uint32_t rb = tid < kClBinsPerCta ? S.loc[kClBinsPerCta - 1 - tid] : 0u;
-            const int excl = block_excl_scan((int)rb, wsum, &tot_unused);
-            __syncthreads();
-            if (tid < kClBinsPerCta) S.hist[kClBinsPerCta - 1 - tid] = (uint32_t)excl;  // count above bin
-            __syncthreads();
-            if (tid < kClBinsPerCta) {
-                const uint32_t run = above_owner + S.hist[tid];
-                if (run < (uint32_t)kk && run + cb >= (uint32_t)kk) {
-                    S.s_bucket = (uint32_t)(owner * kClBinsPerCta + tid);
-                    S.s_rem = (uint32_t)kk - run;
-                    S.s_ncand = cb;
-                }
-            }
-        }
-        __syncthreads();
-        const int B_ = (int)S.s_bucket;
-        const uint32_t rem = S.s_rem, ncand = S.s_ncand;
-        if (ncand <= (uint32_t)kCandMax) {
-            // every CTA sends its members of bucket B_ to CTA 0
-            const uint32_t fill0 = cl_map(&S.ncand_fill, 0);
-            for (int j = tid; j < n_my; j += kClThreads) {
-                const float v = S.vals[j];
-                if (bucket_of(v, smin, scale) == B_) {
-                    const uint32_t p = cl_atom_add(fill0, 1u);
-                    cl_st_u32(cl_map(&S.ckey[p], 0), score_key(v));
-                    cl_st_u32(cl_map(&S.cid[p], 0), (uint32_t)(beg + j));
-                }
-            }
-            cl_sync();
-            // every CTA copies the members from CTA 0 once, then ranks them
-            // locally: the member of rank rem-1 is the pivot
-            if (rank != 0) {
-                const uint32_t ck0 = cl_map(&S.ckey[0], 0), ci0 = cl_map(&S.cid[0], 0);
-                for (int c = tid; c < (int)ncand; c += kClThreads) {
-                    S.ckey[c] = cl_ld_u32(ck0 + 4u * c);
-                    S.cid[c] = cl_ld_u32(ci0 + 4u * c);
-                }
-            }
-            __syncthreads();
-            for (int c = tid; c < (int)ncand; c += kClThreads) {
-                const uint32_t kc = S.ckey[c], ic = S.cid[c];
-                uint32_t rk = 0;
-                for (int o = 0; o < (int)ncand; ++o) {
-                    const uint32_t ko = S.ckey[o];
-                    rk += (ko > kc) || (ko == kc && S.cid[o] < ic);
-                }
-                if (rk == rem - 1u) S.s_pivot = kc;
-            }
-            __syncthreads();
-            int gtc = 0;
-            for (int c = tid; c < (int)ncand; c += kClThreads) gtc += S.ckey[c] > S.s_pivot;
-            int tot_gt;
-            block_excl_scan(gtc, wsum, &tot_gt);
-            pivot = S.s_pivot;
-            need = (int)rem - tot_gt;
+    for (int q = 0; q < ET; q += 4) {
+        if (vec && q + 4 <= ne) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(s + beg + j0 + q));
+            v[q] = t.x; v[q + 1] = t.y; v[q + 2] = t.z; v[q + 3] = t.w;
         } else {
-            // a mass of equal scores: every CTA resolves it alone from the full row
-            // (radix select over the members' exact keys, read from global memory)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[q + e] = q + e < ne ? __ldg(s + beg + j0 + q + e) : 0.f;
+        }
+    }
+
+    const int kk = k < 0 ? 0 : (k > f ? f : k);
+    float pv = 0.f;
+    bool pnan = false;
+    int need = 0;
+    if (KIND == SEL_TOPK && kk > 0 && kk < f) {
+        // 1. min / max of the finite scores, pushed to every CTA
+        float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < ET; ++e)
+            if (e < ne && fabsf(v[e]) < INFINITY) { lo = fminf(lo, v[e]); hi = fmaxf(hi, v[e]); }
+        lo = warp_min(lo);
+        hi = warp_max(hi);
+        if (lane == 0) { S.wlo[warp] = lo; S.whi[warp] = hi; }
+        __syncthreads();
+        if (warp == 0) {
+            lo = warp_min(lane < kClW ? S.wlo[lane] : INFINITY);
+            hi = warp_max(lane < kClW ? S.whi[lane] : -INFINITY);
+            if (lane < kCl) {
+                *cl.map_shared_rank(&S.plo[rank], lane) = lo;
+                *cl.map_shared_rank(&S.phi[rank], lane) = hi;
+            }
+        }
+        cl.sync();                                                        // (1)
+        const float smin = warp_min(lane < kCl ? S.plo[lane] : INFINITY);
+        const float smax = warp_max(lane < kCl ? S.phi[lane] : -INFINITY);
+        const float scale = smax > smin ? (float)(kBuckets - 4) / (smax - smin) : 0.f;
+        const float off = -smin * scale;
+        // 2. local histogram; warp w pushes this CTA's total of slice w
+        //    (bins [w*512, w*512 + 512)) to every CTA
+#pragma unroll
+        for (int e = 0; e < ET; ++e)
+            if (e < ne) atomicAdd(&S.hist[bucket_fast(v[e], scale, off)], 1u);
+        __syncthreads();
+        {
+            constexpr int BPL = kClBins / 32;      // 16 bins per lane
+            const int bin0 = warp * kClBins + lane * BPL;
+            uint32_t sum = 0;
+#pragma unroll
+            for (int q = 0; q < BPL; q += 4) {
+                const uint4 h4 = *reinterpret_cast<const uint4 *>(&S.hist[bin0 + q]);
+                sum += h4.x + h4.y + h4.z + h4.w;
+            }
+            sum = (uint32_t)warp_isum((int)sum);
+            if (lane < kCl) *cl.map_shared_rank(&S.ptot[rank][warp], lane) = sum;
+        }
+        cl.sync();                                                        // (2)
+        // 3. the slice holding the kk-th largest (slice w holds higher scores
+        //    than slice w - 1), then its bins summed over the CTAs (all remote
+        //    loads in flight together), then the bucket
+        uint32_t tw = 0;
+        if (lane < kCl) {
+#pragma unroll
+            for (int r = 0; r < kCl; ++r) tw += S.ptot[r][lane];
+        }
+        uint32_t above = 0, above_owner = 0;
+        int owner = 0;
+#pragma unroll
+        for (int r = kCl - 1; r >= 0; --r) {
+            const uint32_t t = __shfl_sync(kFull, tw, r);
+            if (above < (uint32_t)kk && above + t >= (uint32_t)kk) { owner = r; above_owner = above; }
+            above += t;
+        }
+        {
+            const int bin = owner * kClBins + 2 * tid;
+            uint2 got[kCl];
+#pragma unroll
+            for (int r = 0; r < kCl; ++r)
+                got[r] = *cl.map_shared_rank(reinterpret_cast<const uint2 *>(&S.hist[bin]), r);
+            uint32_t cb[2] = {0u, 0u};
+#pragma unroll
+            for (int r = 0; r < kCl; ++r) { cb[0] += got[r].x; cb[1] += got[r].y; }
+            const uint32_t own = cb[0] + cb[1];
+            uint32_t tot_o;
+            const uint32_t pre = cta_excl_scan(own, S.usum, &tot_o);
+            uint32_t run = above_owner + (tot_o - pre - own);
+#pragma unroll
+            for (int q = 1; q >= 0; --q) {
+                if (run < (uint32_t)kk && run + cb[q] >= (uint32_t)kk) {
+                    S.bucket = (uint32_t)(bin + q);
+                    S.rem = (uint32_t)kk - run;
+                    S.ncand = cb[q];
+                }
+                run += cb[q];
+            }
+        }
+        __syncthreads();
+        const int B_ = (int)S.bucket;
+        const uint32_t rem = S.rem, ncand = S.ncand;
+        uint32_t pkey;
+        if (ncand <= (uint32_t)kCandSmall) {
+            // 4. the bucket's members, pushed to every CTA, ranked exactly
+#pragma unroll
+            for (int e = 0; e < ET; ++e) {
+                if (e < ne && bucket_fast(v[e], scale, off) == B_) {
+                    const uint32_t p = atomicAdd(&S.nfill, 1u);
+                    S.lkey[p] = score_key(v[e]);
+                    S.lid[p] = (uint32_t)(beg + j0 + e);
+                }
+            }
+            __syncthreads();
+            const uint32_t nmine = S.nfill;
+            for (uint32_t i = tid; i < nmine * kCl; i += kClT) {
+                const uint32_t p = i / kCl, r = i % kCl;
+                *cl.map_shared_rank(&S.ckey[rank][p], r) = S.lkey[p];
+                *cl.map_shared_rank(&S.cid[rank][p], r) = S.lid[p];
+            }
+            if (tid < kCl) *cl.map_shared_rank(&S.ccnt[rank], tid) = nmine;
+            cl.sync();                                                    // (3)
+            if (warp == 0) {
+                const uint32_t nr = lane < kCl ? S.ccnt[lane] : 0u;
+                uint32_t inc = nr;
+#pragma unroll
+                for (int o = 1; o < kCl; o <<= 1) {
+                    const uint32_t n = __shfl_up_sync(kFull, inc, o);
+                    if (lane >= o) inc += n;
+                }
+                // lane r copies CTA r's members to positions [inc - nr, inc)
+                if (lane < kCl)
+                    for (uint32_t p = 0; p < nr; ++p) {
+                        S.akey[inc - nr + p] = S.ckey[lane][p];
+                        S.aid[inc - nr + p] = S.cid[lane][p];
+                    }
+            }
+            __syncthreads();
+            for (int c = warp; c < (int)ncand; c += kClW) {
+                const uint32_t kc = S.akey[c], ic = S.aid[c];
+                int rk = 0, gt = 0;
+                for (int o = lane; o < (int)ncand; o += 32) {
+                    const uint32_t ko = S.akey[o];
+                    rk += (ko > kc) || (ko == kc && S.aid[o] < ic);
+                    gt += ko > kc;
+                }
+                rk = warp_isum(rk);
+                gt = warp_isum(gt);
+                if (lane == 0 && rk == (int)rem - 1) {
+                    S.pivot = kc;
+                    S.need = rem - (uint32_t)gt;
+                }
+            }
+            __syncthreads();
+            pkey = S.pivot;
+            need = (int)S.need;
+        } else {
+            // a crowded bucket: each CTA resolves it alone with a radix select
+            // over the whole row's members of the bucket (read from global)
             uint32_t prefix = 0u, pmask = 0u, r_ = rem;
-            uint32_t *h = S.hist;
             for (int pass = 0; pass < 4; ++pass) {
                 const int shift = 24 - 8 * pass;
+                if (tid < 256) S.rhist[tid] = 0u;
                 __syncthreads();
-                if (tid < 256) h[tid] = 0u;
-                __syncthreads();
-                for (int j = tid; j < f; j += kClThreads) {
-                    const float v = __ldg(s + j);
-                    const uint32_t key = score_key(v);
-                    if (bucket_of(v, smin, scale) == B_ && (key & pmask) == prefix)
-                        atomicAdd(&h[(key >> shift) & 255u], 1u);
-                }
-                __syncthreads();
-                if (tid == 0) {
-                    uint32_t run = 0;
-                    for (int dgt = 255; dgt >= 0; --dgt) {
-                        const uint32_t c = h[dgt];
-                        if (run < r_ && run + c >= r_) { S.s_pivot = (uint32_t)dgt; S.s_rem = r_ - run; break; }
-                        run += c;
+                for (int j = tid; j < f; j += kClT) {
+                    const float x = __ldg(s + j);
+                    if (bucket_fast(x, scale, off) == B_) {
+                        const uint32_t key = score_key(x);
+                        if ((key & pmask) == prefix) atomicAdd(&S.rhist[(key >> shift) & 255u], 1u);
                     }
                 }
                 __syncthreads();
-                prefix |= S.s_pivot << shift;
+                if (warp == 0) {
+                    uint32_t c8[8], sum = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) { c8[i] = S.rhist[255 - 8 * lane - i]; sum += c8[i]; }
+                    uint32_t inc = sum;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t nn = __shfl_up_sync(kFull, inc, o);
+                        if (lane >= o) inc += nn;
+                    }
+                    uint32_t run8 = inc - sum;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (run8 < r_ && run8 + c8[i] >= r_) {
+                            S.pivot = (uint32_t)(255 - 8 * lane - i);
+                            S.need = r_ - run8;
+                        }
+                        run8 += c8[i];
+                    }
+                }
+                __syncthreads();
+                prefix |= S.pivot << shift;
                 pmask |= 255u << shift;
-                r_ = S.s_rem;
+                r_ = S.need;
+                __syncthreads();
             }
-            pivot = prefix;
+            pkey = prefix;
             need = (int)r_;
         }
+        pnan = pkey == 0u;
+        pv = __uint_as_float((pkey & 0x80000000u) ? (pkey & 0x7fffffffu) : ~pkey);
     }
 
-    // compaction of this CTA's slice: warp w owns [w*W, (w+1)*W) within it
-    const int nw = kClThreads / 32;
-    const int WL = (((n_my + nw - 1) / nw) + 31) & ~31;
-    const int wbeg = min(warp * WL, n_my), wend = min(wbeg + WL, n_my);
-    const unsigned lt = (1u << lane) - 1u;
-    auto flags = [&](int jl, bool &gt, bool &eq) {
-        gt = false;
-        eq = false;
-        if (jl >= wend) return;
-        const float v = S.vals[jl];
-        if (kind == SEL_TOPK) {
-            if (kk == f) gt = true;
-            else if (kk > 0) { const uint32_t key = score_key(v); gt = key > pivot; eq = key == pivot; }
-        } else if (kind == SEL_THRESHOLD) {
-            gt = v >= tau;
+    // 5. compaction: packed (greater, tie) counts -> CTA scan -> totals pushed
+    //    to every CTA -> this CTA's output offsets
+    auto flags = [&](float x, bool &gt, bool &eq) {
+        if (KIND == SEL_TOPK) {
+            if (kk == f) { gt = true; eq = false; }
+            else if (kk == 0) { gt = false; eq = false; }
+            else rank_flags(x, pv, pnan, gt, eq);
+        } else if (KIND == SEL_THRESHOLD) {
+            gt = x >= tau;
+            eq = false;
         } else {
-            gt = v > 0.f;
+            gt = x > 0.f;
+            eq = false;
         }
     };
-    int w_gt = 0, w_eq = 0;
-    for (int base = wbeg; base < wend; base += 32) {
-        bool gt, eq;
-        flags(base + lane, gt, eq);
-        w_gt += __popc(__ballot_sync(kFull, gt));
-        w_eq += __popc(__ballot_sync(kFull, eq));
-    }
-    if (lane == 0) { S.wtot[warp][0] = (uint32_t)w_gt; S.wtot[warp][1] = (uint32_t)w_eq; }
-    __syncthreads();
-    if (tid == 0) {
-        int g_ = 0, e_ = 0;
-        for (int w = 0; w < nw; ++w) { g_ += (int)S.wtot[w][0]; e_ += (int)S.wtot[w][1]; }
-        S.cta_gt = g_;
-        S.cta_eq = e_;
-    }
-    cl_sync();
-    // this CTA's place: ties and selections of the CTAs before it
-    if (tid < kCl) {
-        S.rgt[tid] = (int)cl_ld_u32(cl_map(&S.cta_gt, (uint32_t)tid));
-        S.req[tid] = (int)cl_ld_u32(cl_map(&S.cta_eq, (uint32_t)tid));
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int eqb = 0, selb = 0;
-        for (int r = 0; r < kCl; ++r) {
-            const int take = max(0, min(S.req[r], need - eqb));
-            if (r == (int)rank) { S.s_base = selb; S.s_eqb = eqb; }
-            eqb += S.req[r];
-            selb += S.rgt[r] + take;
+    uint32_t cgt = 0, ceq = 0;
+#pragma unroll
+    for (int e = 0; e < ET; ++e) {
+        if (e < ne) {
+            bool gt, eq;
+            flags(v[e], gt, eq);
+            cgt += gt;
+            ceq += eq;
         }
-        S.s_total = selb;
     }
-    __syncthreads();
-    if (warp == 0) {
-        // warp offsets inside the CTA (ties first, so the lowest ids win)
-        const int g_ = (int)S.wtot[lane][0], e_ = (int)S.wtot[lane][1];
-        int eb = e_;
+    uint32_t tot;
+    const uint32_t ex = cta_excl_scan((cgt << 16) | ceq, S.usum, &tot);
+    if (tid < kCl) {
+        *cl.map_shared_rank(&S.pgt[rank], tid) = tot >> 16;
+        *cl.map_shared_rank(&S.peq[rank], tid) = tot & 0xffffu;
+    }
+    cl.sync();                                                            // (4)
+    // offsets of this CTA: lanes r < kCl hold CTA r's totals (every warp alike)
+    const uint32_t g_ = lane < kCl ? S.pgt[lane] : 0u, e_ = lane < kCl ? S.peq[lane] : 0u;
+    uint32_t gi = g_, ei = e_;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) { const int nn = __shfl_up_sync(kFull, eb, o); if (lane >= o) eb += nn; }
-        eb = eb - e_ + S.s_eqb;
-        const int take = max(0, min(e_, need - eb));
-        const int sel = g_ + take;
-        int sb = sel;
+    for (int o = 1; o < kCl; o <<= 1) {
+        const uint32_t a1 = __shfl_up_sync(kFull, gi, o), a2 = __shfl_up_sync(kFull, ei, o);
+        if (lane >= o) { gi += a1; ei += a2; }
+    }
+    const int gb = (int)__shfl_sync(kFull, gi - g_, rank), eb = (int)__shfl_sync(kFull, ei - e_, rank);
+    int eq_run = eb + (int)(ex & 0xffffu);
+    int pos = gb + (int)(ex >> 16) + min(eq_run, need);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) { const int nn = __shfl_up_sync(kFull, sb, o); if (lane >= o) sb += nn; }
-        S.wtot[lane][0] = (uint32_t)(sb - sel + S.s_base);
-        S.wtot[lane][1] = (uint32_t)eb;
+    for (int e = 0; e < ET; ++e) {
+        if (e < ne) {
+            bool gt, eq;
+            flags(v[e], gt, eq);
+            const bool take = gt || (eq && eq_run < need);
+            eq_run += eq;
+            if (take) {
+                const int jl = j0 + e;
+                out[pos++] = beg + jl;
+                if (mask) atomicOr(&S.bits[jl >> 5], 1u << (jl & 31));
+            }
+        }
     }
-    __syncthreads();
-    int pos = (int)S.wtot[warp][0], eq_run = (int)S.wtot[warp][1];
-    for (int base = wbeg; base < wend; base += 32) {
-        bool gt, eq;
-        const int jl = base + lane;
-        flags(jl, gt, eq);
-        const unsigned be = __ballot_sync(kFull, eq);
-        const bool take = gt || (eq && eq_run + __popc(be & lt) < need);
-        const unsigned bs = __ballot_sync(kFull, take);
-        if (take) out[pos + __popc(bs & lt)] = beg + jl;
-        if (mask && lane == 0) mask[(size_t)b * words + ((beg + base) >> 5)] = bs;
-        eq_run += __popc(be);
-        pos += __popc(bs);
+    if (rank == 0 && warp == 0) {
+        const uint32_t gt_all = __shfl_sync(kFull, gi, kCl - 1), eq_all = __shfl_sync(kFull, ei, kCl - 1);
+        if (lane == 0) count[b] = (int)gt_all + min((int)eq_all, need);
     }
-    if (rank == 0 && tid == 0) count[b] = S.s_total;
-    cl_sync();  // no CTA leaves while another may still read its shared memory
+    if (mask) {
+        __syncthreads();
+        const int nw = (n_my + 31) >> 5;
+        for (int w = tid; w < nw; w += kClT) mask[(size_t)b * words + (beg >> 5) + w] = S.bits[w];
+    }
 }
 
-size_t select_smem(int f) { return sizeof(uint32_t) * ((size_t)f + kBuckets); }
-
-bool cluster_select_enabled() {
-    static const bool on = [] {
-        const char *v = getenv("CS_SELECT_CLUSTER");
-        return !(v && v[0] == '0');
-    }();
-    return on;
-}
-
-}  // namespace
-
-cudaError_t launch_select_cluster(const SelectArgs &a, cudaStream_t s) {
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const size_t smem = sizeof(ClSmem);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
-    }
+template <int ET, int KIND>
+cudaError_t run_select_cl(const SelectArgs &a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kCl * a.B);
-    cfg.blockDim = dim3(kClThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.blockDim = dim3(kClT);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -672,23 +722,58 @@ cudaError_t launch_select_cluster(const SelectArgs &a, cudaStream_t s) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, select_cluster_kernel, a.scores, a.f, (int)a.kind, a.k, a.tau, a.idx,
-                              a.ld_idx, a.count, a.mask);
+    return cudaLaunchKernelEx(&cfg, select_cl_kernel<ET, KIND>, a.scores, a.f, a.k, a.tau, a.idx, a.ld_idx,
+                              a.count, a.mask);
 }
 
+template <int ET>
+cudaError_t run_select_cl_kind(const SelectArgs &a, cudaStream_t s) {
+    if (a.kind == SEL_TOPK) return run_select_cl<ET, SEL_TOPK>(a, s);
+    if (a.kind == SEL_THRESHOLD) return run_select_cl<ET, SEL_THRESHOLD>(a, s);
+    return run_select_cl<ET, SEL_POSITIVE>(a, s);
+}
+
+cudaError_t launch_select_cl(const SelectArgs &a, cudaStream_t s) {
+    const int SL = (((a.f + kCl - 1) / kCl) + 31) & ~31;
+    const int E = (SL + kClT - 1) / kClT;
+    if (E <= 4) return run_select_cl_kind<4>(a, s);
+    if (E <= 8) return run_select_cl_kind<8>(a, s);
+    if (E <= 12) return run_select_cl_kind<12>(a, s);
+    if (E <= 16) return run_select_cl_kind<16>(a, s);
+    return run_select_cl_kind<24>(a, s);
+}
+
+template <int ET, int KIND>
+cudaError_t run_select_row(const SelectArgs &a, cudaStream_t s) {
+    return launch(select_row_kernel<ET, KIND>, dim3(a.B), dim3(kRowThreads), 0, s, pdl_enabled(), a.scores,
+                  a.f, a.k, a.tau, a.idx, a.ld_idx, a.count, a.mask);
+}
+
+template <int ET>
+cudaError_t run_select_kind(const SelectArgs &a, cudaStream_t s) {
+    if (a.kind == SEL_TOPK) return run_select_row<ET, SEL_TOPK>(a, s);
+    if (a.kind == SEL_THRESHOLD) return run_select_row<ET, SEL_THRESHOLD>(a, s);
+    return run_select_row<ET, SEL_POSITIVE>(a, s);
+}
+
+cudaError_t launch_select_row(const SelectArgs &a, cudaStream_t s) {
+    const int E = (a.f + kRowThreads - 1) / kRowThreads;
+    if (E <= 4) return run_select_kind<4>(a, s);
+    if (E <= 8) return run_select_kind<8>(a, s);
+    if (E <= 12) return run_select_kind<12>(a, s);
+    if (E <= 16) return run_select_kind<16>(a, s);
+    if (E <= 20) return run_select_kind<20>(a, s);
+    if (E <= 24) return run_select_kind<24>(a, s);
+    if (E <= 28) return run_select_kind<28>(a, s);
+    if (E <= 32) return run_select_kind<32>(a, s);
+    return run_select_kind<48>(a, s);
+}
+
+}  // namespace
+
 cudaError_t launch_select(const SelectArgs &a, cudaStream_t s) {
-    if (a.f >= 2048 && a.f <= kCl * kClSliceMax && cluster_select_enabled()) return launch_select_cluster(a, s);
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)select_smem(kSelectMaxF));
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
-    }
-    return launch(select_kernel, dim3(a.B), dim3(kSelThreads), select_smem(a.f), s, pdl_enabled(), a.scores,
-                  a.f, (int)a.kind, a.k, a.tau, a.idx, a.ld_idx, a.count, a.mask);
+    if (a.f >= 2048) return launch_select_cl(a, s);
+    return launch_select_row(a, s);
 }
 
 }  // namespace cs
