@@ -11,18 +11,21 @@
 //
 // Design.  W_down is stored transposed, so each chosen neuron needs two (or
 // three, gated) contiguous rows of d elements.  A persistent grid of one CTA
-// per SM splits the ascending index list into contiguous chunks.  Each of the
-// 512 threads owns fixed 16-byte column vectors of every row, and gathers
-// exactly those vectors of the chunk's rows with per-thread asynchronous
-// copies (cp.async) into its own slots of a shared-memory ring, SG groups of
-// NG neurons ahead.  Because a thread only ever reads the slots it filled,
-// the ring needs no barrier; the one cross-thread step is the gate dot
-// product, whose per-warp sums are combined in a fixed order once per group.
-// x stays in registers; a_j * w_down_j accumulates in fp32 registers.  Each
-// CTA writes its partial y; a second kernel adds the G partials per column in
-// a fixed order (and applies the residual epilogue), so y is bit-reproducible.
-// (One-dimensional bulk copies were measured slower for rows of ~10 KB: each
-// costs a fixed ~0.3 us of the SM's copy engine.)
+// per SM splits the ascending index list into contiguous chunks.  A CTA has
+// one thread per 16-byte column vector of a row (up to 1024 threads; wider
+// rows give each thread MAXV vectors), and each thread gathers exactly its
+// vectors of the chunk's rows with per-thread asynchronous copies (cp.async)
+// into its own slots of a shared-memory ring, SG groups of NG neurons ahead.
+// A thread only ever reads the slots it filled, so the ring needs no barrier.
+// Per group: each thread's partial gate (and up) dot products are summed per
+// warp, one block barrier publishes the warp sums, and every warp then adds
+// them in a fixed shuffle order to get the activations itself, applies its
+// a_j * w_down_j AXPY at once, and refills its slots.  x and the output
+// accumulators live in registers (fp32).  Each CTA writes its partial y; a
+// second kernel adds the G partials per column in a fixed order (and applies
+// the residual epilogue), so y is bit-reproducible.
+// (One-dimensional bulk copies were measured slower for rows of ~10 KB: the
+// copy engine of an SM streams far below its share of HBM bandwidth.)
 #include <utility>
 
 #include "cs_internal.cuh"
@@ -31,8 +34,8 @@ namespace cs {
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxThreads = 1024;
+constexpr int kMaxWarps = kMaxThreads / 32;
 constexpr int kNgMax = 4;                 // neurons per group (max)
 constexpr int kStageMax = 16;             // ring slots (ng * sg)
 constexpr size_t kRingBudget = 200 * 1024;
@@ -58,18 +61,26 @@ __device__ __forceinline__ void cp4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Sum over the warps of a value that lane w (< nwarps) holds for warp w: a
+// fixed xor tree, so every lane gets the same, bit-reproducible sum.
+__device__ __forceinline__ float warps_total(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
 template <typename T, int TB, bool GLU, bool PRE, int MAXV>
-__global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
+__global__ void __launch_bounds__(kMaxThreads, 1) ffn_gather_kernel(const FfnK a) {
     constexpr int V = Vec<T>::N;
     constexpr int NROW = (PRE ? 0 : 1) + (GLU ? 1 : 0) + 1;
     constexpr bool DOTS = !PRE || GLU;
     extern __shared__ __align__(16) uint4 ring[];  // [slot][NROW][nvec]
-    __shared__ float red[2][kWarps][kNgMax][TB][2];
-    __shared__ float act[2][kNgMax][TB];
-    __shared__ float addv[kStageMax];              // bias / pre-activation per slot
+    __shared__ float red[2][kNgMax][TB][2][kMaxWarps];
     __shared__ int s_idx[kChunkMax];               // this CTA's ids, staged once
+    __shared__ float s_add[kChunkMax];             // their bias (or pre-activation)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = blockDim.x, nwarps = nthr >> 5;
     const int c = blockIdx.x, G = gridDim.x;
     const int b0 = blockIdx.y * TB;
     const int nvec = a.nvec;
@@ -82,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
     bool vok[MAXV];
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
-        const int v = tid + i * kThreads;
+        const int v = tid + i * nthr;
         vok[i] = v < nvec;
         voff[i] = v * 16;
     }
@@ -98,13 +109,22 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
     const int n0 = (int)((long long)n * c / G);
     const int cnt = min(kChunkMax, (int)((long long)n * (c + 1) / G) - n0);
     // stage the chunk's ids so issuing copies never waits on a global load
-    for (int m = tid; m < cnt; m += kThreads) s_idx[m] = __ldg(a.idx + n0 + m);
+    for (int m = tid; m < cnt; m += nthr) s_idx[m] = __ldg(a.idx + n0 + m);
     __syncthreads();
+    // the chunk's bias (or pre-activation) values, copied once
+    {
+        const float *addsrc = PRE ? a.preact : a.bias;
+        for (int m = tid; m < cnt; m += nthr) {
+            int j = s_idx[m];
+            j = (j >= 0 && j < a.f) ? j : 0;
+            if (addsrc) cp4(smem_addr(&s_add[m]), addsrc + j);
+            else s_add[m] = 0.f;
+        }
+    }
     const int ng = a.ng, sg = a.sg;
     const int ngroups = (cnt + ng - 1) / ng;
 
-    // this thread's copies for group g into slots [s0, s0 + ng), plus the
-    // bias of neuron q by lane q of warp 0
+    // this thread's copies for group g into slots [s0, s0 + ng)
     auto issue = [&](int g, int s0) {
         if (g < ngroups) {
             const int gn = min(ng, cnt - g * ng);
@@ -125,17 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
                         cp16(r, dr + voff[i]);
                     }
                 }
-                if (warp == 0 && lane == q) {
-                    const float *src = PRE ? a.preact + j : (a.bias ? a.bias + j : nullptr);
-                    if (src) cp4(smem_addr(&addv[s0 + q]), src);
-                    else addv[s0 + q] = 0.f;
-                }
             }
         }
         cp_async_commit();  // always commit, so group counting stays uniform
     };
 
-    for (int g = 0; g < sg; ++g) issue(g, g * ng);
+    for (int g = 0; g < sg; ++g) issue(g, g * ng);  // group 0 also carries s_add
 
     float xr[TB][MAXV][V];
     float yacc[TB][MAXV][V];
@@ -147,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
         const float *xb = a.x + (size_t)b * a.d;
 #pragma unroll
         for (int i = 0; i < MAXV; ++i) {
-            const int col0 = (tid + i * kThreads) * V;
+            const int col0 = (tid + i * nthr) * V;
 #pragma unroll
             for (int e = 0; e < V; ++e) yacc[t][i][e] = 0.f;
             if (live && vok[i] && xvec && col0 + V <= a.d) {
@@ -164,153 +179,118 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
         }
     }
 
-    // Software-pipelined groups: iteration g computes group g's gate (and up)
-    // dot products, then group g-1's down-row AXPY.  Named barriers are split
-    // into arrive / wait: every warp arrives after writing its partial sums
-    // (barrier A) and goes on; warp 0 alone waits on A, finishes the
-    // activations, and arrives on barrier B, which the other warps wait on
-    // only one iteration later, before that group's AXPY.  So no thread waits
-    // on another thread's data for the group it is working on.
-    constexpr int kBarA = 1, kBarB = 3;  // ids 1,2 and 3,4 by group parity
-    int gs = 0;      // ring group of group g
-    int s0_prev = 0, gn_prev = 0;
-    for (int g = 0; g <= ngroups; ++g) {
-        const bool have = g < ngroups;
-        const int gn = have ? min(ng, cnt - g * ng) : 0;
+    int gs = 0;  // ring group of group g
+    for (int g = 0; g < ngroups; ++g) {
+        const int gn = min(ng, cnt - g * ng);
         const int s0 = gs * ng;
         const int p = g & 1;
-        if (have) {
-            // this thread's copies for group g have landed (commits so far: sg at
-            // start, then one per iteration from iteration 1)
-            if (g == 0) { if (sg == 2) cp_async_wait<1>(); else cp_async_wait<2>(); }
-            else { if (sg == 2) cp_async_wait<0>(); else cp_async_wait<1>(); }
-            // gate (and up) dot products: one accumulator per (neuron, vector),
-            // all neurons of the group interleaved.  Slots past the group's
-            // last neuron hold stale data whose sums are never used.
+        // this thread's copies for group g have landed (commits so far: sg
+        // at the start, then one per finished group)
+        if (sg == 2) cp_async_wait<1>(); else cp_async_wait<2>();
+        // gate (and up) dot products: one accumulator per (neuron, vector).
+        // Slots past the group's last neuron hold stale data whose sums are
+        // never used.
+        if (DOTS) {
             float pg[kNgMax][TB], pu[kNgMax][TB];
 #pragma unroll
             for (int q = 0; q < kNgMax; ++q)
 #pragma unroll
                 for (int t = 0; t < TB; ++t) pg[q][t] = pu[q][t] = 0.f;
-            if (DOTS) {
 #pragma unroll
-                for (int i = 0; i < MAXV; ++i) {
-                    if (!vok[i]) continue;
-                    const int v = tid + i * kThreads;
-                    const int ne = a.d - v * V;  // < V only on a row's last vector
-                    float ag[kNgMax][TB], au[kNgMax][TB];
+            for (int i = 0; i < MAXV; ++i) {
+                if (!vok[i]) continue;
+                const int v = tid + i * nthr;
+                const int ne = a.d - v * V;  // < V only on a row's last vector
 #pragma unroll
-                    for (int q = 0; q < kNgMax; ++q) {
-                        const uint4 *slot = ring + (size_t)(s0 + q) * NROW * nvec;
+                for (int q = 0; q < kNgMax; ++q) {
+                    if (q >= ng) continue;  // ng is uniform: no divergence
+                    const uint4 *slot = ring + (size_t)(s0 + q) * NROW * nvec;
+                    if (!PRE) {
+                        float w[V];
+                        unpack<T>(slot[v], w);
+                        if (ne < V) {
 #pragma unroll
-                        for (int t = 0; t < TB; ++t) ag[q][t] = au[q][t] = 0.f;
-                        if (q >= ng) continue;  // ng is uniform: no divergence
-                        if (!PRE) {
-                            float w[V];
-                            unpack<T>(slot[v], w);
-                            if (ne < V) {
-#pragma unroll
-                                for (int e = 0; e < V; ++e) w[e] = e < ne ? w[e] : 0.f;
-                            }
-#pragma unroll
-                            for (int e = 0; e < V; ++e)
-#pragma unroll
-                                for (int t = 0; t < TB; ++t) ag[q][t] = fmaf(w[e], xr[t][i][e], ag[q][t]);
+                            for (int e = 0; e < V; ++e) w[e] = e < ne ? w[e] : 0.f;
                         }
-                        if (GLU) {
-                            float w[V];
-                            unpack<T>(slot[(PRE ? 0 : 1) * nvec + v], w);
-                            if (ne < V) {
 #pragma unroll
-                                for (int e = 0; e < V; ++e) w[e] = e < ne ? w[e] : 0.f;
-                            }
+                        for (int e = 0; e < V; ++e)
 #pragma unroll
-                            for (int e = 0; e < V; ++e)
-#pragma unroll
-                                for (int t = 0; t < TB; ++t) au[q][t] = fmaf(w[e], xr[t][i][e], au[q][t]);
-                        }
+                            for (int t = 0; t < TB; ++t) pg[q][t] = fmaf(w[e], xr[t][i][e], pg[q][t]);
                     }
+                    if (GLU) {
+                        float w[V];
+                        unpack<T>(slot[(PRE ? 0 : 1) * nvec + v], w);
+                        if (ne < V) {
 #pragma unroll
-                    for (int q = 0; q < kNgMax; ++q)
+                            for (int e = 0; e < V; ++e) w[e] = e < ne ? w[e] : 0.f;
+                        }
 #pragma unroll
-                        for (int t = 0; t < TB; ++t) { pg[q][t] += ag[q][t]; pu[q][t] += au[q][t]; }
+                        for (int e = 0; e < V; ++e)
+#pragma unroll
+                            for (int t = 0; t < TB; ++t) pu[q][t] = fmaf(w[e], xr[t][i][e], pu[q][t]);
+                    }
                 }
-#pragma unroll
-                for (int q = 0; q < kNgMax; ++q)
-#pragma unroll
-                    for (int t = 0; t < TB; ++t) {
-                        if (q < gn) {
-                            const float sgv = PRE ? 0.f : warp_sum(pg[q][t]);
-                            const float suv = GLU ? warp_sum(pu[q][t]) : 0.f;
-                            if (lane == 0) {
-                                red[p][warp][q][t][0] = sgv;
-                                red[p][warp][q][t][1] = suv;
-                            }
-                        }
-                    }
             }
-            if (warp != 0) {
-                named_arrive(kBarA + p, kThreads);
-            } else {
-                named_sync(kBarA + p, kThreads);
-                // lane q finishes neuron q (its own bias copy has landed), warps in order
-                if (lane < gn) {
-                    const int q = lane;
-                    const int j = s_idx[g * ng + q];
-                    const bool valid = j >= 0 && j < a.f;
-                    const float add = addv[s0 + q];
-#pragma unroll
-                    for (int t = 0; t < TB; ++t) {
-                        float gsum = 0.f, usum = 0.f;
-                        if (DOTS) {
-#pragma unroll
-                            for (int w = 0; w < kWarps; ++w) {
-                                gsum += red[p][w][q][t][0];
-                                usum += red[p][w][q][t][1];
-                            }
-                        }
-                        const float gv = PRE ? add : gsum + add;
-                        float av = fmaxf(gv, 0.f);
-                        if (GLU) av *= usum;
-                        act[p][q][t] = valid ? av : 0.f;
-                    }
-                    if (!valid) atomicOr(a.err, CS_DEVERR_INDEX);
-                }
-                __syncwarp();
-                named_arrive(kBarB + p, kThreads);
-            }
-        }
-        if (g > 0) {
-            // group g-1: y += a_j * w_down_j
-            const int pp = p ^ 1;
-            if (warp != 0) named_sync(kBarB + pp, kThreads);
-            float av[kNgMax][TB];
 #pragma unroll
             for (int q = 0; q < kNgMax; ++q)
 #pragma unroll
-                for (int t = 0; t < TB; ++t) av[q][t] = q < gn_prev ? act[pp][q][t] : 0.f;
-#pragma unroll
-            for (int q = 0; q < kNgMax; ++q) {
-                if (q < gn_prev) {
-                    const uint4 *dn = ring + ((size_t)(s0_prev + q) * NROW + (NROW - 1)) * nvec;
-#pragma unroll
-                    for (int i = 0; i < MAXV; ++i) {
-                        if (vok[i]) {
-                            float w[V];
-                            unpack<T>(dn[tid + i * kThreads], w);
-#pragma unroll
-                            for (int t = 0; t < TB; ++t)
-#pragma unroll
-                                for (int e = 0; e < V; ++e) yacc[t][i][e] = fmaf(av[q][t], w[e], yacc[t][i][e]);
+                for (int t = 0; t < TB; ++t) {
+                    if (q < gn) {
+                        if (!PRE) {
+                            const float sgv = warp_sum(pg[q][t]);
+                            if (lane == 0) red[p][q][t][0][warp] = sgv;
+                        }
+                        if (GLU) {
+                            const float suv = warp_sum(pu[q][t]);
+                            if (lane == 0) red[p][q][t][1][warp] = suv;
                         }
                     }
                 }
-            }
-            // this thread's slots of group g-1 are free: refill them
-            issue(g - 1 + sg, s0_prev);
         }
-        s0_prev = s0;
-        gn_prev = gn;
+        __syncthreads();  // the warp sums of group g (and, at g = 0, s_add) are visible
+        // activations of group g, computed alike by every warp
+        float av[kNgMax][TB];
+#pragma unroll
+        for (int q = 0; q < kNgMax; ++q) {
+#pragma unroll
+            for (int t = 0; t < TB; ++t) av[q][t] = 0.f;
+            if (q >= gn) continue;
+            const int m = g * ng + q;
+            const int j = s_idx[m];
+            const bool valid = j >= 0 && j < a.f;
+            const float add = s_add[m];
+#pragma unroll
+            for (int t = 0; t < TB; ++t) {
+                float gsum = 0.f, usum = 0.f;
+                if (!PRE) gsum = warps_total(lane < nwarps ? red[p][q][t][0][lane] : 0.f);
+                if (GLU) usum = warps_total(lane < nwarps ? red[p][q][t][1][lane] : 0.f);
+                const float gv = PRE ? add : gsum + add;
+                float act = fmaxf(gv, 0.f);
+                if (GLU) act *= usum;
+                av[q][t] = valid ? act : 0.f;
+            }
+            if (!valid && tid == 0) atomicOr(a.err, CS_DEVERR_INDEX);
+        }
+        // y += a_j * w_down_j over this thread's vectors
+#pragma unroll
+        for (int q = 0; q < kNgMax; ++q) {
+            if (q < gn) {
+                const uint4 *dn = ring + ((size_t)(s0 + q) * NROW + (NROW - 1)) * nvec;
+#pragma unroll
+                for (int i = 0; i < MAXV; ++i) {
+                    if (vok[i]) {
+                        float w[V];
+                        unpack<T>(dn[tid + i * nthr], w);
+#pragma unroll
+                        for (int t = 0; t < TB; ++t)
+#pragma unroll
+                            for (int e = 0; e < V; ++e) yacc[t][i][e] = fmaf(av[q][t], w[e], yacc[t][i][e]);
+                    }
+                }
+            }
+        }
+        // this thread's slots of group g are free: refill them
+        issue(g + sg, s0);
         gs = gs + 1 == sg ? 0 : gs + 1;
     }
     cp_async_wait<0>();
@@ -324,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gather_kernel(const FfnK a) {
 #pragma unroll
         for (int i = 0; i < MAXV; ++i) {
             if (vok[i]) {
-                const int v = tid + i * kThreads;
+                const int v = tid + i * nthr;
 #pragma unroll
                 for (int e = 0; e < V; e += 4) {
                     float4 o = make_float4(yacc[t][i][e], yacc[t][i][e + 1], yacc[t][i][e + 2], yacc[t][i][e + 3]);
@@ -388,16 +368,17 @@ cudaError_t run_gather(const FfnArgs &a, FfnK k, size_t smem, cudaStream_t s) {
     auto fn = ffn_gather_kernel<T, TB, GLU, PRE, MAXV>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    // one thread per vector when a row has at most 1024 of them
+    const int thr = ((k.nvec + MAXV - 1) / MAXV + 31) & ~31;
     dim3 grid(a.G, (a.B + TB - 1) / TB);
-    return launch(fn, grid, dim3(kThreads), smem, s, pdl_enabled(), k);
+    return launch(fn, grid, dim3(thr), smem, s, pdl_enabled(), k);
 }
 
 template <typename T, int TB, bool GLU, bool PRE>
 cudaError_t pick_maxv(const FfnArgs &a, const FfnK &k, size_t smem, cudaStream_t s) {
-    if (k.nvec <= kThreads) return run_gather<T, TB, GLU, PRE, 1>(a, k, smem, s);
-    if (k.nvec <= 2 * kThreads) return run_gather<T, TB, GLU, PRE, 2>(a, k, smem, s);
-    if (k.nvec <= 3 * kThreads) return run_gather<T, TB, GLU, PRE, 3>(a, k, smem, s);
-    if (k.nvec <= 4 * kThreads) return run_gather<T, TB, GLU, PRE, 4>(a, k, smem, s);
+    if (k.nvec <= kMaxThreads) return run_gather<T, TB, GLU, PRE, 1>(a, k, smem, s);
+    if (k.nvec <= 2 * kMaxThreads) return run_gather<T, TB, GLU, PRE, 2>(a, k, smem, s);
+    if (k.nvec <= 4 * kMaxThreads) return run_gather<T, TB, GLU, PRE, 4>(a, k, smem, s);
     return run_gather<T, TB, GLU, PRE, 8>(a, k, smem, s);
 }
 
@@ -454,7 +435,7 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
 // Largest d (in elements) the gather kernel takes for a dtype.
 int ffn_max_d(cs_dtype t) {
     const int V = t == CS_F32 ? 4 : 8;
-    return 8 * kThreads * V;
+    return 8 * kMaxThreads * V;
 }
 
 cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s) {
