@@ -50,6 +50,11 @@ WORKLOADS = {
     "llama70b-stack-lookahead": dict(d=8192, f=28672, r=1024, dt=2, glu=True, rho=0.15, mode="topk",
                                      share=0.15, L=80, stack="lookahead"),
 }
+# batched union (Falcon-40B-shaped layer): a step = union of B token masks +
+# the batched FFN over the union, for B tokens
+for _B in (1, 2, 4, 8, 16, 32):
+    WORKLOADS[f"falcon40b-union-b{_B}"] = dict(d=8192, f=32768, r=1, dt=2, glu=False, rho=0.10, mode="union",
+                                              share=0.10, union=_B)
 NCOPY = 8
 NX = 200
 
@@ -482,6 +487,194 @@ def oracle_step_inputs(W, layer_index=0):
     return L, P
 
 
+def run_union(args, W, rank, world):
+    """B tokens per step: cs_union_mask over their active-set masks, then
+    cs_sparse_ffn of all B tokens over the union (tensor-core path from
+    B = 4 on), rotating over layer copies and mask sets."""
+    import torch
+    import contextual_sparsity_sparse_gb300 as cs
+    import synth
+    import synth.device as synthdev
+    from contextual_sparsity_sparse_gb300 import build as cb
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    cb.build()
+    synthdev.build()
+    d, f, B = W["d"], W["f"], W["union"]
+    words = (f + 31) // 32
+    tdt = torch.bfloat16 if W["dt"] == 2 else torch.float16
+    NCU, NM = 3, 32
+    copies = []
+    for l in range(NCU):
+        t = {}
+        for name, which in (("w_gate", synth.W_GATE), ("w_down_t", synth.W_DOWN_T)):
+            t[name] = torch.empty((f, d), dtype=tdt, device="cuda")
+            synthdev.fill_normal(t[name], 0, synth.tensor_id(l, which), 1 / math.sqrt(d))
+        t["bias"] = torch.from_numpy(synth.zipf_bias(0, l, f, W["rho"])).cuda()
+        copies.append((cs.FfnLayer(t["w_gate"], t["w_down_t"], bias=t["bias"]), t))
+    import numpy as np
+    masks = torch.from_numpy(np.stack([synth.union_masks(7000 + 97 * rank + i, B, f, W["rho"])
+                                       for i in range(NM)]).view(np.int32)).cuda()      # [NM, B, words]
+    X = torch.from_numpy(synth.x_normal(8000 + rank, NM * B, d).reshape(NM, B, d)).cuda()
+    Y = torch.empty((B, d), device="cuda")
+    umask = torch.empty(words, dtype=torch.int32, device="cuda")
+    uidx = torch.empty((NM, f), dtype=torch.int32, device="cuda")
+    ucnt = torch.empty(NM, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    ws = cs.Workspace(d, f, 1, B, stream=s)
+
+    def step(i, ffn_only=False):
+        m = i % NM
+        if not ffn_only:
+            cs.cs_union_mask(masks[m], f, umask, uidx[m], ucnt[m: m + 1], ws, stream=s)
+        cs.cs_sparse_ffn(copies[i % NCU][0], X[m], uidx[m], ucnt[m: m + 1], Y, ws, stream=s)
+
+    NB = 64
+    with torch.cuda.stream(s):
+        for i in range(NM):
+            step(i)
+    s.synchronize()
+    mean_u = float(ucnt.float().mean().item())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(NB):
+                step(i)
+    K = max(NB, (args.steps // NB) * NB)
+    Wm = max(3 * NB, (args.warmup // NB) * NB)
+    with torch.cuda.stream(s):
+        for _ in range(Wm // NB):
+            g.replay()
+    s.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk = Clocks(dev)
+    clk.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(K // NB):
+            g.replay()
+    e1.record(s)
+    e1.synchronize()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    assert cs.cs_get_device_error(ws, stream=s) == 0
+
+    # roofline pass: the batched FFN calls alone (unions already computed)
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g2, stream=s):
+            for i in range(NB):
+                step(i, ffn_only=True)
+        for _ in range(3):
+            g2.replay()
+    s.synchronize()
+    reps = max(3, K // NB // 4)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(reps):
+            g2.replay()
+    f1.record(s)
+    f1.synchronize()
+    ffn_s = f0.elapsed_time(f1) / 1e3 / (reps * NB)
+
+    # e2e through the binding: pinned host masks and x in, y out, every step
+    KE = min(K, 400)
+    mh = masks.cpu().pin_memory()
+    xh = X.cpu().pin_memory()
+    yh = torch.empty((B, d)).pin_memory()
+    md = torch.empty((B, words), dtype=torch.int32, device="cuda")
+    xd = torch.empty((B, d), device="cuda")
+
+    def e2e_step(i):
+        m = i % NM
+        md.copy_(mh[m], non_blocking=True)
+        xd.copy_(xh[m], non_blocking=True)
+        cs.cs_union_mask(md, f, umask, uidx[0], ucnt[0:1], ws, stream=s)
+        cs.cs_sparse_ffn(copies[i % NCU][0], xd, uidx[0], ucnt[0:1], Y, ws, stream=s)
+        yh.copy_(Y, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for i in range(10):
+            e2e_step(i)
+    s.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for i in range(KE):
+            e2e_step(i)
+    s.synchronize()
+    e2e_s = time.perf_counter() - t0
+
+    hbm, src = peaks()
+    ffn_b = mean_u * (2 * d * 2 + 4 + 4) + 2 * 4 * B * d
+    step_b = ffn_b + 4 * B * words + 4 * words + 4 * mean_u
+    tc = 4 <= B and B >= int(os.environ.get("CS_TC_MIN_B", "4")) and B <= 32
+    launches = 1 + (4 if tc else 2)
+    flops = 2 * mean_u * d * 2 * (2 * B)   # two GEMMs, N = 2B (hi and lo halves)
+    res = {
+        "metric": METRIC, "value": world * B * K / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "d": d, "f": f, "batch": B, "global_batch": world * B,
+                   "weights": "bf16", "accumulate": "f32", "union_mean": mean_u, "union_density": mean_u / f,
+                   "path": "tcgen05 gathered GEMM" if tc else "CUDA-core gathered GEMV",
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {NCU} layer copies ({NCU * 2 * f * d * 2 / 1e9:.2f} GB) and {NM} mask sets rotate",
+                   "step": "cs_union_mask + cs_sparse_ffn over B tokens, graph of 64 steps"},
+        "clocks": clocks,
+        "gpu_launches": launches * K,
+        "roofline": {"bound": "hbm", "kernel": "cs_sparse_ffn over the union (" + ("split + tcgen05 gate GEMM + tcgen05 down GEMM + reduce" if tc else "gather + reduce") + ")",
+                     "achieved": ffn_b / ffn_s / 1e9, "peak": hbm, "unit": "GB/s", "frac": ffn_b / ffn_s / 1e9 / hbm,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
+                     "bytes_per_launch": ffn_b, "avg_launch_us": ffn_s * 1e6,
+                     "tensor_tflops": flops / ffn_s / 1e12 if tc else None,
+                     "traffic": profile_traffic("cs_sparse_ffn", args.workload)},
+        "step_roofline": {"bytes_per_step": step_b, "achieved": step_b / (ms / 1e3 / K) / 1e9, "peak": hbm,
+                          "frac": step_b / (ms / 1e3 / K) / 1e9 / hbm, "unit": "GB/s"},
+        "e2e": {"value": world * B * KE / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": B * words * 4 + B * d * 4, "d2h_bytes_per_step": B * d * 4, "steps": KE,
+                "how": "Python binding per step: pinned H2D of masks and x, cs_union_mask, cs_sparse_ffn, D2H of y; wall clock"},
+    }
+    return res
+
+
+def time_oracle_union(W, budget_s, max_steps=None):
+    """Time the oracle's union step (mask union, then the sparse FFN of B tokens)."""
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    B, d, f = W["union"], W["d"], W["f"]
+    Ly = oracle.Layer(d, f, W["dt"], synth.normal_matrix(0, synth.tensor_id(0, synth.W_GATE), f, d, 1 / math.sqrt(d), W["dt"]),
+                      synth.normal_matrix(0, synth.tensor_id(0, synth.W_DOWN_T), f, d, 1 / math.sqrt(d), W["dt"]),
+                      bias=synth.zipf_bias(0, 0, f, W["rho"]))
+    X = synth.x_normal(9000, B, d)
+    n, tok, t0 = 0, 0, time.perf_counter()
+    while True:
+        _, wi = oracle.union(synth.union_masks(9100 + n, B, f, W["rho"]), f)
+        for b in range(B):
+            oracle.ffn(Ly, X[b], wi)
+            tok += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps and n >= max_steps):
+            break
+    return tok, el, oracle.threads()
+
+
 def time_oracle(W, budget_s, max_steps=None):
     """Time the oracle's decode step (predict, select, gathered FFN) on the host."""
     import numpy as np
@@ -514,6 +707,20 @@ def main():
     W = WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference" and "union" in W:
+        if rank != 0:
+            return
+        tok, el, cores = time_oracle_union(W, budget_s=20.0, max_steps=max(1, args.steps))
+        v = tok / el
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / max(1, tok) * W["union"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "d": W["d"], "f": W["f"], "batch": W["union"]},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{tok} tokens of union steps, fp64 CPU oracle (at most 20 s)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
     if args.impl == "reference":
         if rank != 0:
             return
@@ -534,9 +741,15 @@ def main():
         torch.distributed.init_process_group("nccl")
     if "L" in W:
         res = run_stack(args, W, rank, world)
+    elif "union" in W:
+        res = run_union(args, W, rank, world)
     else:
         res, _ = run_ours(args, W, rank, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and "union" in W:
+        tok, el, cores = time_oracle_union(W, args.cpu_sample_s)
+        res["cpu_baseline"] = {"value": tok / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "sample": f"{tok} tokens of union steps (B={W['union']}) in {el:.1f} s, fp64 CPU oracle on {cores} threads"}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, el, cores = time_oracle(W, args.cpu_sample_s)
         L = W.get("L", 1)
         res["cpu_baseline"] = {"value": n / el / L, "unit": "tokens/s", "cores": cores, "kind": "oracle",

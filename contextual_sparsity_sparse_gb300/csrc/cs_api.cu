@@ -66,6 +66,7 @@ WsLayout ws_layout(int d, int f, int r, int B, int num_sms) {
     L.st_idx = off;    off += align256(sizeof(int32_t) * 2 * (size_t)f);
     L.st_count = off;  off += 256;
     L.st_h = off;      off += align256(sizeof(float) * (size_t)r);
+    L.tc = off;        off += tc_workspace_bytes(d, f, B);
     L.total = off;
     return L;
 }
@@ -275,6 +276,10 @@ cs_status cs_sparse_ffn(const cs_ffn_layer *layer, const float *x, int B, const 
     a.err = static_cast<uint32_t *>(ws);
     a.part = reinterpret_cast<float *>(static_cast<char *>(ws) + L.part);
     a.G = L.G; a.dp = L.dp;
+    if (tc_workspace_bytes(a.d, a.f, B) > 0) {
+        a.tc_x = static_cast<char *>(ws) + L.tc;
+        a.tc_a = static_cast<char *>(ws) + L.tc + tc_x_bytes(a.d, B);
+    }
     cudaError_t e = launch_ffn(a, (cudaStream_t)stream);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_sparse_ffn");
 }

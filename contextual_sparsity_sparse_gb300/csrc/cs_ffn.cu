@@ -438,7 +438,14 @@ int ffn_max_d(cs_dtype t) {
     return 8 * kMaxThreads * V;
 }
 
+cudaError_t launch_ffn_reduce(const float *part, int G, int B, int d, int dp, const float *resid, float scale,
+                              float *y, cudaStream_t s) {
+    dim3 g((d + 63) / 64, B);
+    return launch(ffn_reduce_kernel, g, dim3(kRedWarps * 32), 0, s, pdl_enabled(), part, G, B, d, dp, resid, scale, y);
+}
+
 cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s) {
+    if (tc_path_applies(a)) return launch_ffn_tc(a, s);
     switch (a.dtype) {
     case CS_F32: return run_ffn<float>(a, s);
     case CS_F16: return run_ffn<__half>(a, s);

@@ -1,0 +1,596 @@
+// Batched gathered FFN on the fifth-generation tensor cores, for dense unions.
+//
+// Sources: "Contextual Sparsity and Activation Predictors", section "When it
+// breaks" (a batch reads the union of its tokens' active sets, which grows
+// dense with B); "Contextual Sparsity: Activation-Aware LLM Inference and the
+// Deja Vu Paradigm", section "The Prediction Problem" (sparse_mlp_forward: the
+// chosen neurons' gate rows and down columns) and section "The SiLU/GELU
+// Challenge: TurboSparse" (relu(gate x) * up x).
+//
+// With U the union list (ascending ids, n = |U|) and X the B token rows, the
+// batched FFN is two GEMMs over gathered rows:
+//   H  = W_gate[U] X^T            M = n, N = B, K = d   (and W_up[U] X^T)
+//   Y^T = W_down^T[U]^T A^T       M = d, N = B, K = n   (A = act(H) per token)
+// Operands are fp16 / bf16 (the weights' type); accumulation is fp32 in tensor
+// memory.  The fp32 activations enter each GEMM split into two rows of the
+// weights' type, v = hi + lo with hi = round(v) and lo = round(v - hi), so
+// W.hi + W.lo carries ~16 (bf16) or ~22 (fp16) mantissa bits of v and the
+// result stays at fp32-accumulate accuracy.  Row 2b holds hi(v_b) and row
+// 2b + 1 lo(v_b), so N is 2B, padded to NP (16, 32 or 64), and B <= 32.
+//
+// Kernels (one launch each, chained with programmatic dependent launch):
+//   tc_split_kernel  X -> XS [NP, dk] (rows 2b: hi(x_b), rows 2b + 1: lo(x_b))
+//   tc_gate_kernel   persistent, one CTA per SM over 128-neuron tiles of U:
+//                    gathered W_gate (and W_up) rows and XS staged by per-thread
+//                    cp.async into 128-byte-swizzled shared memory (K-major),
+//                    tcgen05.mma issued by one thread into tensor memory, then
+//                    an epilogue that reads the accumulators (tcgen05.ld), adds
+//                    the bias, applies relu (times up) and writes AS [NP, kp]
+//                    (hi / lo rows again)
+//   tc_down_kernel   128-row tiles of d x split-K over U: gathered W_down^T
+//                    rows staged as the MN-major operand (64 neurons x 128
+//                    columns per stage), AS as the K-major operand; per-split
+//                    partial y written for the fixed-order reduce kernel
+// A stage is refilled two k-blocks after its MMAs were issued; their
+// completion is tracked by tcgen05.commit on one mbarrier per stage.  Every
+// wait is bounded: on a timeout the kernel records CS_DEVERR_TIMEOUT, stops
+// issuing, lets its copies land and frees its tensor memory.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cstdlib>
+
+#include "cs_internal.cuh"
+
+namespace cs {
+
+namespace {
+
+constexpr int kTcThreads = 256;        // 8 warps; warps 0..3 own TMEM lanes 0..127 in the epilogues
+constexpr int kTileM = 128;            // rows of an MMA tile
+constexpr int kKB = 64;                // K elements per stage: one 128-byte swizzle row
+constexpr int kTileBytes = kTileM * kKB * 2;   // 16 KB per 128 x 64 operand tile
+constexpr size_t kTcSmemBudget = 200 * 1024;
+constexpr int kIdxMax = 2048 + kTileM; // union ids one gate CTA stages
+
+struct TcArgs {
+    const uint8_t *w_gate, *w_up, *w_down_t;
+    const float *bias;
+    const float *x;        // [B, d]
+    const int32_t *idx;    // union ids, ascending
+    const int32_t *count;  // device count
+    uint16_t *xs;          // [NP, dk]
+    uint16_t *as;          // [NP, kp]
+    float *part;           // [splits, B, dp]
+    uint32_t *err;
+    int d, f, B, ldb, dk, kp, dp, splits, stages;
+};
+
+// ---- element type helpers --------------------------------------------------
+template <typename T> struct Tc;
+template <> struct Tc<__half> {
+    static constexpr bool kBf16 = false;
+    __device__ static uint16_t bits(float v) { return __half_as_ushort(__float2half_rn(v)); }
+    __device__ static float val(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+};
+template <> struct Tc<__nv_bfloat16> {
+    static constexpr bool kBf16 = true;
+    __device__ static uint16_t bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+    __device__ static float val(uint16_t b) { return __bfloat162float(__ushort_as_bfloat16(b)); }
+};
+
+// ---- tcgen05 / TMEM PTX ------------------------------------------------------
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor for kind::f16: fp32 accumulator, A/B fp16 or bf16,
+// A K-major or MN-major, B K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t umma_idesc(bool bf16, bool a_mn, int n) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u));
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+// 8 consecutive fp32 accumulator columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void cp16t(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// offset of 16-byte chunk c of row r in a K-major 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t kmaj_off(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+// offset of 16-byte chunk c (of 16 * MT along M) of k-row k in the MN-major
+// tile: [k / 8][c / 8][k % 8][128 B], swizzled like the K-major rows
+template <int MT>
+__device__ __forceinline__ uint32_t mnmaj_off(int k, int c) {
+    return (uint32_t)((k >> 3) * (2048 * MT) + (c >> 3) * 1024 + (k & 7) * 128 + (((c & 7) ^ (k & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t tmem_cols(int c) {
+    uint32_t n = 32;
+    while ((int)n < c) n <<= 1;
+    return n;
+}
+
+// ---- X -> [hi; lo] rows ------------------------------------------------------
+template <typename T>
+__global__ void tc_split_kernel(const TcArgs a, int np) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const size_t total = (size_t)np * a.dk;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int n = (int)(i / a.dk), c = (int)(i % a.dk);
+        uint16_t out = 0;
+        if (c < a.d && n < 2 * a.B) {
+            const float v = a.x[(size_t)(n >> 1) * a.d + c];
+            const uint16_t hi = Tc<T>::bits(v);
+            out = (n & 1) ? Tc<T>::bits(v - Tc<T>::val(hi)) : hi;
+        }
+        a.xs[i] = out;
+    }
+}
+
+// wait until at most n (0..6) of this thread's copy groups are pending
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+    switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    default: cp_async_wait<6>(); break;
+    }
+}
+
+// bounded wait on a stage barrier; false after the time limit
+__device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait(bar, parity, 1000000000ull);
+}
+
+// ---- gate (and up) GEMM + activation -----------------------------------------
+template <typename T, bool GLU, int NP, int KS>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t bars[8];
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_idx[kIdxMax];
+    constexpr int KA = KS / kKB;                           // 64-element swizzle atoms per row per stage
+    constexpr int kA = GLU ? 2 : 1;                        // weight tiles per stage besides X
+    constexpr int kWBytes = KA * kTileBytes;               // one weight tile: [atom][128 rows][128 B]
+    constexpr int kXAtom = NP * 128;                       // one X atom: [NP rows][128 B]
+    constexpr int kStageBytes = kA * kWBytes + KA * kXAtom;
+    constexpr uint32_t kCols = GLU ? 2 * NP : NP;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = a.stages;
+    const uint32_t base = smem_addr(dsm);
+    const uint32_t sbase = (base + 1023u) & ~1023u;       // 1024-byte aligned stages
+    const uint32_t ncols = tmem_cols((int)kCols);
+
+    if (warp == 0) tmem_alloc(&tmem_base, ncols);
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    pdl_launch_dependents();
+    pdl_wait();  // XS, the union list and its count come from earlier kernels
+
+    int n = *a.count;
+    if (n < 0 || n > a.f) {
+        if (tid == 0 && blockIdx.x == 0) atomicOr(a.err, CS_DEVERR_COUNT);
+        n = n < 0 ? 0 : a.f;
+    }
+    const int ntiles = (n + kTileM - 1) / kTileM;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int my_tiles = c < ntiles ? (ntiles - c + G - 1) / G : 0;
+    // this CTA's ids, tile after tile (positions past n repeat a valid row; their
+    // activations are written as 0)
+    for (int i = tid; i < my_tiles * kTileM; i += kTcThreads) {
+        const int p = (c + (i / kTileM) * G) * kTileM + (i % kTileM);
+        int j = p < n ? a.idx[p] : (n > 0 ? a.idx[n - 1] : 0);
+        if (j < 0 || j >= a.f) {
+            atomicOr(a.err, CS_DEVERR_INDEX);
+            j = 0;
+        }
+        s_idx[i] = j;
+    }
+    __syncthreads();
+
+    const int nkb = a.dk / KS;
+    const int Q = my_tiles * nkb;
+    const bool bf = Tc<T>::kBf16;
+    const uint32_t idesc = umma_idesc(bf, false, NP);
+
+    // copies of step q (tile q / nkb, k-block q % nkb) into stage q % S; the
+    // lanes of a warp cover contiguous bytes of a row (KS * 2 bytes per row)
+    auto issue = [&](int q) {
+        if (q < Q) {
+            const int lt = q / nkb, kb = q % nkb;
+            const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
+            const size_t koff = (size_t)kb * KS * 2;
+            for (int i = tid; i < kTileM * 8 * KA; i += kTcThreads) {
+                const int r = i / (8 * KA), ch = i % (8 * KA);
+                const uint32_t off = (uint32_t)((ch >> 3) * kTileBytes) + kmaj_off(r, ch & 7);
+                const size_t roff = (size_t)s_idx[lt * kTileM + r] * a.ldb + koff + ch * 16;
+                cp16t(st + off, a.w_gate + roff);
+                if (GLU) cp16t(st + kWBytes + off, a.w_up + roff);
+            }
+            const uint32_t sx = st + kA * kWBytes;
+            for (int i = tid; i < NP * 8 * KA; i += kTcThreads) {
+                const int r = i / (8 * KA), ch = i % (8 * KA);
+                cp16t(sx + (uint32_t)((ch >> 3) * kXAtom) + kmaj_off(r, ch & 7),
+                      reinterpret_cast<const uint8_t *>(a.xs) + (size_t)r * a.dk * 2 + koff + ch * 16);
+            }
+        }
+        cp_async_commit();
+    };
+
+    for (int q = 0; q < S - 2; ++q) issue(q);
+    bool ok = true;
+    for (int q = 0; q < Q; ++q) {
+        // every decision to stop is taken by the whole block at a barrier
+        bool mine = q < 2 || stage_wait(&bars[(q - 2) % S], (uint32_t)(((q - 2) / S) & 1));
+        if (mine) issue(q + S - 2);  // stage of step q - 2, whose MMAs have completed
+        cp_async_wait_upto(S - 2);   // step q complete: S - 2 later groups may be pending
+        fence_async_smem();
+        if (!__syncthreads_and(mine)) { ok = false; break; }
+        const int kb = q % nkb;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
+            const uint32_t sx = st + kA * kWBytes;
+#pragma unroll
+            for (int kk = 0; kk < KS / 16; ++kk) {
+                const uint32_t ka = (uint32_t)(kk >> 2), kin = (uint32_t)((kk & 3) * 32);
+                const uint64_t bd = umma_desc(sx + ka * kXAtom + kin, 16, 1024);
+                umma(tmem, umma_desc(st + ka * kTileBytes + kin, 16, 1024), bd, idesc, kb > 0 || kk > 0);
+                if (GLU)
+                    umma(tmem + NP, umma_desc(st + kWBytes + ka * kTileBytes + kin, 16, 1024), bd, idesc,
+                         kb > 0 || kk > 0);
+            }
+            umma_commit(&bars[q % S]);
+        }
+        if (kb == nkb - 1) {
+            // epilogue of tile q / nkb: its MMAs are the ones just committed
+            if (!__syncthreads_and(stage_wait(&bars[q % S], (uint32_t)((q / S) & 1)))) { ok = false; break; }
+            tc_fence_after();
+            if (warp < 4) {
+                const int r = warp * 32 + lane;
+                const int tile = c + (q / nkb) * G;
+                const int p = tile * kTileM + r;
+                const bool live = p < n;
+                const float bias = (live && a.bias) ? a.bias[s_idx[(q / nkb) * kTileM + r]] : 0.f;
+                const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+                float g[NP], u[NP];
+#pragma unroll
+                for (int c0 = 0; c0 < NP; c0 += 8) {
+                    float v[8];
+                    tmem_ld8(lane_addr + (uint32_t)c0, v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) g[c0 + e] = v[e];
+                    if (GLU) {
+                        tmem_ld8(lane_addr + (uint32_t)(NP + c0), v);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) u[c0 + e] = v[e];
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < NP / 2; ++b) {
+                    if (b < a.B) {
+                        float act = fmaxf(g[2 * b] + g[2 * b + 1] + bias, 0.f);
+                        if (GLU) act *= u[2 * b] + u[2 * b + 1];
+                        act = live ? act : 0.f;
+                        const uint16_t hi = Tc<T>::bits(act);
+                        const uint16_t lo = Tc<T>::bits(act - Tc<T>::val(hi));
+                        a.as[(size_t)(2 * b) * a.kp + p] = hi;
+                        a.as[(size_t)(2 * b + 1) * a.kp + p] = lo;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();  // accumulators read before the next tile's first MMA
+        }
+    }
+    if (!ok && tid == 0) atomicOr(a.err, CS_DEVERR_TIMEOUT);
+    cp_async_wait<0>();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_free(tmem, ncols);
+    }
+}
+
+// ---- down GEMM -> per-split partial y ----------------------------------------
+template <typename T, int NP, int MT>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t bars[8];
+    __shared__ uint32_t tmem_base;
+    constexpr int kWBytes = MT * kTileBytes;                // 64 rows x 128 * MT columns
+    constexpr int kStageBytes = kWBytes + NP * 128;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = a.stages;
+    const uint32_t base = smem_addr(dsm);
+    const uint32_t sbase = (base + 1023u) & ~1023u;
+    const uint32_t ncols = tmem_cols(MT * NP);
+
+    if (warp == 0) tmem_alloc(&tmem_base, ncols);
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    pdl_launch_dependents();
+    pdl_wait();  // AS comes from the gate kernel
+
+    int n = *a.count;
+    if (n < 0 || n > a.f) n = n < 0 ? 0 : a.f;
+    const int m0 = blockIdx.x * kTileM * MT;
+    const int split = blockIdx.y;
+    const int nkb_all = (n + kKB - 1) / kKB;
+    const int kb0 = (int)((long long)nkb_all * split / a.splits);
+    const int kb1 = (int)((long long)nkb_all * (split + 1) / a.splits);
+    const int Q = kb1 - kb0;
+    const bool bf = Tc<T>::kBf16;
+    const uint32_t idesc = umma_idesc(bf, true, NP);
+    const int last = n > 0 ? __ldg(a.idx + n - 1) : 0;
+    // a row of a stage is 16 * MT chunks, covered by consecutive lanes; thread
+    // t handles rows t / (16 MT) + i * 256 / (16 MT); their ids for the next
+    // step are loaded one step ahead
+    constexpr int kCh = 16 * MT;
+    constexpr int kRowsPerThread = kKB * kCh / kTcThreads;
+    auto row_ids = [&](int q, int (&j)[kRowsPerThread]) {
+#pragma unroll
+        for (int it = 0; it < kRowsPerThread; ++it) {
+            const int p = (kb0 + q) * kKB + tid / kCh + it * (kTcThreads / kCh);
+            j[it] = (q < Q && p < n) ? __ldg(a.idx + p) : last;
+        }
+    };
+    int jcur[kRowsPerThread], jnext[kRowsPerThread];
+    row_ids(0, jcur);
+
+    // called with q = 0, 1, 2, ... in order
+    auto issue = [&](int q) {
+        row_ids(q + 1, jnext);
+        if (q < Q) {
+            const int kb = kb0 + q;
+            const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
+            // 64 gathered rows x 128 * MT columns (256 * MT bytes) of W_down^T
+#pragma unroll
+            for (int it = 0; it < kRowsPerThread; ++it) {
+                const int i = tid + it * kTcThreads;
+                const int k = i / kCh, ch = i % kCh;
+                int j = jcur[it];
+                j = (j >= 0 && j < a.f) ? j : 0;
+                const int col = m0 + ch * 8;
+                const uint32_t dst = st + mnmaj_off<MT>(k, ch);
+                if (col < a.d) {
+                    cp16t(dst, a.w_down_t + (size_t)j * a.ldb + (size_t)col * 2);
+                } else {
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
+                }
+            }
+            const uint32_t sx = st + kWBytes;
+            const size_t koff = (size_t)kb * kKB * 2;
+            for (int i = tid; i < NP * 8; i += kTcThreads) {
+                const int r = i >> 3, ch = i & 7;
+                cp16t(sx + kmaj_off(r, ch), reinterpret_cast<const uint8_t *>(a.as) + (size_t)r * a.kp * 2 + koff + ch * 16);
+            }
+        }
+        cp_async_commit();
+#pragma unroll
+        for (int it = 0; it < kRowsPerThread; ++it) jcur[it] = jnext[it];
+    };
+
+    for (int q = 0; q < S - 2; ++q) issue(q);
+    bool ok = true;
+    for (int q = 0; q < Q; ++q) {
+        bool mine = q < 2 || stage_wait(&bars[(q - 2) % S], (uint32_t)(((q - 2) / S) & 1));
+        if (mine) issue(q + S - 2);
+        cp_async_wait_upto(S - 2);
+        fence_async_smem();
+        if (!__syncthreads_and(mine)) { ok = false; break; }
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
+            const uint32_t sx = st + kWBytes;
+            constexpr uint32_t kSbo = 2048 * MT;   // bytes between 8-row k groups
+#pragma unroll
+            for (int kk = 0; kk < kKB / 16; ++kk) {
+                const uint64_t bd = umma_desc(sx + kk * 32, 16, 1024);
+#pragma unroll
+                for (int t = 0; t < MT; ++t)
+                    umma(tmem + (uint32_t)(t * NP), umma_desc(st + t * 2048 + kk * 2 * kSbo, 1024, kSbo), bd, idesc,
+                         q > 0 || kk > 0);
+            }
+            umma_commit(&bars[q % S]);
+        }
+    }
+    if (ok && Q > 0) ok = __syncthreads_and(stage_wait(&bars[(Q - 1) % S], (uint32_t)(((Q - 1) / S) & 1)));
+    tc_fence_after();
+    if (warp < 4) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const int r = warp * 32 + lane, m = m0 + t * kTileM + r;
+            float y[NP];
+#pragma unroll
+            for (int c0 = 0; c0 < NP; ++c0) y[c0] = 0.f;
+            if (ok && Q > 0) {
+                const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(t * NP);
+#pragma unroll
+                for (int c0 = 0; c0 < NP; c0 += 8) {
+                    float v[8];
+                    tmem_ld8(lane_addr + (uint32_t)c0, v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[c0 + e] = v[e];
+                }
+            }
+            if (m < a.d) {
+#pragma unroll
+                for (int b = 0; b < NP / 2; ++b)
+                    if (b < a.B) a.part[((size_t)split * a.B + b) * a.dp + m] = y[2 * b] + y[2 * b + 1];
+            }
+        }
+    }
+    if (!ok && tid == 0) atomicOr(a.err, CS_DEVERR_TIMEOUT);
+    cp_async_wait<0>();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_free(tmem, ncols);
+    }
+}
+
+template <typename T, int NP>
+cudaError_t run_tc(const FfnArgs &f, cudaStream_t s) {
+    TcArgs a = {};
+    a.w_gate = static_cast<const uint8_t *>(f.w_gate);
+    a.w_up = static_cast<const uint8_t *>(f.w_up);
+    a.w_down_t = static_cast<const uint8_t *>(f.w_down_t);
+    a.bias = f.bias;
+    a.x = f.x;
+    a.idx = f.idx;
+    a.count = f.count;
+    a.xs = static_cast<uint16_t *>(f.tc_x);
+    a.as = static_cast<uint16_t *>(f.tc_a);
+    a.part = f.part;
+    a.err = f.err;
+    a.d = f.d;
+    a.f = f.f;
+    a.B = f.B;
+    a.ldb = f.ld * 2;
+    a.dk = f.d;  // d is a multiple of kKB on this path
+    a.kp = tc_act_pitch(f.f);
+    a.dp = f.dp;
+    const int sms = f.G > 0 ? f.G : 1;
+    const bool glu = f.w_up != nullptr;
+
+    // 1. X -> [hi; lo]
+    a.stages = 0;
+    cudaError_t e = launch(tc_split_kernel<T>, dim3(std::min(sms, (NP * a.dk + 255) / 256)), dim3(256), 0, s,
+                           pdl_enabled(), a, NP);
+    if (e != cudaSuccess) return e;
+
+    // 2. gate (and up) GEMM + activation, persistent over 128-neuron tiles;
+    //    128 K-elements (256 bytes of each row) per stage where four stages fit
+    {
+        const bool ks128 = !glu && a.dk % 128 == 0;
+        const int stage = ks128 ? 2 * (kTileBytes + NP * 128) : (glu ? 2 : 1) * kTileBytes + NP * 128;
+        a.stages = std::min(8, (int)(kTcSmemBudget / stage));
+        const size_t smem = (size_t)a.stages * stage + 1024;
+        auto fn = ks128 ? tc_gate_kernel<T, false, NP, 128>
+                        : (glu ? tc_gate_kernel<T, true, NP, 64> : tc_gate_kernel<T, false, NP, 64>);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const int tiles_max = (f.f + kTileM - 1) / kTileM;
+        e = launch(fn, dim3(std::min(sms, tiles_max)), dim3(kTcThreads), smem, s, pdl_enabled(), a);
+        if (e != cudaSuccess) return e;
+    }
+    // 3. down GEMM: two adjacent 128-row tiles of d per CTA (512 bytes of each
+    //    gathered row per stage) x split-K over the union
+    {
+        constexpr int MT = 2;
+        const int stage = MT * kTileBytes + NP * 128;
+        a.stages = std::min(8, (int)(kTcSmemBudget / stage));
+        const size_t smem = (size_t)a.stages * stage + 1024;
+        const int mt = (f.d + kTileM * MT - 1) / (kTileM * MT);
+        a.splits = std::max(1, std::min(sms / mt, 8));
+        auto fn = tc_down_kernel<T, NP, MT>;
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = launch(fn, dim3(mt, a.splits), dim3(kTcThreads), smem, s, pdl_enabled(), a);
+        if (e != cudaSuccess) return e;
+    }
+    // 4. fixed-order sum of the split partials (+ residual epilogue)
+    return launch_ffn_reduce(f.part, a.splits, f.B, f.d, f.dp, f.resid, f.scale, f.y, s);
+}
+
+template <typename T>
+cudaError_t run_tc_np(const FfnArgs &f, cudaStream_t s) {
+    const int n2 = 2 * f.B;
+    if (n2 <= 16) return run_tc<T, 16>(f, s);
+    if (n2 <= 32) return run_tc<T, 32>(f, s);
+    return run_tc<T, 64>(f, s);
+}
+
+}  // namespace
+
+int tc_act_pitch(int f) { return (f + kTileM - 1) / kTileM * kTileM; }
+
+static int tc_np(int B) { return 2 * B <= 16 ? 16 : (2 * B <= 32 ? 32 : 64); }
+
+size_t tc_x_bytes(int d, int B) { return align256((size_t)tc_np(B) * d * 2); }
+
+size_t tc_workspace_bytes(int d, int f, int B) {
+    if (B < 2 || B > kTcMaxB) return 0;
+    return tc_x_bytes(d, B) + align256((size_t)tc_np(B) * tc_act_pitch(f) * 2);
+}
+
+bool tc_path_applies(const FfnArgs &f) {
+    if (!f.tc_x || !f.tc_a || f.preact) return false;
+    if (f.dtype == CS_F32 || f.B < tc_min_batch() || f.B > kTcMaxB) return false;
+    if (f.d % kKB != 0 || (f.ld * 2) % 16 != 0) return false;
+    return true;
+}
+
+int tc_min_batch() {
+    static const int v = [] {
+        const char *e = getenv("CS_TC_MIN_B");
+        const int b = e ? atoi(e) : kTcDefaultMinB;
+        return b < 2 ? 2 : b;
+    }();
+    return v;
+}
+
+cudaError_t launch_ffn_tc(const FfnArgs &f, cudaStream_t s) {
+    return f.dtype == CS_F16 ? run_tc_np<__half>(f, s) : run_tc_np<__nv_bfloat16>(f, s);
+}
+
+}  // namespace cs

@@ -32,6 +32,7 @@ struct WsLayout {
     size_t st_count = 0;    // [2] int32 stack counts
     size_t st_h = 0;        // [r] fp32 stack predictor bottleneck
     size_t bt_a = 0;        // [Bmax, fu] fp32 batched activations
+    size_t tc = 0;          // tensor-core path buffers (tc_workspace_bytes), 0 bytes when B < 2
     size_t total = 0;
     int G = 0;              // partial-sum slots (CTAs of the gather kernel)
     int dp = 0;             // padded row length of partial sums
@@ -319,8 +320,25 @@ struct FfnArgs {
     uint32_t *err;
     float *part;            // workspace partials
     int G, dp;
+    void *tc_x = nullptr;   // tensor-core path: [NP, d] split activations (or null)
+    void *tc_a = nullptr;   // tensor-core path: [NP, roundup(f, 128)] split activations (or null)
 };
 cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s);
+
+// y[b, :] = (resid[b, :] + scale *) sum_{c < G} part[c, b, :], fixed order
+cudaError_t launch_ffn_reduce(const float *part, int G, int B, int d, int dp, const float *resid, float scale,
+                              float *y, cudaStream_t s);
+
+// Tensor-core (tcgen05) batched path for dense unions: fp16 / bf16 weights,
+// d a multiple of 64, 2 <= B <= kTcMaxB.
+constexpr int kTcMaxB = 32;
+constexpr int kTcDefaultMinB = 4;   // batch from which the tensor-core path is taken
+int tc_min_batch();                 // kTcDefaultMinB, or CS_TC_MIN_B from the environment
+int tc_act_pitch(int f);
+size_t tc_workspace_bytes(int d, int f, int B);
+size_t tc_x_bytes(int d, int B);   // the first of the two buffers
+bool tc_path_applies(const FfnArgs &a);
+cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s);
 
 struct PreactArgs {
     int d, f, ld;
