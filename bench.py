@@ -142,6 +142,42 @@ def profile_traffic(kernel, workload):
 
 
 # ----------------------------------------------------------------------------
+# replicas across ranks (one process per GPU, no data-path collective)
+# ----------------------------------------------------------------------------
+
+def init_dist(world):
+    """Join the process group (NCCL on GPUs, gloo on CPU-only hosts)."""
+    if world <= 1:
+        return
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+
+def max_over_ranks(ms, world):
+    """The largest per-rank elapsed time, returned on every rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def replica_value(units_per_rank, world, ms):
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    return world * units_per_rank / (ms / 1e3)
+
+
+# ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
 
@@ -243,7 +279,7 @@ def run_ours(args, W, rank, world):
             g.replay()
     s.synchronize()
     if world > 1:
-        torch.distributed.barrier()
+        barrier(world)
     torch.cuda.synchronize()
     clk = Clocks(dev)
     clk.start()
@@ -258,11 +294,8 @@ def run_ours(args, W, rank, world):
     clocks = clk.stop()
     ms = e0.elapsed_time(e1)
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-        torch.distributed.barrier()
+    ms = max_over_ranks(ms, world)
+    barrier(world)
     assert cs.cs_get_device_error(ws, stream=s) == 0
 
     # roofline pass: the FFN calls of the first NB steps alone, back to back on
@@ -335,7 +368,7 @@ def run_ours(args, W, rank, world):
     step_s = ms / 1e3 / K
     ffn_gbs = ffn_b / ffn_avg_s / 1e9
     res = {
-        "metric": METRIC, "value": world * K / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": replica_value(K, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "d": d, "f": f, "r": r, "k": k if W["mode"] == "topk" else None,
@@ -410,7 +443,7 @@ def run_stack(args, W, rank, world):
     sm.synchronize()
     K = max(1, args.steps)
     if world > 1:
-        torch.distributed.barrier()
+        barrier(world)
     clk = Clocks(dev)
     clk.start()
     time.sleep(0.3)
@@ -423,10 +456,7 @@ def run_stack(args, W, rank, world):
     e1.synchronize()
     clocks = clk.stop()
     ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world)
     assert cs.cs_get_device_error(ws, stream=sm) == 0
     # e2e through the API with host buffers
     KE = min(K, 50)
@@ -451,7 +481,7 @@ def run_stack(args, W, rank, world):
     hbm, src = peaks()
     step_s = ms / 1e3 / K
     return {
-        "metric": METRIC, "value": world * K / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": replica_value(K, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "layers": L, "d": d, "f": f, "r": r, "k": k, "selection": "topk",
@@ -548,7 +578,7 @@ def run_union(args, W, rank, world):
             g.replay()
     s.synchronize()
     if world > 1:
-        torch.distributed.barrier()
+        barrier(world)
     torch.cuda.synchronize()
     clk = Clocks(dev)
     clk.start()
@@ -562,11 +592,8 @@ def run_union(args, W, rank, world):
     e1.synchronize()
     clocks = clk.stop()
     ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-        torch.distributed.barrier()
+    ms = max_over_ranks(ms, world)
+    barrier(world)
     assert cs.cs_get_device_error(ws, stream=s) == 0
 
     # roofline pass: the batched FFN calls alone (unions already computed)
@@ -622,7 +649,7 @@ def run_union(args, W, rank, world):
     launches = 1 + (4 if tc else 2)
     flops = 2 * mean_u * d * 2 * (2 * B)   # two GEMMs, N = 2B (hi and lo halves)
     res = {
-        "metric": METRIC, "value": world * B * K / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": replica_value(B * K, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "d": d, "f": f, "batch": B, "global_batch": world * B,
@@ -736,9 +763,7 @@ def main():
                              "sample": f"{n} single-layer decode steps (predict, select, gathered FFN; layer 0) of the workload, fp64 CPU oracle" + (f", scaled to {W['L']} layers" if "L" in W else "")},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
-    if world > 1:
-        import torch
-        torch.distributed.init_process_group("nccl")
+    init_dist(world)
     if "L" in W:
         res = run_stack(args, W, rank, world)
     elif "union" in W:

@@ -1,0 +1,73 @@
+"""The benchmark's multi-rank (replica) path on CPU: two gloo ranks.
+
+Under torchrun every rank runs the same workload on its own GPU with no
+data-path collective; the ranks only agree on the slowest rank's elapsed time,
+and the reported value is the units all ranks processed over that time.  These
+tests run that agreement with the gloo backend in two spawned processes.
+"""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), CUDA_VISIBLE_DEVICES="")
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    bench.init_dist(world)
+    backend = dist.get_backend()
+    ms = bench.max_over_ranks(1.5 + rank, world)     # rank 1 is the slower one
+    bench.barrier(world)
+    q.put((rank, backend, ms, bench.replica_value(100, world, ms)))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_rank():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in range(2))
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [g[0] for g in got] == [0, 1]
+    for rank, backend, ms, v in got:
+        assert backend == "gloo"
+        assert ms == 2.5
+        assert v == pytest.approx(2 * 100 / 2.5e-3)
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    bench.init_dist(1)
+    bench.barrier(1)
+    assert bench.max_over_ranks(3.0, 1) == 3.0
+    assert bench.replica_value(10, 1, 2.0) == pytest.approx(5000.0)
+
+
+def test_reference_arm_on_a_nonzero_rank_prints_nothing():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
