@@ -26,6 +26,7 @@
 // the residual epilogue), so y is bit-reproducible.
 // (One-dimensional bulk copies were measured slower for rows of ~10 KB: the
 // copy engine of an SM streams far below its share of HBM bandwidth.)
+#include <algorithm>
 #include <utility>
 
 #include "cs_internal.cuh"
@@ -412,7 +413,10 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     const int nrow = (a.preact ? 0 : 1) + (a.w_up ? 1 : 0) + 1;
     const size_t per_neuron = (size_t)nrow * k.nvec * 16;
     // ring of sg groups of ng neurons: as deep as the budget allows
-    int nst = (int)(kRingBudget / per_neuron);
+    const size_t budget = a.ring_bytes ? std::min(a.ring_bytes, kRingBudget) : kRingBudget;
+    int nst = (int)(budget / per_neuron);
+    // a reduced ring keeps at least two neurons
+    if (a.ring_bytes && nst < 2) nst = 2;
     if (nst < 2) return cudaErrorInvalidValue;
     // three ring groups keep one group in flight while two are in use
     if (nst >= 3 * kNgMax) { k.ng = kNgMax; k.sg = 3; }

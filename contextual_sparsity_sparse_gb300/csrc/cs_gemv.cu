@@ -150,13 +150,13 @@ __global__ void __launch_bounds__(kThreads) stream_gemv_kernel(const GemvK a) {
 }
 
 template <typename T, int TB, int EPI>
-cudaError_t run_tb(const GemvK &k0, cudaStream_t s) {
+cudaError_t run_tb(const GemvK &k0, cudaStream_t s, size_t per_cta) {
     GemvK k = k0;
     int sms = device_sm_count();
     sms = sms < 1 ? 1 : sms;
     const size_t vbytes = ((size_t)TB * ((k.ncols + 7) & ~7) * 4 + 127) & ~size_t(127);
-    // two CTAs per SM: each gets half of ~220 KB for its vector and two buffers
-    const size_t per_cta = 110 * 1024;
+    // two CTAs per SM: each gets per_cta (half of ~220 KB by default) for its
+    // vector and two buffers
     size_t chunk_budget = per_cta > vbytes ? (per_cta - vbytes) / 2 : 0;
     chunk_budget = std::min<size_t>(chunk_budget, 48 * 1024);
     k.rows_per_cta = std::max(1, (k.nrows + 2 * sms - 1) / (2 * sms));
@@ -171,21 +171,24 @@ cudaError_t run_tb(const GemvK &k0, cudaStream_t s) {
 }
 
 template <typename T, int EPI>
-cudaError_t run_gemv(const GemvK &k, cudaStream_t s) {
+cudaError_t run_gemv(const GemvK &k, cudaStream_t s, size_t per_cta) {
     // tokens per CTA: as many as fit beside the weight buffers (weights are
     // re-streamed for each group of TB tokens)
     const size_t row_f = (size_t)((k.ncols + 7) & ~7) * 4;
-    if (k.B >= 4 && 4 * row_f <= 48 * 1024) return run_tb<T, 4, EPI>(k, s);
-    if (k.B >= 2 && 2 * row_f <= 48 * 1024) return run_tb<T, 2, EPI>(k, s);
-    return run_tb<T, 1, EPI>(k, s);
+    if (k.B >= 4 && 4 * row_f <= 48 * 1024) return run_tb<T, 4, EPI>(k, s, per_cta);
+    if (k.B >= 2 && 2 * row_f <= 48 * 1024) return run_tb<T, 2, EPI>(k, s, per_cta);
+    return run_tb<T, 1, EPI>(k, s, per_cta);
 }
 
+constexpr size_t kGemvCta = 110 * 1024;       // two CTAs per SM
+constexpr size_t kGemvCtaSmall = 60 * 1024;   // beside a gather CTA
+
 template <int EPI>
-cudaError_t dispatch(cs_dtype dt, const GemvK &k, cudaStream_t s) {
+cudaError_t dispatch(cs_dtype dt, const GemvK &k, cudaStream_t s, size_t per_cta = kGemvCta) {
     switch (dt) {
-    case CS_F32: return run_gemv<float, EPI>(k, s);
-    case CS_F16: return run_gemv<__half, EPI>(k, s);
-    default: return run_gemv<__nv_bfloat16, EPI>(k, s);
+    case CS_F32: return run_gemv<float, EPI>(k, s, per_cta);
+    case CS_F16: return run_gemv<__half, EPI>(k, s, per_cta);
+    default: return run_gemv<__nv_bfloat16, EPI>(k, s, per_cta);
     }
 }
 
@@ -203,7 +206,8 @@ cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s) {
     k.B = a.B;
     k.out = a.h;
     k.err = a.err;
-    cudaError_t e = dispatch<EPI_RELU>(a.dtype, k, s);
+    const size_t per_cta = a.small_smem ? kGemvCtaSmall : kGemvCta;
+    cudaError_t e = dispatch<EPI_RELU>(a.dtype, k, s, per_cta);
     if (e != cudaSuccess) return e;
     // P2: s[b, j] = sum_i P_up[j, i] h[b, i]
     k.W = static_cast<const uint8_t *>(a.p_up);
@@ -212,7 +216,7 @@ cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s) {
     k.nrows = a.f;
     k.v = a.h;
     k.out = a.scores;
-    return dispatch<EPI_NONE>(a.dtype, k, s);
+    return dispatch<EPI_NONE>(a.dtype, k, s, per_cta);
 }
 
 cudaError_t launch_preact(const PreactArgs &a, cudaStream_t s) {

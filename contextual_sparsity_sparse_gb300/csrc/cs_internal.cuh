@@ -287,6 +287,7 @@ struct PredictArgs {
     float *h;      // [B, r]
     float *scores; // [B, f]
     uint32_t *err = nullptr;
+    bool small_smem = false;  // ~60 KB per CTA, to share SMs with a gather CTA
 };
 cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s);
 
@@ -320,6 +321,7 @@ struct FfnArgs {
     uint32_t *err;
     float *part;            // workspace partials
     int G, dp;
+    size_t ring_bytes = 0;  // gather ring budget; 0 = the default (most of an SM's shared memory)
     void *tc_x = nullptr;   // tensor-core path: [NP, d] split activations (or null)
     void *tc_a = nullptr;   // tensor-core path: [NP, roundup(f, 128)] split activations (or null)
 };
