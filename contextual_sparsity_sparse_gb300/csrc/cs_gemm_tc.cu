@@ -342,19 +342,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) 
     }
 }
 
-// ---- down GEMM -> per-split partial y ----------------------------------------
+// ---- down GEMM, stream-K -> partial y per (CTA, column group) ------------------
+// Work units are (column group g of 128 * MT output rows, k-block of 64 union
+// neurons), g-major; CTA c of P takes units [U c / P, U (c+1) / P), so every
+// CTA gets the same amount of work.  Its range covers at most two column
+// groups (when there are at most P groups); for each it writes the partial
+// sum of its k-blocks to slot (c, 0) or (c, 1).  tc_reduce_kernel adds, for
+// every column, the slots of the CTAs that cover its group, in CTA order.
+__device__ __forceinline__ long long sk_start(int c, long long U, int P) { return U * c / P; }
+// the CTA whose unit range holds unit u (0 <= u < U)
+__device__ __forceinline__ int sk_owner(long long u, long long U, int P) {
+    int c = (int)(((u + 1) * P - 1) / U);
+    c = c < 0 ? 0 : (c >= P ? P - 1 : c);
+    while (c + 1 < P && sk_start(c + 1, U, P) <= u) ++c;
+    while (c > 0 && sk_start(c, U, P) > u) --c;
+    return c;
+}
+
 template <typename T, int NP, int MT>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t bars[8];
     __shared__ uint32_t tmem_base;
-    constexpr int kWBytes = MT * kTileBytes;                // 64 rows x 128 * MT columns
+    constexpr int kCols = kTileM * MT;                      // output rows of a column group
+    constexpr int kWBytes = MT * kTileBytes;                // 64 rows x kCols columns
     constexpr int kStageBytes = kWBytes + NP * 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.stages;
     const uint32_t base = smem_addr(dsm);
     const uint32_t sbase = (base + 1023u) & ~1023u;
-    const uint32_t ncols = tmem_cols(MT * NP);
+    constexpr int kSegCols = MT * NP;                       // accumulator columns of one segment
+    const uint32_t ncols = tmem_cols(2 * kSegCols);          // two segments, read at the end
 
     if (warp == 0) tmem_alloc(&tmem_base, ncols);
     if (tid == 0) {
@@ -371,37 +389,48 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
 
     int n = *a.count;
     if (n < 0 || n > a.f) n = n < 0 ? 0 : a.f;
-    const int m0 = blockIdx.x * kTileM * MT;
-    const int split = blockIdx.y;
-    const int nkb_all = (n + kKB - 1) / kKB;
-    const int kb0 = (int)((long long)nkb_all * split / a.splits);
-    const int kb1 = (int)((long long)nkb_all * (split + 1) / a.splits);
-    const int Q = kb1 - kb0;
+    const int NG = (a.d + kCols - 1) / kCols;
+    const int NKB = (n + kKB - 1) / kKB;
+    const long long U = (long long)NG * NKB;
+    const int P = gridDim.x, c = blockIdx.x;
+    const long long u0 = U > 0 ? sk_start(c, U, P) : 0;
+    const int Q = U > 0 ? (int)(sk_start(c + 1, U, P) - u0) : 0;
     const bool bf = Tc<T>::kBf16;
     const uint32_t idesc = umma_idesc(bf, true, NP);
     const int last = n > 0 ? __ldg(a.idx + n - 1) : 0;
+    // unit cursors (column group, k-block): one division here, then +1 steps
+    struct Cur {
+        int g, kb;
+    };
+    const Cur first = NKB > 0 ? Cur{(int)(u0 / NKB), (int)(u0 % NKB)} : Cur{0, 0};
+    auto step = [&](Cur &u) {
+        if (++u.kb == NKB) { u.kb = 0; ++u.g; }
+    };
     // a row of a stage is 16 * MT chunks, covered by consecutive lanes; thread
     // t handles rows t / (16 MT) + i * 256 / (16 MT); their ids for the next
     // step are loaded one step ahead
     constexpr int kCh = 16 * MT;
     constexpr int kRowsPerThread = kKB * kCh / kTcThreads;
-    auto row_ids = [&](int q, int (&j)[kRowsPerThread]) {
+    auto row_ids = [&](bool live, int kb, int (&j)[kRowsPerThread]) {
 #pragma unroll
         for (int it = 0; it < kRowsPerThread; ++it) {
-            const int p = (kb0 + q) * kKB + tid / kCh + it * (kTcThreads / kCh);
-            j[it] = (q < Q && p < n) ? __ldg(a.idx + p) : last;
+            const int p = kb * kKB + tid / kCh + it * (kTcThreads / kCh);
+            j[it] = (live && p < n) ? __ldg(a.idx + p) : last;
         }
     };
     int jcur[kRowsPerThread], jnext[kRowsPerThread];
-    row_ids(0, jcur);
+    Cur ic = first;   // unit of the next issue
+    Cur pc = first;   // unit after it (its row ids are prefetched)
+    step(pc);
+    row_ids(Q > 0, ic.kb, jcur);
 
     // called with q = 0, 1, 2, ... in order
     auto issue = [&](int q) {
-        row_ids(q + 1, jnext);
+        row_ids(q + 1 < Q, pc.kb, jnext);
         if (q < Q) {
-            const int kb = kb0 + q;
+            const int kb = ic.kb, m0 = ic.g * kCols;
             const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
-            // 64 gathered rows x 128 * MT columns (256 * MT bytes) of W_down^T
+            // 64 gathered rows x kCols columns (256 * MT bytes) of W_down^T
 #pragma unroll
             for (int it = 0; it < kRowsPerThread; ++it) {
                 const int i = tid + it * kTcThreads;
@@ -426,10 +455,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
         cp_async_commit();
 #pragma unroll
         for (int it = 0; it < kRowsPerThread; ++it) jcur[it] = jnext[it];
+        step(ic);
+        step(pc);
     };
 
     for (int q = 0; q < S - 2; ++q) issue(q);
     bool ok = true;
+    Cur cc = first;        // unit being multiplied
+    int seg = 0;           // slot (and accumulator set) of the current column group
+    bool fresh = true;     // the next MMA starts a new accumulation
     for (int q = 0; q < Q; ++q) {
         bool mine = q < 2 || stage_wait(&bars[(q - 2) % S], (uint32_t)(((q - 2) / S) & 1));
         if (mine) issue(q + S - 2);
@@ -440,29 +474,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
             tc_fence_after();
             const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
             const uint32_t sx = st + kWBytes;
+            const uint32_t acc = tmem + (uint32_t)(seg * kSegCols);
             constexpr uint32_t kSbo = 2048 * MT;   // bytes between 8-row k groups
 #pragma unroll
             for (int kk = 0; kk < kKB / 16; ++kk) {
                 const uint64_t bd = umma_desc(sx + kk * 32, 16, 1024);
 #pragma unroll
                 for (int t = 0; t < MT; ++t)
-                    umma(tmem + (uint32_t)(t * NP), umma_desc(st + t * 2048 + kk * 2 * kSbo, 1024, kSbo), bd, idesc,
-                         q > 0 || kk > 0);
+                    umma(acc + (uint32_t)(t * NP), umma_desc(st + t * 2048 + kk * 2 * kSbo, 1024, kSbo), bd, idesc,
+                         !(fresh && kk == 0));
             }
             umma_commit(&bars[q % S]);
         }
+        fresh = false;
+        // a range covers at most two column groups: the second accumulates
+        // into the second set, so no MMA has to finish before it starts
+        if (cc.kb == NKB - 1 && q < Q - 1) {
+            ++seg;
+            fresh = true;
+        }
+        step(cc);
     }
+    // every segment's partial sums to its slot, once the last MMAs are done
     if (ok && Q > 0) ok = __syncthreads_and(stage_wait(&bars[(Q - 1) % S], (uint32_t)(((Q - 1) / S) & 1)));
     tc_fence_after();
-    if (warp < 4) {
+    if (ok && Q > 0 && warp < 4) {
+        for (int sg = 0; sg <= seg; ++sg) {
+            const size_t slot = (size_t)(c * 2 + sg) * a.B;
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
-            const int r = warp * 32 + lane, m = m0 + t * kTileM + r;
-            float y[NP];
-#pragma unroll
-            for (int c0 = 0; c0 < NP; ++c0) y[c0] = 0.f;
-            if (ok && Q > 0) {
-                const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(t * NP);
+            for (int t = 0; t < MT; ++t) {
+                const int r = t * kTileM + warp * 32 + lane;
+                float y[NP];
+                const uint32_t lane_addr =
+                    tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(sg * kSegCols + t * NP);
 #pragma unroll
                 for (int c0 = 0; c0 < NP; c0 += 8) {
                     float v[8];
@@ -470,11 +514,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
 #pragma unroll
                     for (int e = 0; e < 8; ++e) y[c0 + e] = v[e];
                 }
-            }
-            if (m < a.d) {
 #pragma unroll
                 for (int b = 0; b < NP / 2; ++b)
-                    if (b < a.B) a.part[((size_t)split * a.B + b) * a.dp + m] = y[2 * b] + y[2 * b + 1];
+                    if (b < a.B) a.part[(slot + b) * kCols + r] = y[2 * b] + y[2 * b + 1];
             }
         }
     }
@@ -486,6 +528,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
         tc_fence_after();
         tmem_free(tmem, ncols);
     }
+}
+
+// y[b, m] = (resid[b, m] + scale *) the stream-K partials of m's column
+// group, in CTA order
+template <int MT>
+__global__ void __launch_bounds__(256) tc_reduce_kernel(const TcArgs a, int P, const float *resid, float scale,
+                                                       float *y) {
+    constexpr int kCols = kTileM * MT;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int m = blockIdx.x * 256 + threadIdx.x, b = blockIdx.y;
+    if (m >= a.d) return;
+    int n = *a.count;
+    if (n < 0 || n > a.f) n = n < 0 ? 0 : a.f;
+    const int NG = (a.d + kCols - 1) / kCols;
+    const int NKB = (n + kKB - 1) / kKB;
+    const long long U = (long long)NG * NKB;
+    const int g = m / kCols;
+    float sum = 0.f;
+    if (U > 0) {
+        const int c_lo = sk_owner((long long)g * NKB, U, P), c_hi = sk_owner((long long)(g + 1) * NKB - 1, U, P);
+        for (int c = c_lo; c <= c_hi; ++c) {
+            const long long st = sk_start(c, U, P);
+            if (sk_start(c + 1, U, P) == st) continue;  // an empty range wrote no slot
+            const int seg = g - (int)(st / NKB);
+            sum += __ldcg(a.part + ((size_t)(c * 2 + seg) * a.B + b) * kCols + (m - g * kCols));
+        }
+    }
+    const size_t o = (size_t)b * a.d + m;
+    y[o] = resid ? fmaf(scale, sum, resid[o]) : sum;
 }
 
 template <typename T, int NP>
@@ -533,23 +605,22 @@ cudaError_t run_tc(const FfnArgs &f, cudaStream_t s) {
         e = launch(fn, dim3(std::min(sms, tiles_max)), dim3(kTcThreads), smem, s, pdl_enabled(), a);
         if (e != cudaSuccess) return e;
     }
-    // 3. down GEMM: two adjacent 128-row tiles of d per CTA (512 bytes of each
-    //    gathered row per stage) x split-K over the union
+    // 3. down GEMM, stream-K over (256-row column group, 64-neuron k-block)
+    //    units: every CTA the same share; 512 bytes of each gathered row per stage
+    constexpr int MT = 2;
     {
-        constexpr int MT = 2;
         const int stage = MT * kTileBytes + NP * 128;
         a.stages = std::min(8, (int)(kTcSmemBudget / stage));
         const size_t smem = (size_t)a.stages * stage + 1024;
-        const int mt = (f.d + kTileM * MT - 1) / (kTileM * MT);
-        a.splits = std::max(1, std::min(sms / mt, 8));
         auto fn = tc_down_kernel<T, NP, MT>;
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = launch(fn, dim3(mt, a.splits), dim3(kTcThreads), smem, s, pdl_enabled(), a);
+        e = launch(fn, dim3(sms), dim3(kTcThreads), smem, s, pdl_enabled(), a);
         if (e != cudaSuccess) return e;
     }
-    // 4. fixed-order sum of the split partials (+ residual epilogue)
-    return launch_ffn_reduce(f.part, a.splits, f.B, f.d, f.dp, f.resid, f.scale, f.y, s);
+    // 4. the partials of each column, in CTA order (+ residual epilogue)
+    return launch(tc_reduce_kernel<MT>, dim3((f.d + 255) / 256, f.B), dim3(256), 0, s, pdl_enabled(), a, sms,
+                  f.resid, f.scale, f.y);
 }
 
 template <typename T>
@@ -577,6 +648,9 @@ bool tc_path_applies(const FfnArgs &f) {
     if (!f.tc_x || !f.tc_a || f.preact) return false;
     if (f.dtype == CS_F32 || f.B < tc_min_batch() || f.B > kTcMaxB) return false;
     if (f.d % kKB != 0 || (f.ld * 2) % 16 != 0) return false;
+    // stream-K partials (2 slots x 256 columns per CTA and token) fit the
+    // workspace's partial-sum region, and a CTA's range spans <= 2 column groups
+    if (f.d < 512 || (f.d + 255) / 256 > f.G) return false;
     return true;
 }
 
