@@ -52,7 +52,6 @@ constexpr int kTileM = 128;            // rows of an MMA tile
 constexpr int kKB = 64;                // K elements per stage: one 128-byte swizzle row
 constexpr int kTileBytes = kTileM * kKB * 2;   // 16 KB per 128 x 64 operand tile
 constexpr size_t kTcSmemBudget = 200 * 1024;
-constexpr int kIdxMax = 2048 + kTileM; // union ids one gate CTA stages
 
 struct TcArgs {
     const uint8_t *w_gate, *w_up, *w_down_t;
@@ -62,7 +61,9 @@ struct TcArgs {
     const int32_t *count;  // device count
     uint16_t *xs;          // [NP, dk]
     uint16_t *as;          // [NP, kp]
-    float *part;           // [splits, B, dp]
+    float *part;           // down GEMM: [P, 2, B, 256] stream-K partials
+    float *pieces;         // gate GEMM: [P, 3, 128, NP or 2 NP] partial tile sums
+    unsigned *tile_count;  // gate GEMM: [2P] arrivals per tile, zeroed by the split kernel
     uint32_t *err;
     int d, f, B, ldb, dk, kp, dp, splits, stages;
 };
@@ -150,9 +151,10 @@ __device__ __forceinline__ uint32_t tmem_cols(int c) {
 
 // ---- X -> [hi; lo] rows ------------------------------------------------------
 template <typename T>
-__global__ void tc_split_kernel(const TcArgs a, int np) {
+__global__ void tc_split_kernel(const TcArgs a, int np, int ncount) {
     pdl_launch_dependents();
     pdl_wait();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncount; i += gridDim.x * blockDim.x) a.tile_count[i] = 0u;
     const size_t total = (size_t)np * a.dk;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
         const int n = (int)(i / a.dk), c = (int)(i % a.dk);
@@ -184,24 +186,58 @@ __device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity) {
     return mbar_wait(bar, parity, 1000000000ull);
 }
 
-// ---- gate (and up) GEMM + activation -----------------------------------------
+// ---- gate (and up) GEMM + activation, stream-K ----------------------------------
+// Work units are (tile t of 128 union neurons, k-block of KS elements of d),
+// t-major; CTA c of P takes units [U c / P, U (c+1) / P).  With at most 2P
+// tiles a CTA's range touches at most three tiles ("segments"); each segment
+// accumulates into its own tensor-memory set and all are read once the last
+// MMA is done.  A tile covered by one CTA gets its activation at once; a tile
+// shared by several CTAs has each CTA's partial sums written to a piece slot,
+// and the CTA whose arrival completes the tile's counter adds the pieces in
+// CTA order (so the result does not depend on who arrives last) and applies
+// the bias and activation.
+constexpr int kGateSegMax = 3;
+
+// sk_start / sk_owner: see the down GEMM below
+__device__ __forceinline__ long long sk_start(int c, long long U, int P);
+__device__ __forceinline__ int sk_owner(long long u, long long U, int P);
+
+// act = relu(g + bias) (* u), written as the hi / lo rows of AS
+template <typename T, bool GLU, int NP>
+__device__ __forceinline__ void gate_act_out(const TcArgs &a, const float (&g)[NP], const float (&u)[NP], float bias,
+                                             bool live, int p) {
+#pragma unroll
+    for (int b = 0; b < NP / 2; ++b) {
+        if (b < a.B) {
+            float act = fmaxf(g[2 * b] + g[2 * b + 1] + bias, 0.f);
+            if (GLU) act *= u[2 * b] + u[2 * b + 1];
+            act = live ? act : 0.f;
+            const uint16_t hi = Tc<T>::bits(act);
+            const uint16_t lo = Tc<T>::bits(act - Tc<T>::val(hi));
+            a.as[(size_t)(2 * b) * a.kp + p] = hi;
+            a.as[(size_t)(2 * b + 1) * a.kp + p] = lo;
+        }
+    }
+}
+
 template <typename T, bool GLU, int NP, int KS>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t bars[8];
     __shared__ uint32_t tmem_base;
-    __shared__ int s_idx[kIdxMax];
+    __shared__ int s_idx[kGateSegMax * kTileM];
+    __shared__ int s_last[kGateSegMax];
     constexpr int KA = KS / kKB;                           // 64-element swizzle atoms per row per stage
     constexpr int kA = GLU ? 2 : 1;                        // weight tiles per stage besides X
     constexpr int kWBytes = KA * kTileBytes;               // one weight tile: [atom][128 rows][128 B]
     constexpr int kXAtom = NP * 128;                       // one X atom: [NP rows][128 B]
     constexpr int kStageBytes = kA * kWBytes + KA * kXAtom;
-    constexpr uint32_t kCols = GLU ? 2 * NP : NP;
+    constexpr int kSetCols = GLU ? 2 * NP : NP;            // accumulator columns of one segment
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.stages;
     const uint32_t base = smem_addr(dsm);
     const uint32_t sbase = (base + 1023u) & ~1023u;       // 1024-byte aligned stages
-    const uint32_t ncols = tmem_cols((int)kCols);
+    const uint32_t ncols = tmem_cols(kGateSegMax * kSetCols);
 
     if (warp == 0) tmem_alloc(&tmem_base, ncols);
     if (tid == 0) {
@@ -214,20 +250,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) 
     const uint32_t tmem = tmem_base;
 
     pdl_launch_dependents();
-    pdl_wait();  // XS, the union list and its count come from earlier kernels
+    pdl_wait();  // XS, the union list, its count and the zeroed counters come from earlier kernels
 
     int n = *a.count;
     if (n < 0 || n > a.f) {
         if (tid == 0 && blockIdx.x == 0) atomicOr(a.err, CS_DEVERR_COUNT);
         n = n < 0 ? 0 : a.f;
     }
-    const int ntiles = (n + kTileM - 1) / kTileM;
-    const int G = gridDim.x, c = blockIdx.x;
-    const int my_tiles = c < ntiles ? (ntiles - c + G - 1) / G : 0;
-    // this CTA's ids, tile after tile (positions past n repeat a valid row; their
+    const int NT = (n + kTileM - 1) / kTileM;
+    const int NKB = a.dk / KS;
+    const long long U = (long long)NT * NKB;
+    const int P = gridDim.x, c = blockIdx.x;
+    const long long u0 = U > 0 ? sk_start(c, U, P) : 0;
+    const int Q = U > 0 ? (int)(sk_start(c + 1, U, P) - u0) : 0;
+    const int t_first = Q > 0 ? (int)(u0 / NKB) : 0;
+    const int kb_first = Q > 0 ? (int)(u0 % NKB) : 0;
+    const int nseg = Q > 0 ? (int)((u0 + Q - 1) / NKB) - t_first + 1 : 0;   // <= kGateSegMax
+    const int kb_end = Q > 0 ? (int)((u0 + Q - 1) % NKB) + 1 : 0;           // last segment's end
+
+    // ids of this CTA's tiles (positions past n repeat a valid row; their
     // activations are written as 0)
-    for (int i = tid; i < my_tiles * kTileM; i += kTcThreads) {
-        const int p = (c + (i / kTileM) * G) * kTileM + (i % kTileM);
+    for (int i = tid; i < nseg * kTileM; i += kTcThreads) {
+        const int p = (t_first + i / kTileM) * kTileM + (i % kTileM);
         int j = p < n ? a.idx[p] : (n > 0 ? a.idx[n - 1] : 0);
         if (j < 0 || j >= a.f) {
             atomicOr(a.err, CS_DEVERR_INDEX);
@@ -237,22 +281,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) 
     }
     __syncthreads();
 
-    const int nkb = a.dk / KS;
-    const int Q = my_tiles * nkb;
     const bool bf = Tc<T>::kBf16;
     const uint32_t idesc = umma_idesc(bf, false, NP);
+    struct Cur {
+        int lt, kb;   // tile relative to t_first, k-block
+    };
+    auto step = [&](Cur &u) {
+        if (++u.kb == NKB) { u.kb = 0; ++u.lt; }
+    };
+    Cur ic{0, kb_first};   // unit of the next issue
 
-    // copies of step q (tile q / nkb, k-block q % nkb) into stage q % S; the
-    // lanes of a warp cover contiguous bytes of a row (KS * 2 bytes per row)
+    // copies of the next unit into stage q % S; the lanes of a warp cover
+    // contiguous bytes of a row (KS * 2 bytes per row); called with q in order
     auto issue = [&](int q) {
         if (q < Q) {
-            const int lt = q / nkb, kb = q % nkb;
             const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
-            const size_t koff = (size_t)kb * KS * 2;
+            const size_t koff = (size_t)ic.kb * KS * 2;
             for (int i = tid; i < kTileM * 8 * KA; i += kTcThreads) {
                 const int r = i / (8 * KA), ch = i % (8 * KA);
                 const uint32_t off = (uint32_t)((ch >> 3) * kTileBytes) + kmaj_off(r, ch & 7);
-                const size_t roff = (size_t)s_idx[lt * kTileM + r] * a.ldb + koff + ch * 16;
+                const size_t roff = (size_t)s_idx[ic.lt * kTileM + r] * a.ldb + koff + ch * 16;
                 cp16t(st + off, a.w_gate + roff);
                 if (GLU) cp16t(st + kWBytes + off, a.w_up + roff);
             }
@@ -262,12 +310,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) 
                 cp16t(sx + (uint32_t)((ch >> 3) * kXAtom) + kmaj_off(r, ch & 7),
                       reinterpret_cast<const uint8_t *>(a.xs) + (size_t)r * a.dk * 2 + koff + ch * 16);
             }
+            step(ic);
         }
         cp_async_commit();
     };
 
     for (int q = 0; q < S - 2; ++q) issue(q);
     bool ok = true;
+    Cur cc{0, kb_first};   // unit being multiplied
     for (int q = 0; q < Q; ++q) {
         // every decision to stop is taken by the whole block at a barrier
         bool mine = q < 2 || stage_wait(&bars[(q - 2) % S], (uint32_t)(((q - 2) / S) & 1));
@@ -275,61 +325,104 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) 
         cp_async_wait_upto(S - 2);   // step q complete: S - 2 later groups may be pending
         fence_async_smem();
         if (!__syncthreads_and(mine)) { ok = false; break; }
-        const int kb = q % nkb;
         if (tid == 0) {
             tc_fence_after();
             const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
             const uint32_t sx = st + kA * kWBytes;
+            const uint32_t acc = tmem + (uint32_t)(cc.lt * kSetCols);
+            const bool fresh = q == 0 || cc.kb == 0;
 #pragma unroll
             for (int kk = 0; kk < KS / 16; ++kk) {
                 const uint32_t ka = (uint32_t)(kk >> 2), kin = (uint32_t)((kk & 3) * 32);
                 const uint64_t bd = umma_desc(sx + ka * kXAtom + kin, 16, 1024);
-                umma(tmem, umma_desc(st + ka * kTileBytes + kin, 16, 1024), bd, idesc, kb > 0 || kk > 0);
+                umma(acc, umma_desc(st + ka * kTileBytes + kin, 16, 1024), bd, idesc, !(fresh && kk == 0));
                 if (GLU)
-                    umma(tmem + NP, umma_desc(st + kWBytes + ka * kTileBytes + kin, 16, 1024), bd, idesc,
-                         kb > 0 || kk > 0);
+                    umma(acc + NP, umma_desc(st + kWBytes + ka * kTileBytes + kin, 16, 1024), bd, idesc,
+                         !(fresh && kk == 0));
             }
             umma_commit(&bars[q % S]);
         }
-        if (kb == nkb - 1) {
-            // epilogue of tile q / nkb: its MMAs are the ones just committed
-            if (!__syncthreads_and(stage_wait(&bars[q % S], (uint32_t)((q / S) & 1)))) { ok = false; break; }
-            tc_fence_after();
-            if (warp < 4) {
-                const int r = warp * 32 + lane;
-                const int tile = c + (q / nkb) * G;
-                const int p = tile * kTileM + r;
-                const bool live = p < n;
-                const float bias = (live && a.bias) ? a.bias[s_idx[(q / nkb) * kTileM + r]] : 0.f;
-                const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-                float g[NP], u[NP];
+        step(cc);
+    }
+    if (ok && Q > 0) ok = __syncthreads_and(stage_wait(&bars[(Q - 1) % S], (uint32_t)(((Q - 1) / S) & 1)));
+    tc_fence_after();
+
+    // segments: a whole tile -> activation now; a part -> piece slot (c, sg)
+    const int r = warp * 32 + lane;  // TMEM lane = tile row (warps 0..3)
+    for (int sg = 0; sg < nseg && ok; ++sg) {
+        const int t = t_first + sg;
+        const bool whole = (sg > 0 || kb_first == 0) && (sg < nseg - 1 || kb_end == NKB);
+        if (warp < 4) {
+            float g[NP], u[NP];
+            const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(sg * kSetCols);
 #pragma unroll
-                for (int c0 = 0; c0 < NP; c0 += 8) {
-                    float v[8];
-                    tmem_ld8(lane_addr + (uint32_t)c0, v);
+            for (int c0 = 0; c0 < NP; c0 += 8) {
+                float v[8];
+                tmem_ld8(lane_addr + (uint32_t)c0, v);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) g[c0 + e] = v[e];
-                    if (GLU) {
-                        tmem_ld8(lane_addr + (uint32_t)(NP + c0), v);
+                for (int e = 0; e < 8; ++e) g[c0 + e] = v[e];
+                if (GLU) {
+                    tmem_ld8(lane_addr + (uint32_t)(NP + c0), v);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) u[c0 + e] = v[e];
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < NP / 2; ++b) {
-                    if (b < a.B) {
-                        float act = fmaxf(g[2 * b] + g[2 * b + 1] + bias, 0.f);
-                        if (GLU) act *= u[2 * b] + u[2 * b + 1];
-                        act = live ? act : 0.f;
-                        const uint16_t hi = Tc<T>::bits(act);
-                        const uint16_t lo = Tc<T>::bits(act - Tc<T>::val(hi));
-                        a.as[(size_t)(2 * b) * a.kp + p] = hi;
-                        a.as[(size_t)(2 * b + 1) * a.kp + p] = lo;
-                    }
+                    for (int e = 0; e < 8; ++e) u[c0 + e] = v[e];
                 }
             }
-            tc_fence_before();
-            __syncthreads();  // accumulators read before the next tile's first MMA
+            const int p = t * kTileM + r;
+            if (whole) {
+                const float bias = (p < n && a.bias) ? a.bias[s_idx[sg * kTileM + r]] : 0.f;
+                gate_act_out<T, GLU, NP>(a, g, u, bias, p < n, p);
+            } else {
+                float *piece = a.pieces + ((size_t)(c * kGateSegMax + sg) * kTileM + r) * kSetCols;
+#pragma unroll
+                for (int e = 0; e < NP; ++e) piece[e] = g[e];
+                if (GLU) {
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) piece[NP + e] = u[e];
+                }
+            }
+        }
+    }
+    __syncthreads();  // pieces written
+    if (tid == 0) {
+        for (int sg = 0; sg < kGateSegMax; ++sg) s_last[sg] = 0;
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+            const bool whole = (sg > 0 || kb_first == 0) && (sg < nseg - 1 || kb_end == NKB);
+            if (whole) continue;
+            const int t = t_first + sg;
+            const int c_lo = sk_owner((long long)t * NKB, U, P), c_hi = sk_owner((long long)(t + 1) * NKB - 1, U, P);
+            int pieces = 0;
+            for (int cc2 = c_lo; cc2 <= c_hi; ++cc2) pieces += sk_start(cc2 + 1, U, P) > sk_start(cc2, U, P);
+            __threadfence();
+            const unsigned old = atomicAdd(a.tile_count + t, 1u);
+            s_last[sg] = old == (unsigned)(pieces - 1);
+        }
+    }
+    __syncthreads();
+    for (int sg = 0; sg < nseg && ok; ++sg) {
+        if (!s_last[sg]) continue;
+        // the last piece of tile t arrived: add all pieces in CTA order
+        __threadfence();
+        const int t = t_first + sg;
+        if (warp < 4) {
+            float g[NP], u[NP];
+#pragma unroll
+            for (int e = 0; e < NP; ++e) { g[e] = 0.f; u[e] = 0.f; }
+            const int c_lo = sk_owner((long long)t * NKB, U, P), c_hi = sk_owner((long long)(t + 1) * NKB - 1, U, P);
+            for (int cc2 = c_lo; cc2 <= c_hi; ++cc2) {
+                const long long st2 = sk_start(cc2, U, P);
+                if (sk_start(cc2 + 1, U, P) == st2) continue;
+                const int sg2 = t - (int)(st2 / NKB);
+                const float *piece = a.pieces + ((size_t)(cc2 * kGateSegMax + sg2) * kTileM + r) * kSetCols;
+#pragma unroll
+                for (int e = 0; e < NP; ++e) g[e] += __ldcg(piece + e);
+                if (GLU) {
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) u[e] += __ldcg(piece + NP + e);
+                }
+            }
+            const int p = t * kTileM + r;
+            const float bias = (p < n && a.bias) ? a.bias[s_idx[sg * kTileM + r]] : 0.f;
+            gate_act_out<T, GLU, NP>(a, g, u, bias, p < n, p);
         }
     }
     if (!ok && tid == 0) atomicOr(a.err, CS_DEVERR_TIMEOUT);
@@ -572,6 +665,12 @@ cudaError_t run_tc(const FfnArgs &f, cudaStream_t s) {
     a.count = f.count;
     a.xs = static_cast<uint16_t *>(f.tc_x);
     a.as = static_cast<uint16_t *>(f.tc_a);
+    {
+        // the gate GEMM's piece slots and tile counters follow AS in the workspace
+        char *after_as = static_cast<char *>(f.tc_a) + tc_a_bytes(f.f, f.B);
+        a.pieces = reinterpret_cast<float *>(after_as);
+        a.tile_count = reinterpret_cast<unsigned *>(after_as + tc_pieces_bytes(f.B, f.G));
+    }
     a.part = f.part;
     a.err = f.err;
     a.d = f.d;
@@ -587,11 +686,12 @@ cudaError_t run_tc(const FfnArgs &f, cudaStream_t s) {
     // 1. X -> [hi; lo]
     a.stages = 0;
     cudaError_t e = launch(tc_split_kernel<T>, dim3(std::min(sms, (NP * a.dk + 255) / 256)), dim3(256), 0, s,
-                           pdl_enabled(), a, NP);
+                           pdl_enabled(), a, NP, 2 * sms);
     if (e != cudaSuccess) return e;
 
-    // 2. gate (and up) GEMM + activation, persistent over 128-neuron tiles;
-    //    128 K-elements (256 bytes of each row) per stage where four stages fit
+    // 2. gate (and up) GEMM + activation, stream-K over (128-neuron tile,
+    //    k-block) units; 128 K-elements (256 bytes of each row) per stage where
+    //    four stages fit
     {
         const bool ks128 = !glu && a.dk % 128 == 0;
         const int stage = ks128 ? 2 * (kTileBytes + NP * 128) : (glu ? 2 : 1) * kTileBytes + NP * 128;
@@ -601,8 +701,7 @@ cudaError_t run_tc(const FfnArgs &f, cudaStream_t s) {
                         : (glu ? tc_gate_kernel<T, true, NP, 64> : tc_gate_kernel<T, false, NP, 64>);
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        const int tiles_max = (f.f + kTileM - 1) / kTileM;
-        e = launch(fn, dim3(std::min(sms, tiles_max)), dim3(kTcThreads), smem, s, pdl_enabled(), a);
+        e = launch(fn, dim3(sms), dim3(kTcThreads), smem, s, pdl_enabled(), a);
         if (e != cudaSuccess) return e;
     }
     // 3. down GEMM, stream-K over (256-row column group, 64-neuron k-block)
@@ -638,19 +737,26 @@ int tc_act_pitch(int f) { return (f + kTileM - 1) / kTileM * kTileM; }
 static int tc_np(int B) { return 2 * B <= 16 ? 16 : (2 * B <= 32 ? 32 : 64); }
 
 size_t tc_x_bytes(int d, int B) { return align256((size_t)tc_np(B) * d * 2); }
+size_t tc_a_bytes(int f, int B) { return align256((size_t)tc_np(B) * tc_act_pitch(f) * 2); }
+// [P, 3 segments, 128 rows, 2 NP] fp32 (gate and up halves)
+size_t tc_pieces_bytes(int B, int P) { return align256((size_t)P * kGateSegMax * kTileM * 2 * tc_np(B) * 4); }
 
 size_t tc_workspace_bytes(int d, int f, int B) {
     if (B < 2 || B > kTcMaxB) return 0;
-    return tc_x_bytes(d, B) + align256((size_t)tc_np(B) * tc_act_pitch(f) * 2);
+    int sms = device_sm_count();
+    sms = sms < 1 ? 1 : sms;
+    return tc_x_bytes(d, B) + tc_a_bytes(f, B) + tc_pieces_bytes(B, sms) + align256((size_t)2 * sms * 4);
 }
 
 bool tc_path_applies(const FfnArgs &f) {
     if (!f.tc_x || !f.tc_a || f.preact) return false;
     if (f.dtype == CS_F32 || f.B < tc_min_batch() || f.B > kTcMaxB) return false;
     if (f.d % kKB != 0 || (f.ld * 2) % 16 != 0) return false;
-    // stream-K partials (2 slots x 256 columns per CTA and token) fit the
-    // workspace's partial-sum region, and a CTA's range spans <= 2 column groups
+    // down GEMM: stream-K partials (2 slots x 256 columns per CTA and token)
+    // fit the workspace's partial-sum region, and a CTA's range spans <= 2
+    // column groups; gate GEMM: at most 2P tiles, so a range spans <= 3 tiles
     if (f.d < 512 || (f.d + 255) / 256 > f.G) return false;
+    if ((f.f + kTileM - 1) / kTileM > 2 * f.G) return false;
     return true;
 }
 

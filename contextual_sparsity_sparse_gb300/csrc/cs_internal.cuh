@@ -338,7 +338,9 @@ constexpr int kTcDefaultMinB = 4;   // batch from which the tensor-core path is 
 int tc_min_batch();                 // kTcDefaultMinB, or CS_TC_MIN_B from the environment
 int tc_act_pitch(int f);
 size_t tc_workspace_bytes(int d, int f, int B);
-size_t tc_x_bytes(int d, int B);   // the first of the two buffers
+size_t tc_x_bytes(int d, int B);   // the first buffer: split activations X
+size_t tc_a_bytes(int f, int B);   // the second: split activations A
+size_t tc_pieces_bytes(int B, int P);  // the third: partial tile sums of the gate GEMM
 bool tc_path_applies(const FfnArgs &a);
 cudaError_t launch_ffn_tc(const FfnArgs &a, cudaStream_t s);
 
