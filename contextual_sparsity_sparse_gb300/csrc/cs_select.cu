@@ -347,7 +347,9 @@ select_row_kernel(const float *__restrict__ scores, int f, int k, float tau,
 // that after it each CTA finds it locally: min / max, per-slice histogram
 // totals, the pivot bucket's members, and the (greater, tie) totals behind the
 // output offsets.  The one pull is the pivot slice's 512 bins from every CTA
-// (all loads in flight together).  Four cluster barriers in all; no shared
+// (all loads in flight together).  Three cluster barriers when the pivot
+// bucket is small (every CTA then derives all CTAs' totals from the exchanged
+// members and the pushed above-bucket counts), four otherwise; no shared
 // memory is touched remotely after the last one, so CTAs may leave at once.
 // ---------------------------------------------------------------------------
 constexpr int kCl = 8;
@@ -365,6 +367,8 @@ struct ClSmem {
     uint32_t cid[kCl][kCandSmall];
     uint32_t ccnt[kCl];
     uint32_t pgt[kCl], peq[kCl];            // (greater, tie) totals from each CTA
+    uint32_t pabove[kCl];                   // scores above the pivot bucket in each CTA
+    uint32_t wab[kClW];
     uint32_t lkey[kCandSmall], lid[kCandSmall];
     uint32_t rhist[256];                      // radix digits (crowded bucket)
     uint32_t akey[kCandSmall], aid[kCandSmall];
@@ -447,6 +451,7 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
     float pv = 0.f;
     bool pnan = false;
     int need = 0;
+    bool fast = false;   // the per-CTA totals come from the exchanged candidates (no 4th barrier)
     if (KIND == SEL_TOPK && kk > 0 && kk < f) {
         // 1. min / max of the finite scores, pushed to every CTA
         float lo = INFINITY, hi = -INFINITY;
@@ -472,9 +477,12 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
         const float off = -smin * scale;
         // 2. local histogram; warp w pushes this CTA's total of slice w
         //    (bins [w*512, w*512 + 512)) to every CTA
+        int bk[ET];  // each score's bucket, kept for the candidate pass
 #pragma unroll
-        for (int e = 0; e < ET; ++e)
-            if (e < ne) atomicAdd(&S.hist[bucket_fast(v[e], scale, off)], 1u);
+        for (int e = 0; e < ET; ++e) {
+            bk[e] = e < ne ? bucket_fast(v[e], scale, off) : -1;
+            if (e < ne) atomicAdd(&S.hist[bk[e]], 1u);
+        }
         __syncthreads();
         {
             constexpr int BPL = kClBins / 32;      // 16 bins per lane
@@ -536,11 +544,19 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
             // 4. the bucket's members, pushed to every CTA, ranked exactly
 #pragma unroll
             for (int e = 0; e < ET; ++e) {
-                if (e < ne && bucket_fast(v[e], scale, off) == B_) {
+                if (bk[e] == B_) {
                     const uint32_t p = atomicAdd(&S.nfill, 1u);
                     S.lkey[p] = score_key(v[e]);
                     S.lid[p] = (uint32_t)(beg + j0 + e);
                 }
+            }
+            // and this CTA's count of scores above the pivot bucket
+            {
+                uint32_t ab = 0;
+#pragma unroll
+                for (int e = 0; e < ET; ++e) ab += bk[e] > B_;
+                ab = (uint32_t)warp_isum((int)ab);
+                if (lane == 0) S.wab[warp] = ab;
             }
             __syncthreads();
             const uint32_t nmine = S.nfill;
@@ -549,7 +565,13 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
                 *cl.map_shared_rank(&S.ckey[rank][p], r) = S.lkey[p];
                 *cl.map_shared_rank(&S.cid[rank][p], r) = S.lid[p];
             }
-            if (tid < kCl) *cl.map_shared_rank(&S.ccnt[rank], tid) = nmine;
+            if (tid < kCl) {
+                uint32_t ab = 0;
+#pragma unroll
+                for (int w = 0; w < kClW; ++w) ab += S.wab[w];
+                *cl.map_shared_rank(&S.ccnt[rank], tid) = nmine;
+                *cl.map_shared_rank(&S.pabove[rank], tid) = ab;
+            }
             cl.sync();                                                    // (3)
             if (warp == 0) {
                 const uint32_t nr = lane < kCl ? S.ccnt[lane] : 0u;
@@ -585,6 +607,20 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
             __syncthreads();
             pkey = S.pivot;
             need = (int)S.need;
+            // every CTA's (greater, tie) totals: above the bucket, plus its
+            // members above / equal to the pivot (a higher bucket means a
+            // strictly larger score; equal scores share a bucket)
+            if (warp == 0 && lane < kCl) {
+                uint32_t gt = S.pabove[lane], eq = 0;
+                for (uint32_t p = 0; p < S.ccnt[lane]; ++p) {
+                    const uint32_t kv = S.ckey[lane][p];
+                    gt += kv > pkey;
+                    eq += kv == pkey;
+                }
+                S.pgt[lane] = gt;
+                S.peq[lane] = eq;
+            }
+            fast = true;   // (the next barrier publishes pgt / peq within the CTA)
         } else {
             // a crowded bucket: each CTA resolves it alone with a radix select
             // over the whole row's members of the bucket (read from global)
@@ -649,23 +685,28 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
             eq = false;
         }
     };
-    uint32_t cgt = 0, ceq = 0;
+    // the (greater, tie) flags of this thread's scores as bit masks (ET <= 32)
+    static_assert(ET <= 32, "flag masks");
+    uint32_t gmask = 0, emask = 0;
 #pragma unroll
     for (int e = 0; e < ET; ++e) {
         if (e < ne) {
             bool gt, eq;
             flags(v[e], gt, eq);
-            cgt += gt;
-            ceq += eq;
+            gmask |= (uint32_t)gt << e;
+            emask |= (uint32_t)eq << e;
         }
     }
+    const uint32_t cgt = __popc(gmask), ceq = __popc(emask);
     uint32_t tot;
-    const uint32_t ex = cta_excl_scan((cgt << 16) | ceq, S.usum, &tot);
-    if (tid < kCl) {
-        *cl.map_shared_rank(&S.pgt[rank], tid) = tot >> 16;
-        *cl.map_shared_rank(&S.peq[rank], tid) = tot & 0xffffu;
+    const uint32_t ex = cta_excl_scan((cgt << 16) | ceq, S.usum, &tot);  // also orders pgt / peq
+    if (!fast) {
+        if (tid < kCl) {
+            *cl.map_shared_rank(&S.pgt[rank], tid) = tot >> 16;
+            *cl.map_shared_rank(&S.peq[rank], tid) = tot & 0xffffu;
+        }
+        cl.sync();                                                        // (4)
     }
-    cl.sync();                                                            // (4)
     // offsets of this CTA: lanes r < kCl hold CTA r's totals (every warp alike)
     const uint32_t g_ = lane < kCl ? S.pgt[lane] : 0u, e_ = lane < kCl ? S.peq[lane] : 0u;
     uint32_t gi = g_, ei = e_;
@@ -677,18 +718,16 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
     const int gb = (int)__shfl_sync(kFull, gi - g_, rank), eb = (int)__shfl_sync(kFull, ei - e_, rank);
     int eq_run = eb + (int)(ex & 0xffffu);
     int pos = gb + (int)(ex >> 16) + min(eq_run, need);
-#pragma unroll
-    for (int e = 0; e < ET; ++e) {
-        if (e < ne) {
-            bool gt, eq;
-            flags(v[e], gt, eq);
-            const bool take = gt || (eq && eq_run < need);
-            eq_run += eq;
-            if (take) {
-                const int jl = j0 + e;
-                out[pos++] = beg + jl;
-                if (mask) atomicOr(&S.bits[jl >> 5], 1u << (jl & 31));
-            }
+    // ascending ids: greater scores always, ties while the quota lasts
+    for (uint32_t m = gmask | emask; m; m &= m - 1) {
+        const int e = __ffs(m) - 1;
+        const bool eq = (emask >> e) & 1u;
+        const bool take = ((gmask >> e) & 1u) || (eq && eq_run < need);
+        eq_run += eq;
+        if (take) {
+            const int jl = j0 + e;
+            out[pos++] = beg + jl;
+            if (mask) atomicOr(&S.bits[jl >> 5], 1u << (jl & 31));
         }
     }
     if (rank == 0 && warp == 0) {
