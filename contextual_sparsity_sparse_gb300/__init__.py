@@ -30,7 +30,7 @@ _TORCH_DT = {torch.float32: CS_F32, torch.float16: CS_F16, torch.bfloat16: CS_BF
 EXPORTS = ["cs_version", "cs_status_string", "cs_last_error", "cs_workspace_size",
            "cs_workspace_init", "cs_get_device_error", "cs_pack_transpose", "cs_predict",
            "cs_select", "cs_sparse_ffn", "cs_exact_ffn", "cs_union_mask", "cs_decode_stack",
-           "cs_stack_release", "cs_sparse_ffn_noalloc"]
+           "cs_stack_release", "cs_sparse_ffn_noalloc", "cs_decode_layer"]
 
 
 class CsError(RuntimeError):
@@ -87,10 +87,12 @@ def lib():
             L.cs_decode_stack.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), I, P, C.c_float,
                                           C.POINTER(_Sel), I, P, P, P, S, P, P]
             L.cs_sparse_ffn_noalloc.argtypes = [C.POINTER(_Layer), P, I, P, P, P, P]
+            L.cs_decode_layer.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), P, P, C.POINTER(_Sel),
+                                          P, S, P, P, P]
             for name in ("cs_workspace_init", "cs_get_device_error", "cs_pack_transpose",
                          "cs_predict", "cs_select", "cs_sparse_ffn", "cs_exact_ffn",
                          "cs_union_mask", "cs_decode_stack", "cs_stack_release",
-                         "cs_sparse_ffn_noalloc"):
+                         "cs_sparse_ffn_noalloc", "cs_decode_layer"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -233,6 +235,25 @@ def cs_decode_stack(layers, preds, x, resid_scale, params, mode, ws: Workspace, 
     _check(lib().cs_decode_stack(larr, parr, L, _ptr(x), float(resid_scale), C.byref(params),
                                  int(mode), _stream(s_main), sp, ws.ptr, ws.nbytes,
                                  _ptr(trace_count), _ptr(trace_idx)))
+
+
+def _io_ptr(t, n):
+    """x or y of cs_decode_layer: a CUDA tensor or a pinned CPU tensor, fp32,
+    contiguous, holding at least n values (the library itself refuses
+    pageable host memory)."""
+    if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() < n:
+        raise ValueError(f"expected a contiguous fp32 tensor of at least {n} values")
+    return t.data_ptr()
+
+
+def cs_decode_layer(layer: FfnLayer, pred, x, y, params, ws: Workspace, stream=None, idx=None,
+                    count=None):
+    """One token through one layer: y = FFN(x, select(P(x))) (see include/cs.h).
+    x and y may live on the GPU or in pinned host memory."""
+    d = layer.c.d
+    _check(lib().cs_decode_layer(C.byref(layer.c), C.byref(pred.c) if pred is not None else None,
+                                 _io_ptr(x, d), _io_ptr(y, d), C.byref(params), ws.ptr, ws.nbytes,
+                                 _stream(stream), _ptr(idx), _ptr(count)))
 
 
 def cs_stack_release():

@@ -66,6 +66,7 @@ WsLayout ws_layout(int d, int f, int r, int B, int num_sms) {
     L.st_idx = off;    off += align256(sizeof(int32_t) * 2 * (size_t)f);
     L.st_count = off;  off += 256;
     L.st_h = off;      off += align256(sizeof(float) * (size_t)r);
+    L.io_y = off;      off += align256(sizeof(float) * (size_t)L.dp);
     L.tc = off;        off += tc_workspace_bytes(d, f, B);
     L.total = off;
     return L;

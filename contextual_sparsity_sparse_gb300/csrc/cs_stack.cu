@@ -41,6 +41,8 @@ struct StackPlan {
     char *ws;
     WsLayout lay;
     int32_t *trace_count, *trace_idx;
+    bool layer_only = false;  // single-layer step: y = FFN(x), no residual
+    float *y = nullptr;       // its output
 };
 
 struct Bufs {
@@ -123,7 +125,9 @@ cudaError_t ffn_step(const StackPlan &p, const Bufs &b, int l, const float *xin,
     sel_out(p, b, l, &idx, &cnt);
     a.idx = idx; a.count = cnt;
     a.preact = preact;
-    a.y = xout; a.resid = xin; a.scale = p.scale;
+    a.y = xout;
+    a.resid = p.layer_only ? nullptr : xin;
+    a.scale = p.layer_only ? 1.f : p.scale;
     a.err = b.err; a.part = b.part; a.G = p.lay.G; a.dp = p.lay.dp;
     if (shared) a.ring_bytes = kSharedRing;
     return launch_ffn(a, s);
@@ -215,6 +219,14 @@ cudaError_t enqueue_stack(const StackPlan &p, cudaStream_t sm, cudaStream_t sp, 
     return cudaSuccess;
 }
 
+// Enqueue one layer's step for one token: y = FFN(x, select(P(x))).
+cudaError_t enqueue_layer(const StackPlan &p, cudaStream_t s) {
+    const Bufs b = bufs_of(p);
+    if (p.sel.mode == CS_SEL_EXACT) return exact_step(p, b, 0, p.x, p.y, s);
+    TRY(predict_select(p, b, 0, p.x, s));
+    return ffn_step(p, b, 0, p.x, p.y, nullptr, s);
+}
+
 struct CacheEntry {
     cudaGraphExec_t exec = nullptr;
     int device = -1;
@@ -238,6 +250,8 @@ std::string plan_key(const StackPlan &p, cudaStream_t sp, int dev) {
     put(&p.ws, sizeof p.ws);
     put(&p.trace_count, sizeof p.trace_count);
     put(&p.trace_idx, sizeof p.trace_idx);
+    put(&p.layer_only, sizeof p.layer_only);
+    put(&p.y, sizeof p.y);
     const bool same = sp == nullptr;
     put(&same, sizeof same);
     return k;
@@ -249,41 +263,24 @@ void clear_cache_locked() {
     g_cache.clear();
 }
 
-}  // namespace
-
-extern "C" {
-
-cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds, int L, float *x,
-                          float resid_scale, const cs_select_params *params, cs_stack_mode mode,
-                          cs_stream_t s_main, cs_stream_t s_pred, void *ws, size_t ws_bytes,
-                          int32_t *trace_count, int32_t *trace_idx) {
-    if (L < 1 || !layers || !params || !x || (reinterpret_cast<uintptr_t>(x) & 3u)) {
-        set_error("cs_decode_stack: L >= 1, layers, params and x are required");
-        return CS_ERR_INVALID;
-    }
-    if (params->mode != CS_SEL_TOPK && params->mode != CS_SEL_THRESHOLD && params->mode != CS_SEL_EXACT) {
-        set_error("cs_decode_stack: bad selection mode");
-        return CS_ERR_INVALID;
-    }
-    if (mode != CS_STACK_SEQUENTIAL && mode != CS_STACK_LOOKAHEAD) {
-        set_error("cs_decode_stack: bad stack mode");
-        return CS_ERR_INVALID;
-    }
-    const bool exact = params->mode == CS_SEL_EXACT;
-    if (!exact && !preds) {
-        set_error("cs_decode_stack: predictors are required unless the selection is exact");
-        return CS_ERR_INVALID;
-    }
+// Shape and layout checks shared by the stack and the single-layer step.
+cs_status check_models(const cs_ffn_layer *layers, const cs_predictor *preds, int L, bool exact,
+                       const char *who) {
     const int d = layers[0].d, f = layers[0].f, r = exact ? 1 : preds[0].r;
     const cs_dtype dt = layers[0].dtype;
+    if (d < 1 || f < 1 || (dt != CS_F32 && dt != CS_F16 && dt != CS_BF16)) {
+        set_error("%s: layer 0 has a bad shape or dtype", who);
+        return CS_ERR_INVALID;
+    }
     for (int l = 0; l < L; ++l) {
         const cs_ffn_layer &Ly = layers[l];
         const int ld = Ly.ld ? Ly.ld : Ly.d;
         const size_t es = dtype_size(Ly.dtype);
         if (Ly.d != d || Ly.f != f || Ly.dtype != dt || ld < d || (ld * es) % 16 ||
             !Ly.w_gate || !Ly.w_down_t || (reinterpret_cast<uintptr_t>(Ly.w_gate) & 15u) ||
-            (reinterpret_cast<uintptr_t>(Ly.w_down_t) & 15u) || (reinterpret_cast<uintptr_t>(Ly.w_up) & 15u)) {
-            set_error("cs_decode_stack: layer %d has a different shape or an invalid layout", l);
+            (reinterpret_cast<uintptr_t>(Ly.w_down_t) & 15u) || (reinterpret_cast<uintptr_t>(Ly.w_up) & 15u) ||
+            (reinterpret_cast<uintptr_t>(Ly.bias) & 3u)) {
+            set_error("%s: layer %d has a different shape or an invalid layout", who, l);
             return CS_ERR_INVALID;
         }
         if (!exact) {
@@ -294,19 +291,125 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
                 (ldd * ep) % 16 || (ldu * ep) % 16 || (reinterpret_cast<uintptr_t>(P.p_down) & 15u) ||
                 (reinterpret_cast<uintptr_t>(P.p_up) & 15u) || P.r > 8192 ||
                 (P.dtype != CS_F32 && P.dtype != CS_F16 && P.dtype != CS_BF16)) {
-                set_error("cs_decode_stack: predictor %d does not match the layers or is invalid", l);
+                set_error("%s: predictor %d does not match the layers or is invalid", who, l);
                 return CS_ERR_INVALID;
             }
         }
     }
     if (d > ffn_max_d(dt) || f > kSelectMaxF) {
-        set_error("cs_decode_stack: d=%d or f=%d beyond the supported maximum", d, f);
+        set_error("%s: d=%d or f=%d beyond the supported maximum", who, d, f);
         return CS_ERR_UNSUPPORTED;
     }
+    return CS_OK;
+}
+
+cs_status check_params(const cs_select_params *params, const char *who) {
+    if (!params) {
+        set_error("%s: params is null", who);
+        return CS_ERR_INVALID;
+    }
+    if (params->mode != CS_SEL_TOPK && params->mode != CS_SEL_THRESHOLD && params->mode != CS_SEL_EXACT) {
+        set_error("%s: bad selection mode", who);
+        return CS_ERR_INVALID;
+    }
+    return CS_OK;
+}
+
+// Enqueue the plan directly when the caller is capturing (or on the legacy
+// stream), else replay its cached graph, capturing it on first use.
+template <typename Enq>
+cs_status run_cached(const StackPlan &p, cudaStream_t sm, cudaStream_t sp_key, const char *who, Enq enq) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (sm) {
+        cudaError_t e = cudaStreamIsCapturing(sm, &cap);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+    }
+    if (cap == cudaStreamCaptureStatusActive || !sm) {
+        cudaError_t e = enq();
+        return e == cudaSuccess ? CS_OK : cuda_fail(e, who);
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const std::string key = plan_key(p, sp_key, dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_cache.find(key);
+    if (it == g_cache.end()) {
+        if (g_cache.size() >= kMaxCached) clear_cache_locked();
+        cudaGraph_t graph = nullptr;
+        cudaError_t e = cudaStreamBeginCapture(sm, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+        const cudaError_t ee = enq();
+        e = cudaStreamEndCapture(sm, &graph);
+        if (ee != cudaSuccess) {
+            if (graph) cudaGraphDestroy(graph);
+            return cuda_fail(ee, who);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, who);
+        CacheEntry ce;
+        ce.device = dev;
+        e = cudaGraphInstantiate(&ce.exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+        it = g_cache.emplace(key, ce).first;
+    }
+    cudaError_t e = cudaGraphLaunch(it->second.exec, sm);
+    return e == cudaSuccess ? CS_OK : cuda_fail(e, who);
+}
+
+// Where a pointer given for x or y lives: device (or managed) memory is used
+// in place, page-locked host memory is staged through the workspace, and
+// pageable host memory is refused (its copies cannot be asynchronous).
+cs_status io_kind(const void *ptr, bool *host, const char *what) {
+    cudaPointerAttributes at = {};
+    cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        set_error("cs_decode_layer: %s: %s", what, cudaGetErrorString(e));
+        return CS_ERR_INVALID;
+    }
+    if (at.type == cudaMemoryTypeHost) {
+        *host = true;
+        return CS_OK;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+        *host = false;
+        return CS_OK;
+    }
+    set_error("cs_decode_layer: %s is pageable host memory; use device or page-locked host memory", what);
+    return CS_ERR_INVALID;
+}
+
+}  // namespace
+
+extern "C" {
+
+cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds, int L, float *x,
+                          float resid_scale, const cs_select_params *params, cs_stack_mode mode,
+                          cs_stream_t s_main, cs_stream_t s_pred, void *ws, size_t ws_bytes,
+                          int32_t *trace_count, int32_t *trace_idx) {
+    const char *who = "cs_decode_stack";
+    if (L < 1 || !layers || !params || !x || (reinterpret_cast<uintptr_t>(x) & 3u)) {
+        set_error("cs_decode_stack: L >= 1, layers, params and x are required");
+        return CS_ERR_INVALID;
+    }
+    cs_status st = check_params(params, who);
+    if (st != CS_OK) return st;
+    if (mode != CS_STACK_SEQUENTIAL && mode != CS_STACK_LOOKAHEAD) {
+        set_error("cs_decode_stack: bad stack mode");
+        return CS_ERR_INVALID;
+    }
+    const bool exact = params->mode == CS_SEL_EXACT;
+    if (!exact && !preds) {
+        set_error("cs_decode_stack: predictors are required unless the selection is exact");
+        return CS_ERR_INVALID;
+    }
+    st = check_models(layers, preds, L, exact, who);
+    if (st != CS_OK) return st;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) {
         set_error("cs_decode_stack: workspace is null or not 256-byte aligned");
         return CS_ERR_WORKSPACE;
     }
+    const int d = layers[0].d, f = layers[0].f, r = exact ? 1 : preds[0].r;
     StackPlan p;
     p.layers = layers; p.preds = preds; p.L = L; p.d = d; p.f = f; p.r = r;
     p.x = x; p.scale = resid_scale; p.sel = *params; p.mode = mode;
@@ -321,49 +424,72 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
     cudaStream_t sm = (cudaStream_t)s_main;
     cudaStream_t sp = (cudaStream_t)s_pred;
     const bool two = mode == CS_STACK_LOOKAHEAD && !exact && sp && sp != sm;
-
-    // Caller is capturing: enqueue into the caller's graph.
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (sm) {
-        cudaError_t e = cudaStreamIsCapturing(sm, &cap);
-        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(capture query)");
-    }
-    if (cap == cudaStreamCaptureStatusActive || !sm) {
+    return run_cached(p, sm, two ? sp : nullptr, who, [&]() {
         Events E;
-        cudaError_t e = enqueue_stack(p, sm, two ? sp : sm, E);
-        return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_decode_stack(enqueue)");
-    }
+        return enqueue_stack(p, sm, two ? sp : sm, E);
+    });
+}
 
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const std::string key = plan_key(p, two ? sp : nullptr, dev);
-    std::lock_guard<std::mutex> lock(g_mu);
-    auto it = g_cache.find(key);
-    if (it == g_cache.end()) {
-        if (g_cache.size() >= kMaxCached) clear_cache_locked();
-        cudaGraph_t graph = nullptr;
-        cudaError_t e = cudaStreamBeginCapture(sm, cudaStreamCaptureModeThreadLocal);
-        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(begin capture)");
-        cudaError_t ee;
-        {
-            Events E;
-            ee = enqueue_stack(p, sm, two ? sp : sm, E);
-            e = cudaStreamEndCapture(sm, &graph);
-        }
-        if (ee != cudaSuccess) {
-            if (graph) cudaGraphDestroy(graph);
-            return cuda_fail(ee, "cs_decode_stack(capture)");
-        }
-        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(end capture)");
-        CacheEntry ce;
-        ce.device = dev;
-        e = cudaGraphInstantiate(&ce.exec, graph, 0);
-        cudaGraphDestroy(graph);
-        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(instantiate)");
-        it = g_cache.emplace(key, ce).first;
+cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, const float *x, float *y,
+                          const cs_select_params *params, void *ws, size_t ws_bytes, cs_stream_t stream,
+                          int32_t *idx, int32_t *count) {
+    const char *who = "cs_decode_layer";
+    if (!layer || !params || !x || !y || (reinterpret_cast<uintptr_t>(x) & 3u) ||
+        (reinterpret_cast<uintptr_t>(y) & 3u) || (!idx) != (!count) || (reinterpret_cast<uintptr_t>(idx) & 3u) ||
+        (reinterpret_cast<uintptr_t>(count) & 3u)) {
+        set_error("cs_decode_layer: layer, params, x and y are required (4-byte aligned); idx and count "
+                  "are given together or not at all");
+        return CS_ERR_INVALID;
     }
-    cudaError_t e = cudaGraphLaunch(it->second.exec, sm);
-    return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_decode_stack(launch)");
+    cs_status st = check_params(params, who);
+    if (st != CS_OK) return st;
+    const bool exact = params->mode == CS_SEL_EXACT;
+    if (!exact && !pred) {
+        set_error("cs_decode_layer: a predictor is required unless the selection is exact");
+        return CS_ERR_INVALID;
+    }
+    st = check_models(layer, pred, 1, exact, who);
+    if (st != CS_OK) return st;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) {
+        set_error("cs_decode_layer: workspace is null or not 256-byte aligned");
+        return CS_ERR_WORKSPACE;
+    }
+    bool x_host = false, y_host = false;
+    st = io_kind(x, &x_host, "x");
+    if (st != CS_OK) return st;
+    st = io_kind(y, &y_host, "y");
+    if (st != CS_OK) return st;
+
+    const int d = layer->d, f = layer->f, r = exact ? 1 : pred->r;
+    StackPlan p;
+    p.layers = layer; p.preds = pred; p.L = 1; p.d = d; p.f = f; p.r = r;
+    p.scale = 1.f; p.sel = *params; p.mode = CS_STACK_SEQUENTIAL;
+    p.ws = static_cast<char *>(ws);
+    p.lay = ws_layout(d, f, r, 1, device_sm_count());
+    p.trace_count = count; p.trace_idx = idx;
+    p.layer_only = true;
+    if (ws_bytes < p.lay.total) {
+        set_error("cs_decode_layer: workspace too small: %zu bytes given, %zu needed", ws_bytes, p.lay.total);
+        return CS_ERR_WORKSPACE;
+    }
+    // host x and y go through the stack's ping-pong buffer and the y staging
+    // buffer, so the graph never names a host address
+    p.x = x_host ? reinterpret_cast<float *>(p.ws + p.lay.st_x) : const_cast<float *>(x);
+    p.y = y_host ? reinterpret_cast<float *>(p.ws + p.lay.io_y) : y;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t xy_bytes = sizeof(float) * (size_t)d;
+    if (x_host) {
+        cudaError_t e = cudaMemcpyAsync(p.x, x, xy_bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_layer(x copy)");
+    }
+    st = run_cached(p, s, nullptr, who, [&]() { return enqueue_layer(p, s); });
+    if (st != CS_OK) return st;
+    if (y_host) {
+        cudaError_t e = cudaMemcpyAsync(y, p.y, xy_bytes, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_layer(y copy)");
+    }
+    return CS_OK;
 }
 
 cs_status cs_stack_release(void) {

@@ -231,7 +231,33 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
                           cs_stream_t s_main, cs_stream_t s_pred, void *ws, size_t ws_bytes,
                           int32_t *trace_count, int32_t *trace_idx);
 
-/* Drops every cached stack graph (waits for nothing; call when idle). */
+/*
+ * One decode step of one layer for one token, [P2] "The Prediction Problem"
+ * (predictor, top-k, then the FFN over the chosen neurons only) and [P3]
+ * "Implementation sketch" (predict the active set, then run the FFN on it):
+ *     A = select(P(x)),  y = FFN(x, A)   (no residual).
+ *   params->mode == CS_SEL_EXACT: A = {j : g_j > 0} at x; pred may be NULL.
+ *   x: [d] fp32 input;  y: [d] fp32 output.  Each may be device memory or
+ *      page-locked host memory (cudaHostAlloc, cudaHostRegister, torch
+ *      pin_memory).  Host data is staged through the workspace with
+ *      asynchronous copies on `stream`, so a host y holds the result once the
+ *      stream has passed this call.  Pageable host memory is refused
+ *      (CS_ERR_INVALID) because its copies would not be asynchronous.
+ *   idx: [f] int32 device or NULL; count: int32 device scalar or NULL (both
+ *      or neither) -- the selected ids, ascending, and their number.
+ * The kernels are captured into a CUDA graph on the first call for a given
+ * set of arguments and replayed afterwards; the copies of host x and y run
+ * outside the graph, so host addresses may change from call to call without
+ * a new capture.  A stream that is already capturing, or the legacy stream
+ * (NULL), gets the kernels enqueued directly.  The workspace must hold
+ * cs_workspace_size(d, f, r, 1) bytes.  This call uses the same workspace
+ * regions as cs_decode_stack, so the two must not overlap on one workspace.
+ */
+cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, const float *x, float *y,
+                          const cs_select_params *params, void *ws, size_t ws_bytes, cs_stream_t stream,
+                          int32_t *idx, int32_t *count);
+
+/* Drops every cached stack and layer graph (waits for nothing; call when idle). */
 cs_status cs_stack_release(void);
 
 /*
