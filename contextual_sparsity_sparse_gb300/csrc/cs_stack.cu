@@ -13,6 +13,11 @@
 // Dependencies are CUDA events; the whole L-layer fork/join is captured once
 // into a CUDA graph (per distinct argument set) and replayed, so a decode step
 // costs one graph launch instead of ~4L kernel launches.
+//
+// The same machinery serves cs_decode_layer, one layer's step for one token
+// (predictor, selection, gathered FFN; y without the residual): its five
+// kernels become one cached graph, and x / y in page-locked host memory are
+// staged through the workspace by copies issued around the graph launch.
 #include <cstring>
 #include <mutex>
 #include <string>
