@@ -59,3 +59,31 @@ def test_validation_without_gpu(lib):
     sel = cs.select_params(cs.CS_SEL_TOPK, 1)
     assert lib.cs_decode_stack(None, None, 0, None, 0.1, C.byref(sel), 0, None, None, None, 0, None, None) == 1
     assert lib.cs_pack_transpose(None, 0, 1, 1, 1, None, 0, 1, None) == 1
+
+
+def test_decode_layer_validation_without_gpu(lib):
+    # every case below is refused on the host before the first CUDA call
+    sel = cs.select_params(cs.CS_SEL_TOPK, 1)
+    good = cs._Layer(128, 64, cs.CS_F16, 128, 256, 0, 256, 0)
+    pred = cs._Pred(128, 8, 64, cs.CS_F16, 0, 0, 256, 256)
+    x = y = 1024  # never dereferenced on these paths
+
+    def call(layer, p, params, idx=None, count=None, xx=x):
+        ref = lambda v: C.byref(v) if v is not None else None
+        return lib.cs_decode_layer(ref(layer), ref(p), xx, y, ref(params), 4096, 1 << 20, None, idx, count)
+
+    assert call(None, pred, sel) == 1
+    assert call(good, pred, sel, idx=4096, count=None) == 1
+    assert b"together" in lib.cs_last_error()
+    assert call(good, pred, sel, xx=1026) == 1          # x not 4-byte aligned
+    assert call(good, None, sel) == 1
+    assert b"predictor is required" in lib.cs_last_error()
+    bad_mode = cs._Sel(7, 1, 0.0)
+    assert call(good, pred, bad_mode) == 1
+    assert b"selection mode" in lib.cs_last_error()
+    bad_ld = cs._Layer(100, 64, cs.CS_F16, 100, 256, 0, 256, 0)   # 200-byte rows
+    assert call(bad_ld, pred, sel) == 1
+    assert b"layout" in lib.cs_last_error()
+    short_pred = cs._Pred(128, 8, 32, cs.CS_F16, 0, 0, 256, 256)  # f differs from the layer's
+    assert call(good, short_pred, sel) == 1
+    assert b"predictor 0" in lib.cs_last_error()
