@@ -72,13 +72,15 @@ def lib():
             L.orc_select_topk.restype = I
             L.orc_select_threshold.argtypes = [P, I, F, P]
             L.orc_select_threshold.restype = I
+            L.orc_select_hot.argtypes = [P, I, I, I, I, F, P]
+            L.orc_select_hot.restype = I
             L.orc_select_positive.argtypes = [P, I, P]
             L.orc_select_positive.restype = I
             L.orc_union.argtypes = [P, I, I, P, P]
             L.orc_union.restype = I
             L.orc_recall_precision.argtypes = [P, I, P, I, I, C.POINTER(D), C.POINTER(D)]
             L.orc_recall_precision.restype = None
-            L.orc_stack.argtypes = [I, C.POINTER(_Layer), C.POINTER(_Pred), I, I, I, F, D, P,
+            L.orc_stack.argtypes = [I, C.POINTER(_Layer), C.POINTER(_Pred), I, I, I, F, I, D, P,
                                     P, P, P]
             L.orc_stack.restype = I
             L.orc_decode.argtypes = [P, I, LG]
@@ -194,6 +196,30 @@ def select_positive(pre32):
     return out[:n].copy()
 
 
+def select_hot(tail_scores32, hot, mode=SEL_TOPK, k=0, tau=0.0):
+    """Hot-prefix selection: 0 .. hot-1, then hot + the tail's own top-k (or
+    threshold) selection over the tail's fp32 scores."""
+    s = _c(tail_scores32, np.float32)
+    out = np.empty(max(int(hot) + s.size, 1), np.int32)
+    n = lib().orc_select_hot(_ptr(s), int(s.size), int(hot), 0 if mode == SEL_TOPK else 1, int(k),
+                             float(np.float32(tau)), _ptr(out))
+    if n < 0:
+        raise ValueError(f"orc_select_hot failed ({n})")
+    return out[:n].copy()
+
+
+def hot_order(freq):
+    """The frequency-sorted layout's neuron order: most frequent first, equal
+    frequencies by lower id (a stable sort on the negated frequencies)."""
+    f = np.asarray(freq, np.float64)
+    return np.argsort(-f, kind="stable").astype(np.int32)
+
+
+def permute_rows(arr, perm):
+    """Rows of a storage array in the order perm: out[i] = arr[perm[i]]."""
+    return np.ascontiguousarray(np.asarray(arr)[np.asarray(perm, np.int64)])
+
+
 def union(masks, f):
     m = _c(masks, np.uint32)
     B = m.shape[0]
@@ -214,7 +240,7 @@ def recall_precision(pred_idx, exact_idx, f):
 
 
 def stack(layers, preds, x, *, mode=SEQUENTIAL, sel_mode=SEL_TOPK, k=0, tau=0.0,
-          resid_scale=0.1, trace=False):
+          resid_scale=0.1, trace=False, hot=0):
     """Run an L-layer stack.  Returns x_L (fp64) and, with trace=True, a dict
     of per-layer counts, index lists and fp32 scores."""
     L = len(layers)
@@ -225,7 +251,7 @@ def stack(layers, preds, x, *, mode=SEQUENTIAL, sel_mode=SEL_TOPK, k=0, tau=0.0,
     cnt = np.zeros(L, np.int32) if trace else None
     tidx = np.zeros((L, fmax), np.int32) if trace else None
     tsc = np.zeros((L, fmax), np.float32) if trace else None
-    rc = lib().orc_stack(L, larr, parr, int(mode), int(sel_mode), int(k), float(tau),
+    rc = lib().orc_stack(L, larr, parr, int(mode), int(sel_mode), int(k), float(tau), int(hot),
                          float(resid_scale), _ptr(x), _ptr(cnt), _ptr(tidx), _ptr(tsc))
     if rc != 0:
         raise ValueError(f"orc_stack failed ({rc})")

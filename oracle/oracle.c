@@ -271,6 +271,30 @@ int orc_select_positive(const float *pre, int f, int32_t *idx)
     return n;
 }
 
+/*
+ * Hot-prefix selection ([P2] "Kernel-Level Implementation": neurons sorted by
+ * how often they fire; [P1] "Static locality: hot and cold neurons": a few
+ * neurons fire for most inputs).  With the layout sorted hottest first, the
+ * first `hot` neurons are always taken and only the tail is predicted:
+ * s_tail holds the scores of neurons hot .. hot + f_tail - 1.  The result is
+ * 0 .. hot-1 followed by hot + (the tail's own selection: top-k or
+ * threshold), ascending.  Returns the count.
+ */
+int orc_select_hot(const float *s_tail, int f_tail, int hot, int mode, int k, float tau, int32_t *idx)
+{
+    if (hot < 0 || f_tail < 0)
+        return -1;
+    for (int j = 0; j < hot; j++)
+        idx[j] = j;
+    int n = mode == 0 ? orc_select_topk(s_tail, f_tail, k, idx + hot)
+                      : orc_select_threshold(s_tail, f_tail, tau, idx + hot);
+    if (n < 0)
+        return n;
+    for (int m = 0; m < n; m++)
+        idx[hot + m] += hot;
+    return hot + n;
+}
+
 /* --------------------------------------------------------------- batches */
 
 /*
@@ -339,11 +363,14 @@ enum { ORC_SEQUENTIAL = 0, ORC_LOOKAHEAD = 1 };
  *   exact:      layer l's set is {j : pre-activation > 0} at x_l (no
  *               predictor; mode is ignored).
  * Scores are rounded to fp32 before the selection decision.  x is updated in
- * place.  Optional traces: per-layer counts [L], index lists [L, f] and fp32
- * scores [L, f] (scores of the predictor that chose layer l's set).
+ * place.  hot > 0: the layout is sorted hottest first, neurons 0 .. hot-1
+ * are always taken and each predictor scores only the other f - hot neurons
+ * (orc_select_hot).  Optional traces: per-layer counts [L], index lists
+ * [L, f] and fp32 scores [L, f] (scores of the predictor that chose layer l's
+ * set: its first f - hot entries when hot > 0).
  */
 int orc_stack(int L, const orc_layer *layers, const orc_pred *preds, int mode, int sel_mode,
-              int k, float tau, double resid_scale, double *x,
+              int k, float tau, int hot, double resid_scale, double *x,
               int32_t *trace_count, int32_t *trace_idx, float *trace_scores)
 {
     if (L <= 0)
@@ -374,16 +401,22 @@ int orc_stack(int L, const orc_layer *layers, const orc_pred *preds, int mode, i
         } else {
             const orc_pred *P = &preds[l];
             const double *xin = (mode == ORC_LOOKAHEAD && l > 0) ? xprev : x;
+            /* the predictor scores the tail only: P->f == Ly->f - hot */
+            if (hot < 0 || P->f != Ly->f - hot) {
+                rc = -1;
+                break;
+            }
             orc_predict(P->d, P->r, P->f, P->dtype, P->p_down, P->ld_down, P->p_up, P->ld_up,
                         xin, h, s);
-            for (int j = 0; j < Ly->f; j++)
+            for (int j = 0; j < P->f; j++)
                 s32[j] = (float)s[j];
-            n = sel_mode == ORC_SEL_TOPK ? orc_select_topk(s32, Ly->f, k, idx)
-                                         : orc_select_threshold(s32, Ly->f, tau, idx);
+            n = orc_select_hot(s32, P->f, hot, sel_mode == ORC_SEL_TOPK ? 0 : 1, k, tau, idx);
         }
         if (trace_count) trace_count[l] = n;
         if (trace_idx) memcpy(trace_idx + (size_t)l * fmax, idx, sizeof(int32_t) * (size_t)n);
-        if (trace_scores) memcpy(trace_scores + (size_t)l * fmax, s32, sizeof(float) * Ly->f);
+        if (trace_scores)
+            memcpy(trace_scores + (size_t)l * fmax, s32,
+                   sizeof(float) * (size_t)(sel_mode == ORC_SEL_EXACT ? Ly->f : preds[l].f));
         rc = orc_ffn(Ly, x, idx, n, y);
         memcpy(xprev, x, sizeof(double) * d);
         for (int i = 0; i < d; i++)

@@ -308,3 +308,95 @@ def test_exact_stack_equals_dense_composition(orc):
         want = want + 0.25 * (L.w_down_t.astype(np.float64).T
                               @ np.maximum(L.w_gate.astype(np.float64) @ want + L.bias, 0))
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+# -------------------------------------------------------- hot-prefix layout
+
+@pytest.mark.parametrize("seed", range(16))
+def test_hot_select_brute_force(orc, seed):
+    """Hot prefix: ids 0 .. H-1 always, then H + the tail's own selection,
+    checked against the brute-force ranking above."""
+    rng = np.random.default_rng(100 + seed)
+    ft = int(rng.integers(0, 50))
+    hot = [0, 1, 5, 32][seed % 4]
+    s = synth.score_vector(seed, max(ft, 1), ties=int(rng.integers(0, ft + 1)), specials=bool(seed % 2),
+                           quantize=0.5 if seed % 3 == 0 else None)[:ft]
+    for k in sorted({0, 1, ft // 2, ft, ft + 2}):
+        want = list(range(hot)) + [hot + j for j in brute_topk(s, k)]
+        assert orc.select_hot(s, hot, orc.SEL_TOPK, k=k).tolist() == want, (ft, hot, k)
+    for tau in (-np.inf, 0.0, 0.5, np.nan):
+        want = list(range(hot)) + [hot + j for j in range(ft) if s[j] >= np.float32(tau)]
+        assert orc.select_hot(s, hot, orc.SEL_THRESHOLD, tau=tau).tolist() == want
+
+
+def test_hot_order_sorts_by_frequency_then_id(orc):
+    rng = np.random.default_rng(7)
+    freq = rng.integers(0, 6, size=300).astype(np.float64) / 5   # many equal frequencies
+    o = orc.hot_order(freq)
+    assert sorted(o.tolist()) == list(range(300))
+    for a, b in zip(o[:-1], o[1:]):   # adjacent pairs: strictly hotter, or equal and lower id
+        assert freq[a] > freq[b] or (freq[a] == freq[b] and a < b)
+    # the synthetic Zipf profile: its hottest neurons are the low ranks
+    p = synth.firing_probs(0, 0, 2048, 0.10)
+    o = orc.hot_order(p)
+    assert np.all(np.diff(p[o]) <= 0) and p[o[0]] == p.max()
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.F16])
+def test_hot_layout_leaves_the_ffn_unchanged(orc, dtype):
+    """Reordering neurons (rows of W_gate, W_down^T and the bias together) and
+    renaming the chosen set with them changes nothing but the summation
+    order: dense and sparse FFN agree to fp64 rounding."""
+    d, f = 24, 96
+    sd = 1 / math.sqrt(d)
+    wg = synth.normal_matrix_np(3, 1, f, d, sd, dtype)
+    wd = synth.normal_matrix_np(3, 2, f, d, sd, dtype)
+    b = synth.zipf_bias(3, 0, f, 0.1)
+    x = synth.x_normal(5, 1, d)[0]
+    perm = orc.hot_order(synth.firing_probs(3, 0, f, 0.1))
+    L0 = orc.Layer(d, f, dtype, wg, wd, bias=b)
+    L1 = orc.Layer(d, f, dtype, orc.permute_rows(wg, perm), orc.permute_rows(wd, perm),
+                   bias=orc.permute_rows(b, perm))
+    np.testing.assert_allclose(orc.dense_ffn(L1, x), orc.dense_ffn(L0, x), rtol=1e-12, atol=1e-13)
+    inv = np.empty(f, np.int32)
+    inv[perm] = np.arange(f, dtype=np.int32)
+    A = np.array([3, 17, 40, 41, 77, 95], np.int32)
+    np.testing.assert_allclose(orc.ffn(L1, x, np.sort(inv[A])), orc.ffn(L0, x, A), rtol=1e-12, atol=1e-13)
+
+
+def small_hot_stack(orc, L, d, f, r, hot, dtype):
+    sd = 1 / math.sqrt(d)
+    layers, preds = [], []
+    for l in range(L):
+        mk = lambda w, rows, cols: synth.normal_matrix_np(0, synth.tensor_id(l, w), rows, cols, sd, dtype)
+        layers.append(orc.Layer(d, f, dtype, mk(synth.W_GATE, f, d), mk(synth.W_DOWN_T, f, d),
+                                bias=synth.zipf_bias(0, l, f, 0.1)))
+        preds.append(orc.Predictor(d, r, f - hot, dtype, mk(synth.P_DOWN, r, d), mk(synth.P_UP, f - hot, r)))
+    return layers, preds
+
+
+def numpy_stack(layers, x, c, sets):
+    x = x.astype(np.float64).copy()
+    for L, A in zip(layers, sets):
+        A = np.asarray(A, np.int64)
+        wg, wd = L.w_gate.astype(np.float64)[A], L.w_down_t.astype(np.float64)[A]
+        x = x + c * (wd.T @ np.maximum(wg @ x + L.bias[A], 0))
+    return x
+
+
+@pytest.mark.parametrize("mode", ["seq", "look"])
+def test_hot_stack_extremes(orc, mode):
+    """With no tail budget every layer takes exactly the prefix; with the whole
+    tail it takes every neuron.  Both are plain numpy compositions."""
+    Ls, d, f, r, hot = 3, 32, 128, 8, 32
+    layers, preds = small_hot_stack(orc, Ls, d, f, r, hot, synth.F32)
+    m = orc.SEQUENTIAL if mode == "seq" else orc.LOOKAHEAD
+    x = synth.x_normal(9, 1, d)[0]
+    got, tr = orc.stack(layers, preds, x, mode=m, k=0, hot=hot, resid_scale=0.3, trace=True)
+    assert all(i.tolist() == list(range(hot)) for i in tr["idx"])
+    np.testing.assert_allclose(got, numpy_stack(layers, x, 0.3, [range(hot)] * Ls), rtol=1e-12, atol=1e-12)
+    got, tr = orc.stack(layers, preds, x, mode=m, k=f - hot, hot=hot, resid_scale=0.3, trace=True)
+    assert all(i.tolist() == list(range(f)) for i in tr["idx"])
+    np.testing.assert_allclose(got, numpy_stack(layers, x, 0.3, [range(f)] * Ls), rtol=1e-12, atol=1e-12)
+    with pytest.raises(ValueError):   # a predictor must cover exactly the tail
+        orc.stack(layers, preds, x, mode=m, k=4, hot=hot + 32)
