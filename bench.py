@@ -40,6 +40,10 @@ WORKLOADS = {
     "opt13b-topk20": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.20),
     "opt13b-thr10": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="threshold", share=0.10),
     "tiny-relu-topk10": dict(d=512, f=2048, r=64, dt=0, glu=False, rho=0.10, mode="topk", share=0.10),
+    # frequency-sorted layout: the 1024 hottest neurons always on, top-k 5% of
+    # the other 19,456 predicted (10% active in all, as opt13b-topk10)
+    "opt13b-hot5-topk5": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.05,
+                              hot=1024),
     # layer stacks: one step = one token through every layer (cs_decode_stack)
     "opt30b-stack-seq": dict(d=7168, f=28672, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.10,
                              L=48, stack="seq"),
@@ -197,6 +201,19 @@ def build_copies(W, torch, cs, synthdev):
             t["w_up"] = torch.empty((f, d), dtype=tdt, device="cuda")
             synthdev.fill_normal(t["w_up"], 0, synth.tensor_id(l, synth.W_UP), sd)
         t["bias"] = torch.from_numpy(synth.zipf_bias(0, l, f, W["rho"])).cuda()
+        hot = W.get("hot", 0)
+        if hot:
+            # the frequency-sorted layout: rows hottest first (layer l's own
+            # firing profile), the predictor's up map for the tail only
+            perm = cs.cs_hot_order(synth.firing_probs(0, l, f, W["rho"])).cuda()
+            for name in ("w_gate", "w_down_t", "w_up", "bias"):
+                if name in t:
+                    dst = torch.empty_like(t[name])
+                    cs.cs_permute_rows(t[name], perm, dst)
+                    t[name] = dst
+            pu = torch.empty((f - hot, r), dtype=tdt, device="cuda")
+            cs.cs_permute_rows(t["p_up"], perm[hot:], pu)
+            t["p_up"] = pu
         layer = cs.FfnLayer(t["w_gate"], t["w_down_t"], w_up=t.get("w_up"), bias=t["bias"])
         pred = cs.Predictor(t["p_down"], t["p_up"])
         copies.append((layer, pred, t))
@@ -208,11 +225,12 @@ def step_bytes(W, k):
     """Algorithmic bytes of one step (S8(d)-style accounting): predictor weights,
     scores written and read, selected rows (+ index and bias), x and y."""
     d, f, r = W["d"], W["f"], W["r"]
+    hot = W.get("hot", 0)   # always-on prefix: not predicted, always gathered
     e = 4 if W["dt"] == 0 else 2
     m = 3 if W["glu"] else 2
-    pred = e * (r * d + f * r) + 4 * (d + r) * 2
-    sel = 4 * f + 4 * k
-    ffn = k * (m * d * e + 4 + 4) + 4 * d * 2
+    pred = e * (r * d + (f - hot) * r) + 4 * (d + r) * 2
+    sel = 4 * (f - hot) + 4 * (hot + k)
+    ffn = (hot + k) * (m * d * e + 4 + 4) + 4 * d * 2
     return pred + sel + ffn, ffn
 
 
@@ -233,12 +251,13 @@ def run_ours(args, W, rank, world):
     X = torch.from_numpy(synth.x_normal(1000 + rank, NX, d)).cuda()
     s = torch.cuda.Stream()
     ws = cs.Workspace(d, f, r, stream=s)
-    scores = torch.empty((1, f), device="cuda")
+    hot = W.get("hot", 0)
+    scores = torch.empty((1, f - hot), device="cuda")
     idx = torch.empty((1, f), dtype=torch.int32, device="cuda")
     cnt = torch.empty(1, dtype=torch.int32, device="cuda")
     Y = torch.empty((NX, d), device="cuda")
     if W["mode"] == "topk":
-        params = cs.select_params(cs.CS_SEL_TOPK, k)
+        params = cs.select_params(cs.CS_SEL_TOPK, k, hot=hot)
     else:
         # threshold at the (1 - share) quantile of calibration scores (seed 1)
         layer0, pred0, _ = copies[0]
@@ -368,9 +387,11 @@ def run_ours(args, W, rank, world):
         "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "d": d, "f": f, "r": r, "k": k if W["mode"] == "topk" else None,
+                   **({"hot": hot, "active": hot + k, "layout": "frequency-sorted (cs_hot_order + cs_permute_rows)"}
+                      if hot else {}),
                    "selection": W["mode"], "weights": {0: "f32", 1: "f16", 2: "bf16"}[W["dt"]],
                    "accumulate": "f32", "batch": 1, "global_batch": world, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {NCOPY} layer copies ({NCOPY * (2 * f * d + r * d + f * r) * (4 if W['dt'] == 0 else 2) / 1e9:.2f} GB) and {NX} inputs rotate; 7 other steps ({7 * total_b / 1e6:.0f} MB) run between uses of a copy",
+                   "l2": f"inputs larger than L2: {NCOPY} layer copies ({NCOPY * (2 * f * d + r * d + (f - hot) * r) * (4 if W['dt'] == 0 else 2) / 1e9:.2f} GB) and {NX} inputs rotate; 7 other steps ({7 * total_b / 1e6:.0f} MB) run between uses of a copy",
                    "step": "cs_predict + cs_select + cs_sparse_ffn, graph of 200 steps"},
         "clocks": clocks,
         "gpu_launches": 5 * K,
@@ -706,12 +727,20 @@ def time_oracle(W, budget_s, max_steps=None):
     oracle.build()
     L, P = oracle_step_inputs(W)
     k = synth.ceil_k(W["f"], W["share"])
+    hot = W.get("hot", 0)
+    if hot:   # the frequency-sorted layout, built by the oracle's own order
+        perm = oracle.hot_order(synth.firing_probs(0, 0, W["f"], W["rho"]))
+        pr = lambda a: oracle.permute_rows(a, perm) if a is not None else None
+        L = oracle.Layer(L.d, L.f, L.dtype, pr(L.w_gate), pr(L.w_down_t), w_up=pr(L.w_up), bias=pr(L.bias))
+        P = oracle.Predictor(P.d, P.r, P.f - hot, P.dtype, P.p_down, oracle.permute_rows(P.p_up, perm[hot:]))
     X = synth.x_normal(3000, 64, W["d"])
     n, t0 = 0, time.perf_counter()
     while True:
         _, s = oracle.predict(P, X[n % 64])
         s32 = s.astype(np.float32)
-        if W["mode"] == "topk":
+        if hot:
+            sel = oracle.select_hot(s32, hot, oracle.SEL_TOPK, k=k)
+        elif W["mode"] == "topk":
             sel = oracle.select_topk(s32, k)
         else:
             if n == 0:  # threshold at the (1 - share) quantile of the oracle's own scores

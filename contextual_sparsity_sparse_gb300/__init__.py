@@ -30,7 +30,8 @@ _TORCH_DT = {torch.float32: CS_F32, torch.float16: CS_F16, torch.bfloat16: CS_BF
 EXPORTS = ["cs_version", "cs_status_string", "cs_last_error", "cs_workspace_size",
            "cs_workspace_init", "cs_get_device_error", "cs_pack_transpose", "cs_predict",
            "cs_select", "cs_sparse_ffn", "cs_exact_ffn", "cs_union_mask", "cs_decode_stack",
-           "cs_stack_release", "cs_sparse_ffn_noalloc", "cs_decode_layer"]
+           "cs_stack_release", "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows",
+           "cs_hot_order"]
 
 
 class CsError(RuntimeError):
@@ -52,7 +53,7 @@ class _Layer(C.Structure):
 
 
 class _Sel(C.Structure):
-    _fields_ = [("mode", C.c_int), ("k", C.c_int), ("tau", C.c_float)]
+    _fields_ = [("mode", C.c_int), ("k", C.c_int), ("tau", C.c_float), ("hot", C.c_int)]
 
 
 def library_path() -> str:
@@ -89,10 +90,12 @@ def lib():
             L.cs_sparse_ffn_noalloc.argtypes = [C.POINTER(_Layer), P, I, P, P, P, P]
             L.cs_decode_layer.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), P, P, C.POINTER(_Sel),
                                           P, S, P, P, P]
+            L.cs_permute_rows.argtypes = [P, I, I, P, I, I, I, P, I, P]
+            L.cs_hot_order.argtypes = [P, I, P]
             for name in ("cs_workspace_init", "cs_get_device_error", "cs_pack_transpose",
                          "cs_predict", "cs_select", "cs_sparse_ffn", "cs_exact_ffn",
                          "cs_union_mask", "cs_decode_stack", "cs_stack_release",
-                         "cs_sparse_ffn_noalloc", "cs_decode_layer"):
+                         "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows", "cs_hot_order"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -147,8 +150,10 @@ class FfnLayer:
                         _ptr(bias))
 
 
-def select_params(mode, k=0, tau=0.0):
-    return _Sel(int(mode), int(k), float(tau))
+def select_params(mode, k=0, tau=0.0, hot=0):
+    """hot: an always-on prefix of neurons for a frequency-sorted layout (a
+    multiple of 32); k and tau then apply to the tail (see include/cs.h)."""
+    return _Sel(int(mode), int(k), float(tau), int(hot))
 
 
 class Workspace:
@@ -254,6 +259,32 @@ def cs_decode_layer(layer: FfnLayer, pred, x, y, params, ws: Workspace, stream=N
     _check(lib().cs_decode_layer(C.byref(layer.c), C.byref(pred.c) if pred is not None else None,
                                  _io_ptr(x, d), _io_ptr(y, d), C.byref(params), ws.ptr, ws.nbytes,
                                  _stream(stream), _ptr(idx), _ptr(count)))
+
+
+def cs_permute_rows(src, perm, dst, rows=None, cols=None, stream=None):
+    """dst[i, :cols] = src[perm[i], :cols] for i < rows (the frequency-sorted
+    layout step; src and dst are 2-D CUDA tensors of one dtype, or 1-D fp32
+    vectors such as the bias)."""
+    if src.dtype != dst.dtype:
+        raise ValueError("src and dst must have the same dtype")
+    s2 = src if src.dim() == 2 else src.view(-1, 1)
+    d2 = dst if dst.dim() == 2 else dst.view(-1, 1)
+    rows = d2.shape[0] if rows is None else int(rows)
+    cols = s2.shape[1] if cols is None else int(cols)
+    if perm.dtype != torch.int32 or perm.numel() < rows or s2.stride(1) != 1 or d2.stride(1) != 1:
+        raise ValueError("perm must be int32 with >= rows entries; rows must be contiguous")
+    _check(lib().cs_permute_rows(_ptr(s2), s2.shape[0], s2.stride(0), _ptr(perm), rows, cols, _dt(s2),
+                                 _ptr(d2), d2.stride(0), _stream(stream)))
+
+
+def cs_hot_order(freq):
+    """The frequency-sorted neuron order (host): most frequent first, ties by
+    lower id.  freq: a sequence or CPU array of f frequencies; returns an
+    int32 CPU tensor."""
+    fr = torch.as_tensor(freq, dtype=torch.float32).contiguous()
+    out = torch.empty(fr.numel(), dtype=torch.int32)
+    _check(lib().cs_hot_order(fr.data_ptr(), fr.numel(), out.data_ptr()))
+    return out
 
 
 def cs_stack_release():

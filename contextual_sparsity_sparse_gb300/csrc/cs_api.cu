@@ -242,6 +242,8 @@ cs_status cs_select(const float *scores, int B, int f, const cs_select_params *p
     CS_CHECK(B >= 1 && f >= 1, "cs_select: B and f must be >= 1");
     CS_CHECK(params->mode == CS_SEL_TOPK || params->mode == CS_SEL_THRESHOLD,
              "cs_select: mode must be CS_SEL_TOPK or CS_SEL_THRESHOLD (exact mode is cs_exact_ffn)");
+    CS_CHECK(params->hot >= 0 && params->hot % 32 == 0 && params->hot <= (1 << 30) - f,
+             "cs_select: hot must be a non-negative multiple of 32 (got %d)", params->hot);
     if (f > kSelectMaxF) {
         set_error("cs_select: f=%d exceeds the supported maximum %d", f, kSelectMaxF);
         return CS_ERR_UNSUPPORTED;
@@ -252,7 +254,8 @@ cs_status cs_select(const float *scores, int B, int f, const cs_select_params *p
     a.scores = scores; a.B = B; a.f = f;
     a.kind = params->mode == CS_SEL_TOPK ? SEL_TOPK : SEL_THRESHOLD;
     a.k = params->k; a.tau = params->tau;
-    a.idx = idx; a.ld_idx = f; a.count = count; a.mask = mask;
+    a.hot = params->hot;
+    a.idx = idx; a.ld_idx = params->hot + f; a.count = count; a.mask = mask;
     cudaError_t e = launch_select(a, (cudaStream_t)stream);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_select");
 }

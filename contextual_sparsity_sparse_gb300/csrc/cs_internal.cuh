@@ -299,10 +299,11 @@ struct SelectArgs {
     SelKind kind;
     int k;
     float tau;
-    int32_t *idx;   // [B, ld_idx]
+    int32_t *idx;   // [B, ld_idx], ld_idx >= hot + f
     int ld_idx;
     int32_t *count; // [B]
-    uint32_t *mask; // [B, words] or null
+    uint32_t *mask; // [B, ceil((hot + f) / 32)] or null
+    int hot = 0;    // ids 0 .. hot-1 always taken (a multiple of 32); the f scores are neurons hot ..
 };
 cudaError_t launch_select(const SelectArgs &a, cudaStream_t s);
 constexpr int kSelectMaxF = 49152;

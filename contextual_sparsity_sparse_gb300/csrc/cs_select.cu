@@ -126,7 +126,7 @@ template <int ET, int KIND>
 __global__ void __launch_bounds__(kRowThreads, 1)
 select_row_kernel(const float *__restrict__ scores, int f, int k, float tau,
                   int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
-                  uint32_t *__restrict__ mask) {
+                  uint32_t *__restrict__ mask, int hot) {
     __shared__ __align__(16) uint32_t hist[kBuckets];
     __shared__ uint32_t ckey[kCandSmall], cid[kCandSmall];
     __shared__ float wlo[32], whi[32];
@@ -137,8 +137,12 @@ select_row_kernel(const float *__restrict__ scores, int f, int k, float tau,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
     const float *s = scores + (size_t)b * f;
-    int32_t *out = idx + (size_t)b * ld_idx;
-    const int words = (f + 31) >> 5;
+    // a hot prefix of `hot` neurons (a multiple of 32) comes first: ids
+    // 0 .. hot-1, then hot + the tail's selection; the scores are the tail's
+    int32_t *const row = idx + (size_t)b * ld_idx;
+    int32_t *out = row + hot;
+    const int words = (f + 31) >> 5;                 // the tail's mask words
+    const int mwords = (hot + f + 31) >> 5;          // a mask row
     const int E = (f + kRowThreads - 1) / kRowThreads;
     const int j0 = tid * E;
     const int ne = max(0, min(E, f - j0));
@@ -326,15 +330,18 @@ select_row_kernel(const float *__restrict__ scores, int f, int k, float tau,
             eq_run += eq;
             if (take) {
                 const int j = j0 + e;
-                out[pos++] = j;
+                out[pos++] = hot + j;
                 if (mask) atomicOr(&bits[j >> 5], 1u << (j & 31));
             }
         }
     }
-    if (tid == kRowThreads - 1) count[b] = (int)(tot >> 16) + min((int)(tot & 0xffffu), need);
+    if (tid == kRowThreads - 1) count[b] = hot + (int)(tot >> 16) + min((int)(tot & 0xffffu), need);
+    for (int i = tid; i < hot; i += kRowThreads) row[i] = i;
     if (mask) {
+        uint32_t *mrow = mask + (size_t)b * mwords;
+        for (int w = tid; w < (hot >> 5); w += kRowThreads) mrow[w] = 0xffffffffu;
         __syncthreads();
-        for (int w = tid; w < words; w += kRowThreads) mask[(size_t)b * words + w] = bits[w];
+        for (int w = tid; w < words; w += kRowThreads) mrow[(hot >> 5) + w] = bits[w];
     }
 }
 
@@ -407,7 +414,7 @@ template <int ET, int KIND>
 __global__ void __launch_bounds__(kClT, 1)
 select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
                  int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
-                 uint32_t *__restrict__ mask) {
+                 uint32_t *__restrict__ mask, int hot) {
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
     __shared__ __align__(16) ClSmem S;
@@ -415,8 +422,10 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
     const int rank = (int)cl.block_rank();
     const int b = blockIdx.x / kCl;
     const float *s = scores + (size_t)b * f;
-    int32_t *out = idx + (size_t)b * ld_idx;
-    const int words = (f + 31) >> 5;
+    // hot prefix as in the row kernel: ids 0 .. hot-1 first (hot a multiple of 32)
+    int32_t *const row = idx + (size_t)b * ld_idx;
+    int32_t *out = row + hot;
+    const int mwords = (hot + f + 31) >> 5;
     const int SL = (((f + kCl - 1) / kCl) + 31) & ~31;
     const int beg = min(rank * SL, f), n_my = min(SL, f - beg);
     const int E = (SL + kClT - 1) / kClT;
@@ -726,18 +735,21 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
         eq_run += eq;
         if (take) {
             const int jl = j0 + e;
-            out[pos++] = beg + jl;
+            out[pos++] = hot + beg + jl;
             if (mask) atomicOr(&S.bits[jl >> 5], 1u << (jl & 31));
         }
     }
     if (rank == 0 && warp == 0) {
         const uint32_t gt_all = __shfl_sync(kFull, gi, kCl - 1), eq_all = __shfl_sync(kFull, ei, kCl - 1);
-        if (lane == 0) count[b] = (int)gt_all + min((int)eq_all, need);
+        if (lane == 0) count[b] = hot + (int)gt_all + min((int)eq_all, need);
     }
+    for (int i = rank * kClT + tid; i < hot; i += kCl * kClT) row[i] = i;
     if (mask) {
+        uint32_t *mrow = mask + (size_t)b * mwords;
+        for (int w = rank * kClT + tid; w < (hot >> 5); w += kCl * kClT) mrow[w] = 0xffffffffu;
         __syncthreads();
         const int nw = (n_my + 31) >> 5;
-        for (int w = tid; w < nw; w += kClT) mask[(size_t)b * words + (beg >> 5) + w] = S.bits[w];
+        for (int w = tid; w < nw; w += kClT) mrow[(hot >> 5) + (beg >> 5) + w] = S.bits[w];
     }
 }
 
@@ -762,7 +774,7 @@ cudaError_t run_select_cl(const SelectArgs &a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, select_cl_kernel<ET, KIND>, a.scores, a.f, a.k, a.tau, a.idx, a.ld_idx,
-                              a.count, a.mask);
+                              a.count, a.mask, a.hot);
 }
 
 template <int ET>
@@ -785,7 +797,7 @@ cudaError_t launch_select_cl(const SelectArgs &a, cudaStream_t s) {
 template <int ET, int KIND>
 cudaError_t run_select_row(const SelectArgs &a, cudaStream_t s) {
     return launch(select_row_kernel<ET, KIND>, dim3(a.B), dim3(kRowThreads), 0, s, pdl_enabled(), a.scores,
-                  a.f, a.k, a.tau, a.idx, a.ld_idx, a.count, a.mask);
+                  a.f, a.k, a.tau, a.idx, a.ld_idx, a.count, a.mask, a.hot);
 }
 
 template <int ET>

@@ -94,10 +94,11 @@ cudaError_t predict_select(const StackPlan &p, const Bufs &b, int l, const float
     a.small_smem = shared;
     cudaError_t e = launch_predict(a, s);
     if (e != cudaSuccess) return e;
+    // the predictor scores neurons hot .. f-1; the selection adds 0 .. hot-1
     SelectArgs sa;
-    sa.scores = b.scores; sa.B = 1; sa.f = p.f;
+    sa.scores = b.scores; sa.B = 1; sa.f = p.f - p.sel.hot;
     sa.kind = p.sel.mode == CS_SEL_TOPK ? SEL_TOPK : SEL_THRESHOLD;
-    sa.k = p.sel.k; sa.tau = p.sel.tau;
+    sa.k = p.sel.k; sa.tau = p.sel.tau; sa.hot = p.sel.hot;
     sel_out(p, b, l, &sa.idx, &sa.count);
     sa.ld_idx = p.f; sa.mask = nullptr;
     return launch_select(sa, s);
@@ -270,7 +271,7 @@ void clear_cache_locked() {
 
 // Shape and layout checks shared by the stack and the single-layer step.
 cs_status check_models(const cs_ffn_layer *layers, const cs_predictor *preds, int L, bool exact,
-                       const char *who) {
+                       int hot, const char *who) {
     const int d = layers[0].d, f = layers[0].f, r = exact ? 1 : preds[0].r;
     const cs_dtype dt = layers[0].dtype;
     if (d < 1 || f < 1 || (dt != CS_F32 && dt != CS_F16 && dt != CS_BF16)) {
@@ -292,11 +293,12 @@ cs_status check_models(const cs_ffn_layer *layers, const cs_predictor *preds, in
             const cs_predictor &P = preds[l];
             const int ldd = P.ld_down ? P.ld_down : P.d, ldu = P.ld_up ? P.ld_up : P.r;
             const size_t ep = dtype_size(P.dtype);
-            if (P.d != d || P.f != f || P.r != r || !P.p_down || !P.p_up || ldd < d || ldu < r ||
+            if (P.d != d || P.f != f - hot || P.r != r || !P.p_down || !P.p_up || ldd < d || ldu < r ||
                 (ldd * ep) % 16 || (ldu * ep) % 16 || (reinterpret_cast<uintptr_t>(P.p_down) & 15u) ||
                 (reinterpret_cast<uintptr_t>(P.p_up) & 15u) || P.r > 8192 ||
                 (P.dtype != CS_F32 && P.dtype != CS_F16 && P.dtype != CS_BF16)) {
-                set_error("%s: predictor %d does not match the layers or is invalid", who, l);
+                set_error("%s: predictor %d does not match the layers or is invalid (it must score the "
+                          "f - hot = %d tail neurons)", who, l, f - hot);
                 return CS_ERR_INVALID;
             }
         }
@@ -315,6 +317,10 @@ cs_status check_params(const cs_select_params *params, const char *who) {
     }
     if (params->mode != CS_SEL_TOPK && params->mode != CS_SEL_THRESHOLD && params->mode != CS_SEL_EXACT) {
         set_error("%s: bad selection mode", who);
+        return CS_ERR_INVALID;
+    }
+    if (params->hot < 0 || params->hot % 32 || (params->mode == CS_SEL_EXACT && params->hot)) {
+        set_error("%s: hot must be a non-negative multiple of 32, and 0 in exact mode", who);
         return CS_ERR_INVALID;
     }
     return CS_OK;
@@ -408,7 +414,7 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
         set_error("cs_decode_stack: predictors are required unless the selection is exact");
         return CS_ERR_INVALID;
     }
-    st = check_models(layers, preds, L, exact, who);
+    st = check_models(layers, preds, L, exact, params->hot, who);
     if (st != CS_OK) return st;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) {
         set_error("cs_decode_stack: workspace is null or not 256-byte aligned");
@@ -453,7 +459,7 @@ cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, c
         set_error("cs_decode_layer: a predictor is required unless the selection is exact");
         return CS_ERR_INVALID;
     }
-    st = check_models(layer, pred, 1, exact, who);
+    st = check_models(layer, pred, 1, exact, params->hot, who);
     if (st != CS_OK) return st;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) {
         set_error("cs_decode_layer: workspace is null or not 256-byte aligned");

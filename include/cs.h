@@ -104,11 +104,20 @@ typedef struct cs_ffn_layer {
     const float *bias;    /* [f] device fp32 or NULL              */
 } cs_ffn_layer;
 
-/* Selection: k for CS_SEL_TOPK (clamped to [0, f]); tau for CS_SEL_THRESHOLD. */
+/*
+ * Selection: k for CS_SEL_TOPK (clamped to [0, f]); tau for CS_SEL_THRESHOLD.
+ * hot: size of an always-on prefix for a frequency-sorted layout ([P2]
+ * "Kernel-Level Implementation", neurons pre-sorted by how often they fire;
+ * [P1] "Static locality: hot and cold neurons").  Neurons 0 .. hot-1 are
+ * always taken and only the tail is scored and selected (k and tau apply to
+ * the tail).  0 for a plain selection; otherwise a multiple of 32.  Not
+ * allowed with CS_SEL_EXACT.
+ */
 typedef struct cs_select_params {
     cs_sel_mode mode;
     int k;
     float tau;
+    int hot;
 } cs_select_params;
 
 /* ------------------------------------------------------------ utilities */
@@ -135,6 +144,28 @@ cs_status cs_workspace_init(void *ws, size_t ws_bytes, cs_stream_t stream);
 cs_status cs_get_device_error(void *ws, cs_stream_t stream, int clear, uint32_t *code_out);
 
 /*
+ * Layout step for a frequency-sorted layout ([P2] "Kernel-Level
+ * Implementation": neurons pre-sorted by firing frequency; [P1] "Static
+ * locality: hot and cold neurons"): dst[i, :] = src[perm[i], :] for
+ * i < rows, `cols` elements of `dtype` per row.  Apply the same perm to the
+ * rows of w_gate, w_up, w_down_t and the bias (cols = 1, fp32), and perm + H
+ * (rows = f - H) to p_up for a hot prefix of H neurons; y is unchanged up to
+ * summation order.  src [src_rows, ld_src] and dst [rows, ld_dst] are
+ * device memory and must not overlap; perm [rows] int32 device.  A perm
+ * entry outside [0, src_rows) gives a zero row.
+ */
+cs_status cs_permute_rows(const void *src, int src_rows, int ld_src, const int32_t *perm, int rows, int cols,
+                          cs_dtype dtype, void *dst, int ld_dst, cs_stream_t stream);
+
+/*
+ * The frequency-sorted order on the host: perm[i] = the neuron of rank i,
+ * most frequent first, equal frequencies by lower id (NaN counts as the
+ * lowest frequency).  freq [f] and perm [f] are host memory (may be NULL
+ * when f == 0); synchronous.
+ */
+cs_status cs_hot_order(const float *freq, int f, int32_t *perm);
+
+/*
  * Layout step: dst[c, r] = src[r, c] with dtype conversion (round to nearest
  * even).  Turns a user's W_down [d, f] into w_down_t [f, ld_dst].  src is
  * [rows, ld_src], dst is [cols, ld_dst]; both device.  Neuron-major rows
@@ -157,16 +188,17 @@ cs_status cs_predict(const cs_predictor *pred, const float *x, int B, float *sco
 
 /*
  * Selection per token row, [P2] "The Prediction Problem" (top-k) and [P3]
- * "Implementation sketch" (threshold).
- *   scores: [B, f] fp32 device.
- *   idx:    [B, f] int32 device (output): row b holds count[b] ascending ids.
- *   count:  [B] int32 device (output).
- *   mask:   [B, ceil(f/32)] uint32 device or NULL (output): bit j%32 of word
- *           j/32 set iff j selected.
+ * "Implementation sketch" (threshold).  With H = params->hot:
+ *   scores: [B, f] fp32 device -- the scores of neurons H .. H + f - 1.
+ *   idx:    [B, H + f] int32 device (output): row b holds count[b] ascending
+ *           ids, 0 .. H-1 first.
+ *   count:  [B] int32 device (output): H + the tail's count.
+ *   mask:   [B, ceil((H + f)/32)] uint32 device or NULL (output): bit j%32 of
+ *           word j/32 set iff neuron j is selected.
  * TOPK: the min(k, f) best scores; higher score first, equal scores by lower
  * id, -0 == +0, NaN below every number.  THRESHOLD: {j : s_j >= tau}, NaN
  * never passes.  mode CS_SEL_EXACT is not a score selection: use
- * cs_exact_ffn.  f <= 65536.
+ * cs_exact_ffn.  f <= 49152; H a non-negative multiple of 32.
  */
 cs_status cs_select(const float *scores, int B, int f, const cs_select_params *params,
                     int32_t *idx, int32_t *count, uint32_t *mask,

@@ -87,3 +87,37 @@ def test_decode_layer_validation_without_gpu(lib):
     short_pred = cs._Pred(128, 8, 32, cs.CS_F16, 0, 0, 256, 256)  # f differs from the layer's
     assert call(good, short_pred, sel) == 1
     assert b"predictor 0" in lib.cs_last_error()
+
+
+def test_hot_order_matches_the_oracle(lib):
+    """cs_hot_order runs on the host: most frequent first, ties by lower id,
+    NaN last, exactly as the oracle's stable sort."""
+    import numpy as np
+    import oracle
+    import synth
+    rng = np.random.default_rng(3)
+    for f in (0, 1, 37, 2048):
+        freq = (rng.integers(0, 9, size=f) / 8).astype(np.float32)
+        if f > 10:
+            freq[::7] = np.nan
+        got = cs.cs_hot_order(freq).numpy()
+        assert np.array_equal(got, oracle.hot_order(freq)), f
+    p = synth.firing_probs(0, 0, 20480, 0.10).astype(np.float32)
+    assert np.array_equal(cs.cs_hot_order(p).numpy(), oracle.hot_order(p))
+
+
+def test_select_hot_validation_without_gpu(lib):
+    fake = 4096  # never dereferenced: the call is refused first
+    for hot in (-32, 16, 33):
+        sel = cs.select_params(cs.CS_SEL_TOPK, 5, hot=hot)
+        assert lib.cs_select(fake, 1, 64, C.byref(sel), fake, fake, None, None, 0, None) == 1
+        assert b"hot" in lib.cs_last_error()
+    L = cs._Layer(128, 64, cs.CS_F16, 128, 256, 0, 256, 0)
+    P = cs._Pred(128, 8, 64, cs.CS_F16, 0, 0, 256, 256)   # scores all 64 neurons
+    sel = cs.select_params(cs.CS_SEL_TOPK, 5, hot=32)       # ... but only 32 are a tail
+    assert lib.cs_decode_layer(C.byref(L), C.byref(P), 1024, 1024, C.byref(sel), 4096, 1 << 20, None,
+                               None, None) == 1
+    assert b"tail" in lib.cs_last_error()
+    ex = cs.select_params(cs.CS_SEL_EXACT, hot=32)
+    assert lib.cs_decode_layer(C.byref(L), None, 1024, 1024, C.byref(ex), 4096, 1 << 20, None,
+                               None, None) == 1
