@@ -26,6 +26,7 @@ _lib = None
 F32, F16, BF16 = 0, 1, 2
 SEL_TOPK, SEL_THRESHOLD, SEL_EXACT = 0, 1, 2
 SEQUENTIAL, LOOKAHEAD = 0, 1
+ACT_RELU, ACT_SILU = 0, 1
 
 
 def build(force: bool = False) -> str:
@@ -44,7 +45,7 @@ def build(force: bool = False) -> str:
 class _Layer(C.Structure):
     _fields_ = [("d", C.c_int), ("f", C.c_int), ("dtype", C.c_int), ("ld", C.c_long),
                 ("w_gate", C.c_void_p), ("w_up", C.c_void_p), ("w_down_t", C.c_void_p),
-                ("bias", C.c_void_p)]
+                ("bias", C.c_void_p), ("act", C.c_int)]
 
 
 class _Pred(C.Structure):
@@ -74,6 +75,8 @@ def lib():
             L.orc_select_threshold.restype = I
             L.orc_select_hot.argtypes = [P, I, I, I, I, F, P]
             L.orc_select_hot.restype = I
+            L.orc_select_magnitude.argtypes = [P, I, I, F, P]
+            L.orc_select_magnitude.restype = I
             L.orc_select_positive.argtypes = [P, I, P]
             L.orc_select_positive.restype = I
             L.orc_union.argtypes = [P, I, I, P, P]
@@ -107,8 +110,9 @@ class Layer:
     """FFN layer in storage form.  Rows are neuron-major: w_gate, w_up and
     w_down_t are [f, ld]; row j of w_down_t is column j of W_down."""
 
-    def __init__(self, d, f, dtype, w_gate, w_down_t, w_up=None, bias=None, ld=None):
+    def __init__(self, d, f, dtype, w_gate, w_down_t, w_up=None, bias=None, ld=None, act=ACT_RELU):
         self.d, self.f, self.dtype = int(d), int(f), int(dtype)
+        self.act = int(act)
         self.ld = int(ld if ld is not None else d)
         self.w_gate = _c(w_gate)
         self.w_down_t = _c(w_down_t)
@@ -120,7 +124,7 @@ class Layer:
 
     def c(self):
         return _Layer(self.d, self.f, self.dtype, self.ld, _ptr(self.w_gate), _ptr(self.w_up),
-                      _ptr(self.w_down_t), _ptr(self.bias))
+                      _ptr(self.w_down_t), _ptr(self.bias), self.act)
 
 
 class Predictor:
@@ -218,6 +222,14 @@ def hot_order(freq):
 def permute_rows(arr, perm):
     """Rows of a storage array in the order perm: out[i] = arr[perm[i]]."""
     return np.ascontiguousarray(np.asarray(arr)[np.asarray(perm, np.int64)])
+
+
+def select_magnitude(pre32, act, tau):
+    """Functional sparsity: {j : |act(g_j)| > tau} from fp32 pre-activations."""
+    s = _c(pre32, np.float32)
+    out = np.empty(max(s.size, 1), np.int32)
+    n = lib().orc_select_magnitude(_ptr(s), int(s.size), int(act), float(np.float32(tau)), _ptr(out))
+    return out[:n].copy()
 
 
 def union(masks, f):

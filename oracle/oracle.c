@@ -107,7 +107,22 @@ typedef struct {
     const void *w_up;      /* [f, ld] or NULL (gate-only ReLU FFN)          */
     const void *w_down_t;  /* [f, ld] row j = column j of W_down            */
     const float *bias;     /* [f] or NULL                                    */
+    int act;               /* ORC_ACT_RELU or ORC_ACT_SILU                   */
 } orc_layer;
+
+enum { ORC_ACT_RELU = 0, ORC_ACT_SILU = 1 };
+
+/*
+ * The gate's activation: relu(g) = max(g, 0), or silu(g) = g / (1 + e^-g)
+ * ([P2] "The SiLU/GELU Challenge: TurboSparse": down(silu(gate x) * up x);
+ * [P2] "The Empirical Foundation": SiLU layers are only functionally sparse).
+ */
+static double gate_act(int act, double g)
+{
+    if (act == ORC_ACT_SILU)
+        return g / (1.0 + exp(-g));
+    return g > 0.0 ? g : 0.0;
+}
 
 /* Gate pre-activation g_j = w_gate_j . x + b_j. */
 static double preact_j(const orc_layer *L, const double *x, int j)
@@ -121,15 +136,16 @@ static double preact_j(const orc_layer *L, const double *x, int j)
 }
 
 /*
- * Neuron activation a_j = relu(w_gate_j . x + b_j) * (w_up_j . x if the layer
- * has an up projection, else 1).  ReLU gate-only FFN: [P2] "The Empirical
- * Foundation" (ReLU layers) and [P1] first section; ReLUfied SwiGLU:
- * [P2] "The SiLU/GELU Challenge: TurboSparse" (down(relu(gate x) * up x)).
+ * Neuron activation a_j = act(w_gate_j . x + b_j) * (w_up_j . x if the layer
+ * has an up projection, else 1), act = relu or silu.  ReLU gate-only FFN:
+ * [P2] "The Empirical Foundation" (ReLU layers) and [P1] first section;
+ * ReLUfied SwiGLU and SwiGLU: [P2] "The SiLU/GELU Challenge: TurboSparse"
+ * (down(act(gate x) * up x)).
  */
 static double act_j(const orc_layer *L, const double *x, int j)
 {
     double g = preact_j(L, x, j);
-    double a = g > 0.0 ? g : 0.0;
+    double a = gate_act(L->act, g);
     if (L->w_up) {
         double u = 0.0;
         for (int t = 0; t < L->d; t++)
@@ -295,6 +311,24 @@ int orc_select_hot(const float *s_tail, int f_tail, int hot, int mode, int k, fl
     return hot + n;
 }
 
+/*
+ * Magnitude selection for functional sparsity ([P2] "The Empirical
+ * Foundation": under SiLU, neurons whose outputs are non-zero but too small to
+ * matter): {j : |act(g_j)| > tau} from the fp32 gate pre-activations,
+ * ascending; the gate's activation is evaluated in fp64.  NaN never passes.
+ * With relu and tau = 0 this is the exact mask {j : g_j > 0}.
+ */
+int orc_select_magnitude(const float *pre, int f, int act, float tau, int32_t *idx)
+{
+    int n = 0;
+    for (int j = 0; j < f; j++) {
+        double a = fabs(gate_act(act, (double)pre[j]));
+        if (a > (double)tau)
+            idx[n++] = j;
+    }
+    return n;
+}
+
 /* --------------------------------------------------------------- batches */
 
 /*
@@ -360,8 +394,9 @@ enum { ORC_SEQUENTIAL = 0, ORC_LOOKAHEAD = 1 };
  *   look-ahead: layer l's set is selected from P_l(x_{l-1}) -- the predictor
  *               of the next layer reads the current layer's input -- and
  *               layer 0 from P_0(x_0).
- *   exact:      layer l's set is {j : pre-activation > 0} at x_l (no
- *               predictor; mode is ignored).
+ *   exact:      layer l's set is {j : |act(pre-activation)| > tau} at x_l
+ *               (no predictor; mode is ignored): {j : pre-activation > 0}
+ *               for relu at tau = 0.
  * Scores are rounded to fp32 before the selection decision.  x is updated in
  * place.  hot > 0: the layout is sorted hottest first, neurons 0 .. hot-1
  * are always taken and each predictor scores only the other f - hot neurons
@@ -397,7 +432,7 @@ int orc_stack(int L, const orc_layer *layers, const orc_pred *preds, int mode, i
         if (sel_mode == ORC_SEL_EXACT) {
             for (int j = 0; j < Ly->f; j++)
                 s32[j] = (float)preact_j(Ly, x, j);
-            n = orc_select_positive(s32, Ly->f, idx);
+            n = orc_select_magnitude(s32, Ly->f, Ly->act, tau, idx);
         } else {
             const orc_pred *P = &preds[l];
             const double *xin = (mode == ORC_LOOKAHEAD && l > 0) ? xprev : x;

@@ -400,3 +400,72 @@ def test_hot_stack_extremes(orc, mode):
     np.testing.assert_allclose(got, numpy_stack(layers, x, 0.3, [range(f)] * Ls), rtol=1e-12, atol=1e-12)
     with pytest.raises(ValueError):   # a predictor must cover exactly the tail
         orc.stack(layers, preds, x, mode=m, k=4, hot=hot + 32)
+
+
+# ------------------------------------------------------------- SiLU (next row 2)
+
+def silu_pair_layer(orc, d, npairs, glu, dtype, seed=0):
+    """Neurons in pairs whose contributions differ by the sign of silu(-g):
+    gated (w, u, v) and (-w, -u, v), gate-only (w, v) and (-w, -v).  Since
+    silu(g) - silu(-g) = g for every g, each pair adds exactly
+    g * (u . x or 1) * v."""
+    rng = np.random.default_rng(seed)
+    W = (rng.standard_normal((npairs, d)) / math.sqrt(d)).astype(np.float32)
+    U = (rng.standard_normal((npairs, d)) / math.sqrt(d)).astype(np.float32)
+    V = rng.standard_normal((npairs, d)).astype(np.float32)
+    wg = np.concatenate([W, -W]).astype(np.float32)
+    wu = np.concatenate([U, -U]).astype(np.float32)
+    wd = np.concatenate([V, V if glu else -V]).astype(np.float32)
+    L = orc.Layer(d, 2 * npairs, synth.F32, wg, wd, w_up=wu if glu else None, act=orc.ACT_SILU)
+    return L, W.astype(np.float64), U.astype(np.float64), V.astype(np.float64)
+
+
+@pytest.mark.parametrize("glu", [False, True])
+def test_silu_odd_part_closed_form(orc, glu):
+    d, npairs = 48, 40
+    L, W, U, V = silu_pair_layer(orc, d, npairs, glu, synth.F32)
+    x = synth.x_normal(8, 1, d)[0].astype(np.float64) * 3.0   # g spans the curved region and beyond
+    g = W @ x
+    coef = g * (U @ x) if glu else g
+    want = V.T @ coef
+    got = orc.dense_ffn(L, x)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
+def test_silu_limits_and_a_known_value(orc):
+    """silu(g) -> g far above 0 and -> 0 far below it; silu(0) = 0; and
+    silu(1) = e / (1 + e), the logistic function at 1 times 1."""
+    d, f = 16, 3
+    eye = np.zeros((f, d), np.float32)
+    for j in range(f):
+        eye[j, j] = 1.0
+    down = np.eye(f, d, dtype=np.float32)
+    x = np.zeros(d)
+    for bias, want in ((np.array([40.0, 60.0, 35.5], np.float32), [40.0, 60.0, 35.5]),
+                       (np.array([-40.0, -60.0, 0.0], np.float32), [0.0, 0.0, 0.0]),
+                       (np.array([1.0, 0.0, -1.0], np.float32),
+                        [math.e / (1 + math.e), 0.0, -1.0 / (1 + math.e)])):
+        L = orc.Layer(d, f, synth.F32, eye, down, bias=bias, act=orc.ACT_SILU)
+        y = orc.dense_ffn(L, x)[:f]
+        np.testing.assert_allclose(y, want, rtol=1e-14, atol=1e-15)
+        # ReLU is the SiLU limit on the positive side
+        if bias[0] > 0 and bias[2] > 0:
+            Lr = orc.Layer(d, f, synth.F32, eye, down, bias=bias)
+            np.testing.assert_allclose(orc.dense_ffn(Lr, x)[:f], y, rtol=1e-14)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_magnitude_selection_brute_force(orc, seed):
+    s = synth.score_vector(seed, 300, ties=20, specials=True, quantize=0.25 if seed % 2 else None) * 2
+    sig = lambda v: 1.0 / (1.0 + np.exp(-v))
+    with np.errstate(over="ignore", invalid="ignore"):
+        silu = np.where(np.isnan(s), np.nan, s.astype(np.float64) * sig(s.astype(np.float64)))
+    silu = np.where(np.isinf(s) & (s < 0), 0.0, silu)
+    relu = np.maximum(s.astype(np.float64), 0)
+    for tau in (0.0, 0.05, 0.2, 0.27, 1.0):
+        assert orc.select_magnitude(s, orc.ACT_SILU, tau).tolist() == \
+            [j for j in range(s.size) if abs(silu[j]) > tau], tau
+        assert orc.select_magnitude(s, orc.ACT_RELU, tau).tolist() == \
+            [j for j in range(s.size) if relu[j] > tau], tau
+    # relu at tau = 0 is the exact mask
+    assert orc.select_magnitude(s, orc.ACT_RELU, 0.0).tolist() == orc.select_positive(s).tolist()
