@@ -44,6 +44,9 @@ WORKLOADS = {
     # the other 19,456 predicted (10% active in all, as opt13b-topk10)
     "opt13b-hot5-topk5": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.05,
                               hot=1024),
+    # one LLaMA-70B-shaped SwiGLU layer with SiLU kept (functional sparsity), top-k 15%
+    "llama70b-silu-topk15": dict(d=8192, f=28672, r=1024, dt=2, glu=True, rho=0.15, mode="topk", share=0.15,
+                                 act=1),
     # layer stacks: one step = one token through every layer (cs_decode_stack)
     "opt30b-stack-seq": dict(d=7168, f=28672, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.10,
                              L=48, stack="seq"),
@@ -214,7 +217,7 @@ def build_copies(W, torch, cs, synthdev):
             pu = torch.empty((f - hot, r), dtype=tdt, device="cuda")
             cs.cs_permute_rows(t["p_up"], perm[hot:], pu)
             t["p_up"] = pu
-        layer = cs.FfnLayer(t["w_gate"], t["w_down_t"], w_up=t.get("w_up"), bias=t["bias"])
+        layer = cs.FfnLayer(t["w_gate"], t["w_down_t"], w_up=t.get("w_up"), bias=t["bias"], act=W.get("act", 0))
         pred = cs.Predictor(t["p_down"], t["p_up"])
         copies.append((layer, pred, t))
     torch.cuda.synchronize()
@@ -387,6 +390,7 @@ def run_ours(args, W, rank, world):
         "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "d": d, "f": f, "r": r, "k": k if W["mode"] == "topk" else None,
+                   "activation": "silu" if W.get("act", 0) else "relu", "gated": W["glu"],
                    **({"hot": hot, "active": hot + k, "layout": "frequency-sorted (cs_hot_order + cs_permute_rows)"}
                       if hot else {}),
                    "selection": W["mode"], "weights": {0: "f32", 1: "f16", 2: "bf16"}[W["dt"]],
@@ -529,7 +533,7 @@ def oracle_step_inputs(W, layer_index=0):
     mk = lambda which, rows, cols: synth.normal_matrix(0, synth.tensor_id(layer_index, which), rows, cols, sd, dt)
     L = oracle.Layer(d, f, dt, mk(synth.W_GATE, f, d), mk(synth.W_DOWN_T, f, d),
                      w_up=mk(synth.W_UP, f, d) if W["glu"] else None,
-                     bias=synth.zipf_bias(0, layer_index, f, W["rho"]))
+                     bias=synth.zipf_bias(0, layer_index, f, W["rho"]), act=W.get("act", 0))
     P = oracle.Predictor(d, r, f, dt, mk(synth.P_DOWN, r, d), mk(synth.P_UP, f, r))
     return L, P
 
@@ -731,7 +735,8 @@ def time_oracle(W, budget_s, max_steps=None):
     if hot:   # the frequency-sorted layout, built by the oracle's own order
         perm = oracle.hot_order(synth.firing_probs(0, 0, W["f"], W["rho"]))
         pr = lambda a: oracle.permute_rows(a, perm) if a is not None else None
-        L = oracle.Layer(L.d, L.f, L.dtype, pr(L.w_gate), pr(L.w_down_t), w_up=pr(L.w_up), bias=pr(L.bias))
+        L = oracle.Layer(L.d, L.f, L.dtype, pr(L.w_gate), pr(L.w_down_t), w_up=pr(L.w_up), bias=pr(L.bias),
+                         act=L.act)
         P = oracle.Predictor(P.d, P.r, P.f - hot, P.dtype, P.p_down, oracle.permute_rows(P.p_up, perm[hot:]))
     X = synth.x_normal(3000, 64, W["d"])
     n, t0 = 0, time.perf_counter()

@@ -22,6 +22,7 @@ _lib = None
 CS_F32, CS_F16, CS_BF16 = 0, 1, 2
 CS_SEL_TOPK, CS_SEL_THRESHOLD, CS_SEL_EXACT = 0, 1, 2
 CS_STACK_SEQUENTIAL, CS_STACK_LOOKAHEAD = 0, 1
+CS_ACT_RELU, CS_ACT_SILU = 0, 1
 CS_DEVERR_INDEX, CS_DEVERR_COUNT, CS_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
 _TORCH_DT = {torch.float32: CS_F32, torch.float16: CS_F16, torch.bfloat16: CS_BF16}
@@ -49,7 +50,7 @@ class _Pred(C.Structure):
 class _Layer(C.Structure):
     _fields_ = [("d", C.c_int), ("f", C.c_int), ("dtype", C.c_int), ("ld", C.c_int),
                 ("w_gate", C.c_void_p), ("w_up", C.c_void_p), ("w_down_t", C.c_void_p),
-                ("bias", C.c_void_p)]
+                ("bias", C.c_void_p), ("act", C.c_int)]
 
 
 class _Sel(C.Structure):
@@ -83,7 +84,7 @@ def lib():
             L.cs_predict.argtypes = [C.POINTER(_Pred), P, I, P, P, S, P]
             L.cs_select.argtypes = [P, I, I, C.POINTER(_Sel), P, P, P, P, S, P]
             L.cs_sparse_ffn.argtypes = [C.POINTER(_Layer), P, I, P, P, P, P, S, P]
-            L.cs_exact_ffn.argtypes = [C.POINTER(_Layer), P, P, P, P, P, P, P, S, P]
+            L.cs_exact_ffn.argtypes = [C.POINTER(_Layer), P, P, P, P, P, P, C.c_float, P, S, P]
             L.cs_union_mask.argtypes = [P, I, I, P, P, P, P, S, P]
             L.cs_decode_stack.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), I, P, C.c_float,
                                           C.POINTER(_Sel), I, P, P, P, S, P, P]
@@ -142,12 +143,13 @@ class FfnLayer:
     """Neuron-major layer: w_gate, w_up, w_down_t are [f, ld]; d is the used
     width (default ld).  w_up None gives the gate-only ReLU FFN."""
 
-    def __init__(self, w_gate, w_down_t, w_up=None, bias=None, d=None):
+    def __init__(self, w_gate, w_down_t, w_up=None, bias=None, d=None, act=CS_ACT_RELU):
         self.w_gate, self.w_down_t, self.w_up, self.bias = w_gate, w_down_t, w_up, bias
         self.f, ld = w_gate.shape
         self.d = int(d if d is not None else ld)
+        self.act = int(act)
         self.c = _Layer(self.d, self.f, _dt(w_gate), ld, _ptr(w_gate), _ptr(w_up), _ptr(w_down_t),
-                        _ptr(bias))
+                        _ptr(bias), self.act)
 
 
 def select_params(mode, k=0, tau=0.0, hot=0):
@@ -220,9 +222,11 @@ def cs_sparse_ffn_noalloc(layer: FfnLayer, x, idx, count, y, stream=None):
                                        _ptr(y), _stream(stream)))
 
 
-def cs_exact_ffn(layer: FfnLayer, x, preact, idx, count, y, ws: Workspace, mask=None, stream=None):
+def cs_exact_ffn(layer: FfnLayer, x, preact, idx, count, y, ws: Workspace, mask=None, stream=None,
+                 tau=0.0):
+    """tau: the magnitude cut |act(g_j)| > tau (0 with relu: the exact mask g_j > 0)."""
     _check(lib().cs_exact_ffn(C.byref(layer.c), _ptr(x), _ptr(preact), _ptr(idx), _ptr(count),
-                              _ptr(mask), _ptr(y), ws.ptr, ws.nbytes, _stream(stream)))
+                              _ptr(mask), _ptr(y), float(tau), ws.ptr, ws.nbytes, _stream(stream)))
 
 
 def cs_union_mask(masks, f, umask, uidx, ucount, ws: Workspace | None = None, stream=None):

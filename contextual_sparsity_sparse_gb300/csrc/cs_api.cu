@@ -107,6 +107,7 @@ cs_status check_layer(const cs_ffn_layer *L, int *ld_out) {
     CS_CHECK(L, "layer is null");
     CS_CHECK(L->d >= 1 && L->f >= 1, "layer: d and f must be >= 1 (d=%d f=%d)", L->d, L->f);
     CS_CHECK(dtype_ok(L->dtype), "layer: bad dtype %d", (int)L->dtype);
+    CS_CHECK(L->act == CS_ACT_RELU || L->act == CS_ACT_SILU, "layer: bad activation %d", (int)L->act);
     const int ld = L->ld ? L->ld : L->d;
     const size_t es = dtype_size(L->dtype);
     CS_CHECK(ld >= L->d, "layer: ld %d < d %d", ld, L->d);
@@ -276,7 +277,7 @@ cs_status cs_sparse_ffn(const cs_ffn_layer *layer, const float *x, int B, const 
     a.d = layer->d; a.f = layer->f; a.ld = ld; a.B = B; a.dtype = layer->dtype;
     a.w_gate = layer->w_gate; a.w_up = layer->w_up; a.w_down_t = layer->w_down_t; a.bias = layer->bias;
     a.x = x; a.idx = idx; a.count = count; a.preact = nullptr; a.y = y;
-    a.resid = nullptr; a.scale = 1.f;
+    a.resid = nullptr; a.scale = 1.f; a.act = layer->act;
     a.err = static_cast<uint32_t *>(ws);
     a.part = reinterpret_cast<float *>(static_cast<char *>(ws) + L.part);
     a.G = L.G; a.dp = L.dp;
@@ -289,7 +290,7 @@ cs_status cs_sparse_ffn(const cs_ffn_layer *layer, const float *x, int B, const 
 }
 
 cs_status cs_exact_ffn(const cs_ffn_layer *layer, const float *x, float *preact, int32_t *idx,
-                       int32_t *count, uint32_t *mask, float *y, void *ws, size_t ws_bytes,
+                       int32_t *count, uint32_t *mask, float *y, float tau, void *ws, size_t ws_bytes,
                        cs_stream_t stream) {
     int ld = 0;
     cs_status st = check_layer(layer, &ld);
@@ -298,6 +299,7 @@ cs_status cs_exact_ffn(const cs_ffn_layer *layer, const float *x, float *preact,
                  al4(y) && al4(mask),
              "cs_exact_ffn: x, preact, idx, count and y are required (4-byte aligned)");
     CS_CHECK(x != y, "cs_exact_ffn: y must not alias x");
+    CS_CHECK(tau >= 0.f, "cs_exact_ffn: tau must be >= 0");
     if (layer->f > kSelectMaxF) {
         set_error("cs_exact_ffn: f=%d exceeds the supported maximum %d", layer->f, kSelectMaxF);
         return CS_ERR_UNSUPPORTED;
@@ -313,7 +315,8 @@ cs_status cs_exact_ffn(const cs_ffn_layer *layer, const float *x, float *preact,
     cudaError_t e = launch_preact(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "cs_exact_ffn(preact)");
     SelectArgs sa;
-    sa.scores = preact; sa.B = 1; sa.f = layer->f; sa.kind = SEL_POSITIVE; sa.k = 0; sa.tau = 0.f;
+    sa.scores = preact; sa.B = 1; sa.f = layer->f; sa.k = 0; sa.tau = tau;
+    sa.kind = layer->act == CS_ACT_SILU ? SEL_SILU_MAG : SEL_POSITIVE;
     sa.idx = idx; sa.ld_idx = layer->f; sa.count = count; sa.mask = mask;
     e = launch_select(sa, s);
     if (e != cudaSuccess) return cuda_fail(e, "cs_exact_ffn(select)");
@@ -321,7 +324,7 @@ cs_status cs_exact_ffn(const cs_ffn_layer *layer, const float *x, float *preact,
     a.d = layer->d; a.f = layer->f; a.ld = ld; a.B = 1; a.dtype = layer->dtype;
     a.w_gate = layer->w_gate; a.w_up = layer->w_up; a.w_down_t = layer->w_down_t; a.bias = layer->bias;
     a.x = x; a.idx = idx; a.count = count; a.preact = preact; a.y = y;
-    a.resid = nullptr; a.scale = 1.f;
+    a.resid = nullptr; a.scale = 1.f; a.act = layer->act;
     a.err = static_cast<uint32_t *>(ws);
     a.part = reinterpret_cast<float *>(static_cast<char *>(ws) + L.part);
     a.G = L.G; a.dp = L.dp;

@@ -53,6 +53,7 @@ struct FfnK {
     int nvec;       // 16-byte vectors per row
     int ng;         // neurons per group
     int sg;         // groups in the ring (2 or 3)
+    int act;        // the gate's activation (CS_ACT_*)
 };
 
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) ffn_gather_kernel(const FfnK a
                 if (!PRE) gsum = warps_total(lane < nwarps ? red[p][q][t][0][lane] : 0.f);
                 if (GLU) usum = warps_total(lane < nwarps ? red[p][q][t][1][lane] : 0.f);
                 const float gv = PRE ? add : gsum + add;
-                float act = fmaxf(gv, 0.f);
+                float act = gate_act(a.act, gv);
                 if (GLU) act *= usum;
                 av[q][t] = valid ? act : 0.f;
             }
@@ -409,6 +410,7 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     k.B = a.B;
     k.dp = a.dp;
     k.ldb = a.ld * esz;
+    k.act = a.act;
     k.nvec = (a.d * esz + 15) / 16;
     const int nrow = (a.preact ? 0 : 1) + (a.w_up ? 1 : 0) + 1;
     const size_t per_neuron = (size_t)nrow * k.nvec * 16;

@@ -66,6 +66,7 @@ struct TcArgs {
     unsigned *tile_count;  // gate GEMM: [2P] arrivals per tile, zeroed by the split kernel
     uint32_t *err;
     int d, f, B, ldb, dk, kp, dp, splits, stages;
+    int act;               // the gate's activation (CS_ACT_*)
 };
 
 // ---- element type helpers --------------------------------------------------
@@ -202,14 +203,14 @@ constexpr int kGateSegMax = 3;
 __device__ __forceinline__ long long sk_start(int c, long long U, int P);
 __device__ __forceinline__ int sk_owner(long long u, long long U, int P);
 
-// act = relu(g + bias) (* u), written as the hi / lo rows of AS
+// act = relu(g + bias) or silu(g + bias) (* u), written as the hi / lo rows of AS
 template <typename T, bool GLU, int NP>
 __device__ __forceinline__ void gate_act_out(const TcArgs &a, const float (&g)[NP], const float (&u)[NP], float bias,
                                              bool live, int p) {
 #pragma unroll
     for (int b = 0; b < NP / 2; ++b) {
         if (b < a.B) {
-            float act = fmaxf(g[2 * b] + g[2 * b + 1] + bias, 0.f);
+            float act = gate_act(a.act, g[2 * b] + g[2 * b + 1] + bias);
             if (GLU) act *= u[2 * b] + u[2 * b + 1];
             act = live ? act : 0.f;
             const uint16_t hi = Tc<T>::bits(act);
@@ -660,6 +661,7 @@ cudaError_t run_tc(const FfnArgs &f, cudaStream_t s) {
     a.w_up = static_cast<const uint8_t *>(f.w_up);
     a.w_down_t = static_cast<const uint8_t *>(f.w_down_t);
     a.bias = f.bias;
+    a.act = f.act;
     a.x = f.x;
     a.idx = f.idx;
     a.count = f.count;

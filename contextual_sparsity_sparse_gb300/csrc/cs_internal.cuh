@@ -209,6 +209,13 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
         : "memory");
 }
 
+// The gate's activation: relu(g), or silu(g) = g / (1 + e^-g) with CUDA's
+// expf and an IEEE division (silu(-inf) = -inf / inf is NaN, never taken by
+// a magnitude cut; +inf stays +inf).
+__device__ __forceinline__ float gate_act(int act, float g) {
+    return act == CS_ACT_SILU ? g / (1.f + expf(-g)) : fmaxf(g, 0.f);
+}
+
 // ----------------------------------------------------------------------------
 // Reductions (fixed order, so results are bit-reproducible)
 // ----------------------------------------------------------------------------
@@ -292,7 +299,9 @@ struct PredictArgs {
 };
 cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s);
 
-enum SelKind { SEL_TOPK = 0, SEL_THRESHOLD = 1, SEL_POSITIVE = 2 };
+// SEL_POSITIVE: relu(s) > tau, i.e. s > tau (tau >= 0); SEL_SILU_MAG:
+// |silu(s)| > tau.  Both never take NaN.
+enum SelKind { SEL_TOPK = 0, SEL_THRESHOLD = 1, SEL_POSITIVE = 2, SEL_SILU_MAG = 3 };
 struct SelectArgs {
     const float *scores;
     int B, f;
@@ -323,6 +332,7 @@ struct FfnArgs {
     uint32_t *err;
     float *part;            // workspace partials
     int G, dp;
+    int act = CS_ACT_RELU;  // the gate's activation
     size_t ring_bytes = 0;  // gather ring budget; 0 = the default (most of an SM's shared memory)
     void *tc_x = nullptr;   // tensor-core path: [NP, d] split activations (or null)
     void *tc_a = nullptr;   // tensor-core path: [NP, roundup(f, 128)] split activations (or null)

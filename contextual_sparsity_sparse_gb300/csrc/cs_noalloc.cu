@@ -79,7 +79,7 @@ extern "C" cs_status cs_sparse_ffn_noalloc(const cs_ffn_layer *layer, const floa
     a.d = layer->d; a.f = layer->f; a.ld = ld; a.B = B; a.dtype = layer->dtype;
     a.w_gate = layer->w_gate; a.w_up = layer->w_up; a.w_down_t = layer->w_down_t; a.bias = layer->bias;
     a.x = x; a.idx = idx; a.count = count; a.preact = nullptr; a.y = y;
-    a.resid = nullptr; a.scale = 1.f;
+    a.resid = nullptr; a.scale = 1.f; a.act = layer->act;
     a.err = err;     // device-side error bits are not reported by this entry point
     a.part = part;   // every partial row is fully rewritten, so nothing needs clearing
     a.G = G; a.dp = dp;

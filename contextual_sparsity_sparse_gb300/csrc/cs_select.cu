@@ -300,8 +300,11 @@ select_row_kernel(const float *__restrict__ scores, int f, int k, float tau,
         } else if (KIND == SEL_THRESHOLD) {
             gt = x >= tau;
             eq = false;
-        } else {
-            gt = x > 0.f;
+        } else if (KIND == SEL_SILU_MAG) {
+            gt = fabsf(gate_act(CS_ACT_SILU, x)) > tau;
+            eq = false;
+        } else {   // SEL_POSITIVE: relu(x) > tau, tau >= 0
+            gt = x > tau;
             eq = false;
         }
     };
@@ -689,8 +692,11 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
         } else if (KIND == SEL_THRESHOLD) {
             gt = x >= tau;
             eq = false;
-        } else {
-            gt = x > 0.f;
+        } else if (KIND == SEL_SILU_MAG) {
+            gt = fabsf(gate_act(CS_ACT_SILU, x)) > tau;
+            eq = false;
+        } else {   // SEL_POSITIVE: relu(x) > tau, tau >= 0
+            gt = x > tau;
             eq = false;
         }
     };
@@ -781,6 +787,7 @@ template <int ET>
 cudaError_t run_select_cl_kind(const SelectArgs &a, cudaStream_t s) {
     if (a.kind == SEL_TOPK) return run_select_cl<ET, SEL_TOPK>(a, s);
     if (a.kind == SEL_THRESHOLD) return run_select_cl<ET, SEL_THRESHOLD>(a, s);
+    if (a.kind == SEL_SILU_MAG) return run_select_cl<ET, SEL_SILU_MAG>(a, s);
     return run_select_cl<ET, SEL_POSITIVE>(a, s);
 }
 
@@ -804,6 +811,7 @@ template <int ET>
 cudaError_t run_select_kind(const SelectArgs &a, cudaStream_t s) {
     if (a.kind == SEL_TOPK) return run_select_row<ET, SEL_TOPK>(a, s);
     if (a.kind == SEL_THRESHOLD) return run_select_row<ET, SEL_THRESHOLD>(a, s);
+    if (a.kind == SEL_SILU_MAG) return run_select_row<ET, SEL_SILU_MAG>(a, s);
     return run_select_row<ET, SEL_POSITIVE>(a, s);
 }
 

@@ -126,6 +126,7 @@ cudaError_t ffn_step(const StackPlan &p, const Bufs &b, int l, const float *xin,
     FfnArgs a;
     a.d = Ly.d; a.f = Ly.f; a.ld = Ly.ld ? Ly.ld : Ly.d; a.B = 1; a.dtype = Ly.dtype;
     a.w_gate = Ly.w_gate; a.w_up = Ly.w_up; a.w_down_t = Ly.w_down_t; a.bias = Ly.bias;
+    a.act = Ly.act;
     a.x = xin;
     int32_t *idx, *cnt;
     sel_out(p, b, l, &idx, &cnt);
@@ -148,7 +149,9 @@ cudaError_t exact_step(const StackPlan &p, const Bufs &b, int l, const float *xi
     cudaError_t e = launch_preact(pa, s);
     if (e != cudaSuccess) return e;
     SelectArgs sa;
-    sa.scores = b.pre; sa.B = 1; sa.f = p.f; sa.kind = SEL_POSITIVE; sa.k = 0; sa.tau = 0.f;
+    // the magnitude cut |act(g)| > tau (g > 0 for relu at tau = 0)
+    sa.scores = b.pre; sa.B = 1; sa.f = p.f; sa.k = 0; sa.tau = p.sel.tau;
+    sa.kind = Ly.act == CS_ACT_SILU ? SEL_SILU_MAG : SEL_POSITIVE;
     sel_out(p, b, l, &sa.idx, &sa.count);
     sa.ld_idx = p.f; sa.mask = nullptr;
     e = launch_select(sa, s);
@@ -283,6 +286,7 @@ cs_status check_models(const cs_ffn_layer *layers, const cs_predictor *preds, in
         const int ld = Ly.ld ? Ly.ld : Ly.d;
         const size_t es = dtype_size(Ly.dtype);
         if (Ly.d != d || Ly.f != f || Ly.dtype != dt || ld < d || (ld * es) % 16 ||
+            (Ly.act != CS_ACT_RELU && Ly.act != CS_ACT_SILU) ||
             !Ly.w_gate || !Ly.w_down_t || (reinterpret_cast<uintptr_t>(Ly.w_gate) & 15u) ||
             (reinterpret_cast<uintptr_t>(Ly.w_down_t) & 15u) || (reinterpret_cast<uintptr_t>(Ly.w_up) & 15u) ||
             (reinterpret_cast<uintptr_t>(Ly.bias) & 3u)) {
@@ -321,6 +325,10 @@ cs_status check_params(const cs_select_params *params, const char *who) {
     }
     if (params->hot < 0 || params->hot % 32 || (params->mode == CS_SEL_EXACT && params->hot)) {
         set_error("%s: hot must be a non-negative multiple of 32, and 0 in exact mode", who);
+        return CS_ERR_INVALID;
+    }
+    if (params->mode == CS_SEL_EXACT && !(params->tau >= 0.f)) {
+        set_error("%s: the exact mode's magnitude cut tau must be >= 0", who);
         return CS_ERR_INVALID;
     }
     return CS_OK;

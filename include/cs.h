@@ -64,7 +64,7 @@ typedef enum cs_dtype { CS_F32 = 0, CS_F16 = 1, CS_BF16 = 2 } cs_dtype;
 typedef enum cs_sel_mode {
     CS_SEL_TOPK = 0,      /* the k best scores, lower id wins ties [P2 "The Prediction Problem"] */
     CS_SEL_THRESHOLD = 1, /* scores >= tau [P3 "Implementation sketch", predict_active]          */
-    CS_SEL_EXACT = 2      /* gate pre-activation > 0, no predictor [P1, first section]           */
+    CS_SEL_EXACT = 2      /* |act(gate pre-activation)| > tau (relu, 0: g > 0), no predictor [P1] */
 } cs_sel_mode;
 
 typedef enum cs_stack_mode {
@@ -89,10 +89,19 @@ typedef struct cs_predictor {
 } cs_predictor;
 
 /*
- * One FFN layer, neuron-major.  w_up == NULL gives the ReLU FFN
- * (a_j = relu(g_j)); otherwise the ReLUfied gated FFN of [P2] "The SiLU/GELU
- * Challenge: TurboSparse" (a_j = relu(g_j) * (w_up_j . x)).  g_j = w_gate_j . x
- * + bias_j (bias may be NULL).  All three matrices share dtype and ld.
+ * The gate's activation: CS_ACT_RELU, relu(g) = max(g, 0); CS_ACT_SILU,
+ * silu(g) = g / (1 + e^-g), for SiLU-family models, which are only
+ * functionally sparse ([P2] "The Empirical Foundation": outputs non-zero but
+ * too small to matter; "The SiLU/GELU Challenge: TurboSparse").
+ */
+typedef enum cs_act { CS_ACT_RELU = 0, CS_ACT_SILU = 1 } cs_act;
+
+/*
+ * One FFN layer, neuron-major.  w_up == NULL gives the gate-only FFN
+ * (a_j = act(g_j)); otherwise the gated FFN of [P2] "The SiLU/GELU Challenge:
+ * TurboSparse" (a_j = act(g_j) * (w_up_j . x): ReLUfied SwiGLU with relu,
+ * SwiGLU with silu).  g_j = w_gate_j . x + bias_j (bias may be NULL).  All
+ * three matrices share dtype and ld.
  */
 typedef struct cs_ffn_layer {
     int d, f;
@@ -102,10 +111,13 @@ typedef struct cs_ffn_layer {
     const void *w_up;     /* [f, ld] device or NULL               */
     const void *w_down_t; /* [f, ld] device; row j = W_down[:, j] */
     const float *bias;    /* [f] device fp32 or NULL              */
+    cs_act act;           /* the gate's activation                */
 } cs_ffn_layer;
 
 /*
- * Selection: k for CS_SEL_TOPK (clamped to [0, f]); tau for CS_SEL_THRESHOLD.
+ * Selection: k for CS_SEL_TOPK (clamped to [0, f]); tau for CS_SEL_THRESHOLD
+ * (and, for CS_SEL_EXACT in cs_decode_stack / cs_decode_layer, the magnitude
+ * cut |act(g_j)| > tau, tau >= 0; see cs_exact_ffn).
  * hot: size of an always-on prefix for a frequency-sorted layout ([P2]
  * "Kernel-Level Implementation", neurons pre-sorted by how often they fire;
  * [P1] "Static locality: hot and cold neurons").  Neurons 0 .. hot-1 are
@@ -221,14 +233,16 @@ cs_status cs_sparse_ffn(const cs_ffn_layer *layer, const float *x, int B, const 
 /*
  * Exact-mask FFN for one token ([P1] first section: knowing which neurons are
  * inactive means computing every gate row).  Computes all pre-activations
- * g_j = w_gate_j . x + bias_j, selects A = {j : g_j > 0}, then
- * y = sum_{j in A} relu(g_j) (* w_up_j . x) w_down_t[j, :].
+ * g_j = w_gate_j . x + bias_j, selects A = {j : |act(g_j)| > tau} (the
+ * functional-sparsity cut of [P2] "The Empirical Foundation"; for relu at
+ * tau = 0 the exact mask {j : g_j > 0}), then
+ * y = sum_{j in A} act(g_j) (* w_up_j . x) w_down_t[j, :].
  *   preact: [f] fp32 device (output);  idx: [f] int32 device (output);
  *   count: int32 device (output);  mask: [ceil(f/32)] uint32 device or NULL;
- *   y: [d] fp32 device (output).
+ *   y: [d] fp32 device (output);  tau >= 0.  The selection decides in fp32.
  */
 cs_status cs_exact_ffn(const cs_ffn_layer *layer, const float *x, float *preact, int32_t *idx,
-                       int32_t *count, uint32_t *mask, float *y,
+                       int32_t *count, uint32_t *mask, float *y, float tau,
                        void *ws, size_t ws_bytes, cs_stream_t stream);
 
 /*
@@ -248,7 +262,8 @@ cs_status cs_union_mask(const uint32_t *masks, int B, int f, uint32_t *umask, in
  *   LOOKAHEAD:  A_l = select(P_l(x_{l-1})) (A_0 from x_0): the predictor and
  *               selection of layer l+1 run on s_pred while layer l's FFN runs
  *               on s_main.
- *   params->mode == CS_SEL_EXACT: A_l = {j : g_j > 0} at x_l; preds unused.
+ *   params->mode == CS_SEL_EXACT: A_l = {j : |act(g_j)| > params->tau} at x_l
+ *               (g_j > 0 for relu at tau = 0); preds unused.
  *   x: [d] fp32 device, input x_0 and output x_L.
  *   layers, preds: host arrays of L structs (same d, f, r and dtype).
  *   trace_count: [L] int32 device or NULL; trace_idx: [L, f] int32 device or
@@ -268,7 +283,8 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
  * (predictor, top-k, then the FFN over the chosen neurons only) and [P3]
  * "Implementation sketch" (predict the active set, then run the FFN on it):
  *     A = select(P(x)),  y = FFN(x, A)   (no residual).
- *   params->mode == CS_SEL_EXACT: A = {j : g_j > 0} at x; pred may be NULL.
+ *   params->mode == CS_SEL_EXACT: A = {j : |act(g_j)| > params->tau} at x (g_j > 0
+ *      for relu at tau = 0); pred may be NULL.
  *   x: [d] fp32 input;  y: [d] fp32 output.  Each may be device memory or
  *      page-locked host memory (cudaHostAlloc, cudaHostRegister, torch
  *      pin_memory).  Host data is staged through the workspace with

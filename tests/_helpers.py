@@ -44,8 +44,9 @@ def pad_ld(d, dt):
 class HostLayer:
     """One synthetic layer + predictor, as host arrays (storage form)."""
 
-    def __init__(self, d, f, r, dt, glu=False, seed=0, layer=0, rho=0.1, ld=None, bias=True):
+    def __init__(self, d, f, r, dt, glu=False, seed=0, layer=0, rho=0.1, ld=None, bias=True, act=0):
         self.d, self.f, self.r, self.dt, self.glu = d, f, r, dt, glu
+        self.act = act  # 0 relu, 1 silu
         self.ld = ld or pad_ld(d, dt)
         self.ldr = pad_ld(r, dt) if r else 0
         sd = 1 / math.sqrt(d)
@@ -60,7 +61,7 @@ class HostLayer:
 
     def oracle_layer(self):
         return oracle.Layer(self.d, self.f, self.dt, self.w_gate, self.w_down_t, w_up=self.w_up,
-                            bias=self.bias, ld=self.ld)
+                            bias=self.bias, ld=self.ld, act=self.act)
 
     def oracle_pred(self):
         return oracle.Predictor(self.d, self.r, self.f, self.dt, self.p_down, self.p_up,
@@ -72,7 +73,7 @@ class HostLayer:
         t = {k: upload(getattr(self, k), self.dt) for k in ("w_gate", "w_down_t")}
         t["w_up"] = upload(self.w_up, self.dt) if self.glu else None
         t["bias"] = torch.from_numpy(self.bias).cuda() if self.bias is not None else None
-        layer = cs.FfnLayer(t["w_gate"], t["w_down_t"], w_up=t["w_up"], bias=t["bias"], d=self.d)
+        layer = cs.FfnLayer(t["w_gate"], t["w_down_t"], w_up=t["w_up"], bias=t["bias"], d=self.d, act=self.act)
         pred = None
         if self.r:
             pd, pu = upload(self.p_down, self.dt), upload(self.p_up, self.dt)
@@ -130,8 +131,8 @@ def pick_tau_with_gap(s, eps, q):
     raise AssertionError("no decidable threshold")
 
 
-def stack_inputs(L, d, f, r, dt, glu=False, seed=0, rho=0.1):
-    Hs = [HostLayer(d, f, r, dt, glu=glu, seed=seed, layer=l, rho=rho) for l in range(L)]
+def stack_inputs(L, d, f, r, dt, glu=False, seed=0, rho=0.1, act=0):
+    Hs = [HostLayer(d, f, r, dt, glu=glu, seed=seed, layer=l, rho=rho, act=act) for l in range(L)]
     dev = [H.device() for H in Hs]
     return Hs, [a for a, _ in dev], [b for _, b in dev]
 
