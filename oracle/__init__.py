@@ -88,6 +88,8 @@ def lib():
             L.orc_stack.restype = I
             L.orc_decode.argtypes = [P, I, LG]
             L.orc_decode.restype = D
+            L.orc_decode_array.argtypes = [P, I, LG, P]
+            L.orc_decode_array.restype = None
             L.orc_threads.argtypes = []
             L.orc_threads.restype = I
             L.orc_set_threads.argtypes = [I]
@@ -232,6 +234,24 @@ def select_magnitude(pre32, act, tau):
     return out[:n].copy()
 
 
+def fit_predictor(Ly: Layer, P: Predictor, X, lam):
+    """The up map fitted to a layer: with P_down fixed, the ridge regression of
+    the gate pre-activations g(x) = W_gate x + b onto the bottleneck features
+    h(x) = relu(P_down x) over the calibration inputs X [N, d],
+        P_up = argmin_P  sum_n |P h(x_n) - g(x_n)|^2 + lam |P|_F^2
+             = G^T H (H^T H + lam I)^-1        (fp64, [f, r]),
+    with H = [h(x_n)]_n and G = [g(x_n)]_n.  Matrix products and the solve are
+    numpy's; the weights come through the oracle's own bit decoders."""
+    X = np.asarray(X, np.float64)
+    pd = decode(P.p_down, P.dtype).reshape(P.r, P.ld_down)[:, :P.d]
+    wg = decode(Ly.w_gate, Ly.dtype).reshape(Ly.f, Ly.ld)[:, :Ly.d]
+    b = np.zeros(Ly.f) if Ly.bias is None else Ly.bias.astype(np.float64)
+    H = np.maximum(X @ pd.T, 0.0)
+    G = X @ wg.T + b
+    A = H.T @ H + float(lam) * np.eye(P.r)
+    return np.linalg.solve(A, H.T @ G).T
+
+
 def union(masks, f):
     m = _c(masks, np.uint32)
     B = m.shape[0]
@@ -276,10 +296,8 @@ def decode(arr, dtype):
     """Decode a storage array to fp64 with the oracle's own bit decoders."""
     a = np.ascontiguousarray(arr)
     out = np.empty(a.size, np.float64)
-    L = lib()
-    flat = a.reshape(-1)
-    for i in range(flat.size):
-        out[i] = L.orc_decode(_ptr(flat), int(dtype), i)
+    if a.size:
+        lib().orc_decode_array(_ptr(a.reshape(-1)), int(dtype), int(a.size), _ptr(out))
     return out.reshape(a.shape)
 
 

@@ -66,6 +66,11 @@ static double elem(const void *base, int dtype, size_t i)
 }
 
 double orc_decode(const void *base, int dtype, long i) { return elem(base, dtype, (size_t)i); }
+void orc_decode_array(const void *base, int dtype, long n, double *out)
+{
+    for (long i = 0; i < n; i++)
+        out[i] = elem(base, dtype, (size_t)i);
+}
 
 /* -------------------------------------------------------------- predictor */
 

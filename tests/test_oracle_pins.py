@@ -469,3 +469,46 @@ def test_magnitude_selection_brute_force(orc, seed):
             [j for j in range(s.size) if relu[j] > tau], tau
     # relu at tau = 0 is the exact mask
     assert orc.select_magnitude(s, orc.ACT_RELU, 0.0).tolist() == orc.select_positive(s).tolist()
+
+
+# ------------------------------------------------ fitted predictor (next row 3)
+
+def identity_predictor(orc, d, f, dtype):
+    """r = 2d, P_down = [I; -I]: h(x) = [relu(x); relu(-x)], and x = h_top - h_bottom."""
+    eye = np.concatenate([np.eye(d), -np.eye(d)]).astype(np.float32)
+    pd = synth.to_storage(eye, dtype)
+    return orc.Predictor(d, 2 * d, f, dtype, pd, np.zeros((f, 2 * d), pd.dtype))
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.F16])
+def test_fit_recovers_an_exactly_representable_layer(orc, dtype):
+    """With P_down = [I; -I] and no bias, W x = [W, -W] h(x) exactly, so the
+    least-squares fit (lam -> 0) must return [W, -W]."""
+    d, f = 16, 40
+    W = synth.normal_matrix(6, 0, f, d, 1 / math.sqrt(d), dtype)
+    L = orc.Layer(d, f, dtype, W, W)
+    P = identity_predictor(orc, d, f, dtype)
+    X = synth.x_normal(7, 300, d)
+    got = orc.fit_predictor(L, P, X, 1e-10)
+    w = synth.storage_to_f64(W, dtype)
+    np.testing.assert_allclose(got, np.concatenate([w, -w], axis=1), rtol=0, atol=1e-7)
+
+
+def test_fit_heavy_ridge_limit_and_linearity(orc):
+    """(H^T H + lam I)^-1 -> I / lam as lam grows, so lam * P_up -> G^T H; and
+    doubling the layer (weights and bias) doubles the fit."""
+    d, f, r = 24, 60, 10
+    sd = 1 / math.sqrt(d)
+    W = synth.normal_matrix(8, 0, f, d, sd, synth.F32)
+    b = synth.zipf_bias(8, 0, f, 0.1)
+    pd = synth.normal_matrix(8, 1, r, d, sd, synth.F32)
+    L = orc.Layer(d, f, synth.F32, W, W, bias=b)
+    P = orc.Predictor(d, r, f, synth.F32, pd, np.zeros((f, r), np.float32))
+    X = synth.x_normal(9, 50, d).astype(np.float64)
+    H = np.maximum(X @ pd.astype(np.float64).T, 0)
+    G = X @ W.astype(np.float64).T + b
+    lam = 1e12
+    np.testing.assert_allclose(lam * orc.fit_predictor(L, P, X, lam), G.T @ H, rtol=1e-6)
+    L2 = orc.Layer(d, f, synth.F32, 2 * W, W, bias=2 * b)
+    np.testing.assert_allclose(orc.fit_predictor(L2, P, X, 0.5), 2 * orc.fit_predictor(L, P, X, 0.5),
+                               rtol=1e-12, atol=1e-12)
