@@ -44,6 +44,10 @@ WORKLOADS = {
     # the other 19,456 predicted (10% active in all, as opt13b-topk10)
     "opt13b-hot5-topk5": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.05,
                               hot=1024),
+    # opt13b-topk10 with every up map fitted to its layer (ridge regression over
+    # 2,048 synthetic calibration tokens); the line adds recall and precision
+    "opt13b-fitted-topk10": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.10,
+                                 fit=dict(N=2048, lam_per_token=1e-3)),
     # one LLaMA-70B-shaped SwiGLU layer with SiLU kept (functional sparsity), top-k 15%
     "llama70b-silu-topk15": dict(d=8192, f=28672, r=1024, dt=2, glu=True, rho=0.15, mode="topk", share=0.15,
                                  act=1),
@@ -224,6 +228,35 @@ def build_copies(W, torch, cs, synthdev):
     return copies
 
 
+def fitted_quality(cs, torch, copy, d, f, r, k, n_tokens=32):
+    """Mean recall and precision of a layer copy's predictor (top-k) against
+    the exact mask {g > 0}, both computed on the GPU, over held-out tokens."""
+    import numpy as np
+    import synth
+    layer, pred, _ = copy
+    ws = cs.Workspace(d, f, r)
+    pre = torch.empty(f, device="cuda")
+    ei = torch.empty(f, dtype=torch.int32, device="cuda")
+    ec = torch.empty(1, dtype=torch.int32, device="cuda")
+    y = torch.empty(d, device="cuda")
+    sc = torch.empty((1, f), device="cuda")
+    pi = torch.empty((1, f), dtype=torch.int32, device="cuda")
+    pc = torch.empty(1, dtype=torch.int32, device="cuda")
+    rec, prec = [], []
+    for x in synth.x_normal(7000, n_tokens, d):
+        xt = torch.from_numpy(x[None]).cuda()
+        cs.cs_exact_ffn(layer, xt, pre, ei, ec, y, ws)
+        cs.cs_predict(pred, xt, sc, ws)
+        cs.cs_select(sc, cs.select_params(cs.CS_SEL_TOPK, k), pi, pc, ws=ws)
+        torch.cuda.synchronize()
+        P = pi.cpu().numpy()[0, :int(pc.item())]
+        E = ei.cpu().numpy()[:int(ec.item())]
+        hit = np.intersect1d(P, E).size
+        rec.append(hit / max(E.size, 1))
+        prec.append(hit / max(P.size, 1))
+    return float(np.mean(rec)), float(np.mean(prec))
+
+
 def step_bytes(W, k):
     """Algorithmic bytes of one step (S8(d)-style accounting): predictor weights,
     scores written and read, selected rows (+ index and bias), x and y."""
@@ -251,6 +284,18 @@ def run_ours(args, W, rank, world):
     d, f, r = W["d"], W["f"], W["r"]
     k = synth.ceil_k(f, W["share"])
     copies = build_copies(W, torch, cs, synthdev)
+    quality = None
+    if W.get("fit"):
+        # setup: fit every copy's up map, then measure the first copy's
+        # recall / precision against the exact mask on held-out tokens
+        Nc, lam = W["fit"]["N"], W["fit"]["lam_per_token"] * W["fit"]["N"]
+        rec0, _ = fitted_quality(cs, torch, copies[0], d, f, r, k)
+        for l, (layer, pred, _) in enumerate(copies):
+            cs.cs_fit_predictor(layer, pred, torch.from_numpy(synth.x_normal(5000 + l, Nc, d)).cuda(), lam)
+        rec, prec = fitted_quality(cs, torch, copies[0], d, f, r, k)
+        quality = {"recall": rec, "precision": prec, "k": k, "random_up_map_recall": rec0,
+                   "calibration_tokens": Nc, "lambda": lam, "held_out_tokens": 32,
+                   "against": "exact mask {g > 0} (cs_exact_ffn) per held-out token"}
     X = torch.from_numpy(synth.x_normal(1000 + rank, NX, d)).cuda()
     s = torch.cuda.Stream()
     ws = cs.Workspace(d, f, r, stream=s)
@@ -398,6 +443,7 @@ def run_ours(args, W, rank, world):
                    "l2": f"inputs larger than L2: {NCOPY} layer copies ({NCOPY * (2 * f * d + r * d + (f - hot) * r) * (4 if W['dt'] == 0 else 2) / 1e9:.2f} GB) and {NX} inputs rotate; 7 other steps ({7 * total_b / 1e6:.0f} MB) run between uses of a copy",
                    "step": "cs_predict + cs_select + cs_sparse_ffn, graph of 200 steps"},
         "clocks": clocks,
+        **({"quality": quality} if quality else {}),
         "gpu_launches": 5 * K,
         "roofline": {"bound": "hbm", "kernel": "cs_sparse_ffn (gather + fixed-order reduce)",
                      "achieved": ffn_gbs, "peak": hbm, "unit": "GB/s", "frac": ffn_gbs / hbm,

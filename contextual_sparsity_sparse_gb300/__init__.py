@@ -32,7 +32,7 @@ EXPORTS = ["cs_version", "cs_status_string", "cs_last_error", "cs_workspace_size
            "cs_workspace_init", "cs_get_device_error", "cs_pack_transpose", "cs_predict",
            "cs_select", "cs_sparse_ffn", "cs_exact_ffn", "cs_union_mask", "cs_decode_stack",
            "cs_stack_release", "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows",
-           "cs_hot_order"]
+           "cs_hot_order", "cs_fit_scratch_size", "cs_fit_predictor"]
 
 
 class CsError(RuntimeError):
@@ -93,10 +93,14 @@ def lib():
                                           P, S, P, P, P]
             L.cs_permute_rows.argtypes = [P, I, I, P, I, I, I, P, I, P]
             L.cs_hot_order.argtypes = [P, I, P]
+            L.cs_fit_scratch_size.argtypes = [I, I, I, I]
+            L.cs_fit_scratch_size.restype = S
+            L.cs_fit_predictor.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), P, I, C.c_double, P, S, P]
             for name in ("cs_workspace_init", "cs_get_device_error", "cs_pack_transpose",
                          "cs_predict", "cs_select", "cs_sparse_ffn", "cs_exact_ffn",
                          "cs_union_mask", "cs_decode_stack", "cs_stack_release",
-                         "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows", "cs_hot_order"):
+                         "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows", "cs_hot_order",
+                         "cs_fit_predictor"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -289,6 +293,22 @@ def cs_hot_order(freq):
     out = torch.empty(fr.numel(), dtype=torch.int32)
     _check(lib().cs_hot_order(fr.data_ptr(), fr.numel(), out.data_ptr()))
     return out
+
+
+def cs_fit_predictor(layer: FfnLayer, pred: Predictor, X, lam, stream=None):
+    """Overwrite pred's up map with the ridge fit of the layer's gate
+    pre-activations onto relu(P_down x) over the calibration inputs X [N, d]
+    (see include/cs.h).  Waits for the stream."""
+    if X.dtype != torch.float32 or not X.is_cuda or not X.is_contiguous():
+        raise ValueError("X must be a contiguous fp32 CUDA tensor [N, d]")
+    N = X.shape[0]
+    n = lib().cs_fit_scratch_size(layer.d, layer.f, pred.r, N)
+    if n == 0:
+        raise ValueError("bad fit dimensions")
+    buf = torch.empty(n + 256, dtype=torch.uint8, device=X.device)
+    ptr = (buf.data_ptr() + 255) & ~255
+    _check(lib().cs_fit_predictor(C.byref(layer.c), C.byref(pred.c), _ptr(X), N, float(lam), ptr, n,
+                                  _stream(stream)))
 
 
 def cs_stack_release():

@@ -219,6 +219,23 @@ cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s) {
     return dispatch<EPI_NONE>(a.dtype, k, s, per_cta);
 }
 
+cudaError_t launch_gemv_batch(cs_dtype dt, const void *W, int ldb_bytes, int ncols, int nrows, const float *v,
+                              int B, float *out, const float *bias, int epi, uint32_t *err, cudaStream_t s) {
+    GemvK k = {};
+    k.W = static_cast<const uint8_t *>(W);
+    k.ldb = ldb_bytes;
+    k.ncols = ncols;
+    k.nrows = nrows;
+    k.v = v;
+    k.B = B;
+    k.out = out;
+    k.bias = bias;
+    k.err = err;
+    if (epi == 1) return dispatch<EPI_RELU>(dt, k, s);
+    if (epi == 2) return dispatch<EPI_BIAS>(dt, k, s);
+    return dispatch<EPI_NONE>(dt, k, s);
+}
+
 cudaError_t launch_preact(const PreactArgs &a, cudaStream_t s) {
     GemvK k = {};
     k.W = static_cast<const uint8_t *>(a.w_gate);

@@ -298,6 +298,11 @@ struct PredictArgs {
     bool small_smem = false;  // ~60 KB per CTA, to share SMs with a gather CTA
 };
 cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s);
+// out[b, row] = epi(sum_c W[row, c] v[b, c]) for rows < nrows and B tokens of
+// v [B, ncols]: epi 0 none, 1 relu, 2 + bias[row] (the predictor's streaming
+// GEMV, for calibration batches)
+cudaError_t launch_gemv_batch(cs_dtype dt, const void *W, int ldb_bytes, int ncols, int nrows, const float *v,
+                              int B, float *out, const float *bias, int epi, uint32_t *err, cudaStream_t s);
 
 // SEL_POSITIVE: relu(s) > tau, i.e. s > tau (tau >= 0); SEL_SILU_MAG:
 // |silu(s)| > tau.  Both never take NaN.

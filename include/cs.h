@@ -305,6 +305,27 @@ cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, c
                           const cs_select_params *params, void *ws, size_t ws_bytes, cs_stream_t stream,
                           int32_t *idx, int32_t *count);
 
+/*
+ * Fits a predictor's up map to its layer, [P2] "The Prediction Problem" (the
+ * predictor is trained to reproduce which neurons the layer activates) and
+ * [P1] "Precision, recall, and which error hurts".  With pred->p_down fixed,
+ * pred->p_up is overwritten with the ridge regression of the gate
+ * pre-activations g(x) = w_gate x + bias onto the bottleneck features
+ * h(x) = relu(p_down x) over N calibration inputs:
+ *     P_up = G^T H (H^T H + lambda I)^-1,  H = [h(x_n)] (N x r),  G = [g(x_n)] (N x f),
+ * H and G in fp32, H^T H and H^T G summed in fp64, the solve in fp64, the
+ * result rounded to pred->dtype.
+ *   X: [N, d] fp32 device (16-byte aligned).  lambda >= 0 (absolute; the
+ *   diagonal of H^T H grows with N).  pred->d and pred->f must equal the
+ *   layer's; r <= 2048; N <= 65535.  scratch: cs_fit_scratch_size(d, f, r, N) device
+ *   bytes, 256-byte aligned.
+ * A setup call: it waits for `stream` before returning, and returns
+ * CS_ERR_INVALID if H^T H + lambda I is not positive definite.
+ */
+size_t cs_fit_scratch_size(int d, int f, int r, int N);
+cs_status cs_fit_predictor(const cs_ffn_layer *layer, cs_predictor *pred, const float *X, int N, double lambda,
+                           void *scratch, size_t scratch_bytes, cs_stream_t stream);
+
 /* Drops every cached stack and layer graph (waits for nothing; call when idle). */
 cs_status cs_stack_release(void);
 
