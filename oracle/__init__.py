@@ -48,6 +48,11 @@ class _Layer(C.Structure):
                 ("bias", C.c_void_p), ("act", C.c_int)]
 
 
+class _Attn(C.Structure):
+    _fields_ = [("d", C.c_int), ("n_heads", C.c_int), ("d_head", C.c_int), ("dtype", C.c_int),
+                ("w_q", C.c_void_p), ("w_o_t", C.c_void_p)]
+
+
 class _Pred(C.Structure):
     _fields_ = [("d", C.c_int), ("r", C.c_int), ("f", C.c_int), ("dtype", C.c_int),
                 ("ld_down", C.c_long), ("ld_up", C.c_long),
@@ -75,6 +80,8 @@ def lib():
             L.orc_select_threshold.restype = I
             L.orc_select_hot.argtypes = [P, I, I, I, I, F, P]
             L.orc_select_hot.restype = I
+            L.orc_attention.argtypes = [C.POINTER(_Attn), P, P, I, P, P, I, P]
+            L.orc_attention.restype = I
             L.orc_select_magnitude.argtypes = [P, I, I, F, P]
             L.orc_select_magnitude.restype = I
             L.orc_select_positive.argtypes = [P, I, P]
@@ -250,6 +257,34 @@ def fit_predictor(Ly: Layer, P: Predictor, X, lam):
     G = X @ wg.T + b
     A = H.T @ H + float(lam) * np.eye(P.r)
     return np.linalg.solve(A, H.T @ G).T
+
+
+class AttnLayer:
+    """Head-sparse attention weights in storage form: w_q and w_o_t are
+    [H * d_head, d]; row block h holds head h (w_o_t is W_o transposed)."""
+
+    def __init__(self, d, n_heads, d_head, dtype, w_q, w_o_t):
+        self.d, self.n_heads, self.d_head, self.dtype = int(d), int(n_heads), int(d_head), int(dtype)
+        self.w_q = _c(w_q)
+        self.w_o_t = _c(w_o_t)
+
+    def c(self):
+        return _Attn(self.d, self.n_heads, self.d_head, self.dtype, _ptr(self.w_q), _ptr(self.w_o_t))
+
+
+def attention(A: AttnLayer, x, heads, k_cache, v_cache):
+    """y [d] (fp64) of head-sparse attention over the listed heads; caches are
+    [H, S, d_head] storage arrays."""
+    x = _c(x, np.float64)
+    h = _c(heads, np.int32)
+    kc, vc = _c(k_cache), _c(v_cache)
+    S = kc.shape[1]
+    y = np.empty(A.d, np.float64)
+    c = A.c()
+    rc = lib().orc_attention(C.byref(c), _ptr(x), _ptr(h), int(h.size), _ptr(kc), _ptr(vc), int(S), _ptr(y))
+    if rc != 0:
+        raise ValueError(f"orc_attention failed ({rc})")
+    return y
 
 
 def union(masks, f):

@@ -380,6 +380,83 @@ void orc_recall_precision(const int32_t *pred, int np, const int32_t *exact, int
     *precision = np ? (double)hit / np : 1.0;
 }
 
+/* ------------------------------------------------------------- attention */
+
+typedef struct {
+    int d, n_heads, d_head, dtype;
+    const void *w_q;     /* [H * d_head, d]: rows h*d_head .. of head h          */
+    const void *w_o_t;   /* [H * d_head, d]: W_o transposed, the same row blocks  */
+} orc_attn;
+
+/*
+ * Head-sparse attention for one token ([P1] first section: a small,
+ * input-dependent set of heads; [P2] "The Empirical Foundation": 20-30% of
+ * heads contribute per token; [P2] "Implications for System Design": select
+ * the heads to compute per token).  For each listed head h, over a cache of S
+ * keys and values k_{h,i}, v_{h,i} ([H, S, d_head] each):
+ *     q = W_q[h] x,  s_i = q . k_{h,i} / sqrt(d_head),  p = softmax(s),
+ *     o = sum_i p_i v_{h,i},  y += W_o[:, h] o.
+ * Heads in list order; ids outside [0, H) are a caller error (-1).
+ */
+int orc_attention(const orc_attn *A, const double *x, const int32_t *heads, int n, const void *kc,
+                  const void *vc, int S, double *y)
+{
+    const int d = A->d, dh = A->d_head, H = A->n_heads;
+    for (int t = 0; t < d; t++)
+        y[t] = 0.0;
+    if (n <= 0)
+        return 0;
+    if (S < 1)
+        return -1;
+    double *q = (double *)malloc(sizeof(double) * (size_t)dh);
+    double *o = (double *)malloc(sizeof(double) * (size_t)dh);
+    double *sc = (double *)malloc(sizeof(double) * (size_t)S);
+    if (!q || !o || !sc)
+        return -2;
+    int rc = 0;
+    const double scale = 1.0 / sqrt((double)dh);
+    for (int m = 0; m < n && rc == 0; m++) {
+        const int h = heads[m];
+        if (h < 0 || h >= H) {
+            rc = -1;
+            break;
+        }
+        for (int c = 0; c < dh; c++) {
+            double acc = 0.0;
+            for (int t = 0; t < d; t++)
+                acc += elem(A->w_q, A->dtype, ((size_t)h * dh + c) * d + t) * x[t];
+            q[c] = acc;
+        }
+        double mx = -INFINITY;
+        for (int i = 0; i < S; i++) {
+            double acc = 0.0;
+            for (int c = 0; c < dh; c++)
+                acc += q[c] * elem(kc, A->dtype, ((size_t)h * S + i) * dh + c);
+            sc[i] = acc * scale;
+            if (sc[i] > mx) mx = sc[i];
+        }
+        double z = 0.0;
+        for (int i = 0; i < S; i++) {
+            sc[i] = exp(sc[i] - mx);
+            z += sc[i];
+        }
+        for (int c = 0; c < dh; c++) {
+            double acc = 0.0;
+            for (int i = 0; i < S; i++)
+                acc += sc[i] * elem(vc, A->dtype, ((size_t)h * S + i) * dh + c);
+            o[c] = acc / z;
+        }
+        for (int t = 0; t < d; t++) {
+            double acc = 0.0;
+            for (int c = 0; c < dh; c++)
+                acc += o[c] * elem(A->w_o_t, A->dtype, ((size_t)h * dh + c) * d + t);
+            y[t] += acc;
+        }
+    }
+    free(q); free(o); free(sc);
+    return rc;
+}
+
 /* ------------------------------------------------------------------ stack */
 
 typedef struct {

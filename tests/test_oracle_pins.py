@@ -512,3 +512,73 @@ def test_fit_heavy_ridge_limit_and_linearity(orc):
     L2 = orc.Layer(d, f, synth.F32, 2 * W, W, bias=2 * b)
     np.testing.assert_allclose(orc.fit_predictor(L2, P, X, 0.5), 2 * orc.fit_predictor(L, P, X, 0.5),
                                rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------ head-sparse attention (next row 4)
+
+def attn_inputs(orc, d, H, dh, S, dtype, seed):
+    sd = 1 / math.sqrt(d)
+    wq = synth.normal_matrix(seed, 0, H * dh, d, sd, dtype)
+    wo = synth.normal_matrix(seed, 1, H * dh, d, 1 / math.sqrt(dh), dtype)
+    kc = synth.normal_matrix(seed, 2, H * S, dh, 1.0, dtype).reshape(H, S, dh)
+    vc = synth.normal_matrix(seed, 3, H * S, dh, 1.0, dtype).reshape(H, S, dh)
+    return orc.AttnLayer(d, H, dh, dtype, wq, wo), wq, wo, kc, vc
+
+
+def test_attention_one_key_returns_its_value(orc):
+    """With one cached position the softmax weight is 1 whatever q is:
+    y = sum_h W_o[:, h] v_h0, the same for any W_q."""
+    d, H, dh = 32, 4, 8
+    A, wq, wo, kc, vc = attn_inputs(orc, d, H, dh, 1, synth.F32, 1)
+    A0 = orc.AttnLayer(d, H, dh, synth.F32, np.zeros_like(wq), wo)
+    x = synth.x_normal(2, 1, d)[0]
+    heads = [0, 2, 3]
+    want = sum(wo[h * dh:(h + 1) * dh].astype(np.float64).T @ vc[h, 0].astype(np.float64) for h in heads)
+    np.testing.assert_allclose(orc.attention(A, x, heads, kc, vc), want, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(orc.attention(A0, x, heads, kc, vc), want, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_equal_keys_average_the_values(orc):
+    d, H, dh, S = 32, 3, 8, 9
+    A, wq, wo, kc, vc = attn_inputs(orc, d, H, dh, S, synth.F32, 3)
+    kc[:] = kc[:, :1, :]   # every position of a head has the same key
+    x = synth.x_normal(4, 1, d)[0]
+    want = sum(wo[h * dh:(h + 1) * dh].astype(np.float64).T @ vc[h].astype(np.float64).mean(axis=0)
+               for h in range(H))
+    np.testing.assert_allclose(orc.attention(A, x, range(H), kc, vc), want, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_two_keys_logistic_weight(orc):
+    """q = (c, 0, ..) and keys (a, 0, ..), 0: the weights are the logistic
+    function of c a / sqrt(d_head) and its complement."""
+    d, H, dh = 16, 2, 8
+    wq = np.zeros((H * dh, d), np.float32)
+    wq[1 * dh + 0, 5] = 1.0                 # head 1: q_0 = x_5
+    wo = np.zeros((H * dh, d), np.float32)
+    wo[1 * dh:2 * dh, :dh] = np.eye(dh)     # head 1: y[:dh] = o
+    kc = np.zeros((H, 2, dh), np.float32)
+    kc[1, 0, 0] = 1.5
+    vc = np.zeros((H, 2, dh), np.float32)
+    vc[1, 0, :] = 1.0
+    vc[1, 1, :] = -3.0
+    A = orc.AttnLayer(d, H, dh, synth.F32, wq, wo)
+    x = np.zeros(d)
+    x[5] = 2.0
+    p = 1.0 / (1.0 + math.exp(-2.0 * 1.5 / math.sqrt(dh)))
+    y = orc.attention(A, x, [1], kc, vc)
+    np.testing.assert_allclose(y[:dh], p * 1.0 + (1 - p) * -3.0, rtol=1e-14)
+    assert np.all(y[dh:] == 0)
+
+
+def test_attention_is_additive_over_heads_and_blind_to_cache_order(orc):
+    d, H, dh, S = 40, 6, 8, 13
+    A, wq, wo, kc, vc = attn_inputs(orc, d, H, dh, S, synth.F16, 5)
+    x = synth.x_normal(6, 1, d)[0]
+    heads = [1, 2, 4, 5]
+    both = orc.attention(A, x, heads, kc, vc)
+    np.testing.assert_allclose(both, sum(orc.attention(A, x, [h], kc, vc) for h in heads), rtol=1e-12,
+                               atol=1e-12)
+    perm = np.random.default_rng(7).permutation(S)
+    np.testing.assert_allclose(orc.attention(A, x, heads, kc[:, perm], vc[:, perm]), both, rtol=1e-12,
+                               atol=1e-12)
+    assert np.all(orc.attention(A, x, [], kc, vc) == 0)
