@@ -48,6 +48,9 @@ WORKLOADS = {
     # 2,048 synthetic calibration tokens); the line adds recall and precision
     "opt13b-fitted-topk10": dict(d=5120, f=20480, r=512, dt=1, glu=False, rho=0.10, mode="topk", share=0.10,
                                  fit=dict(N=2048, lam_per_token=1e-3)),
+    # head-sparse attention of an OPT-13B-shaped layer: 40 heads of 128, a
+    # 2,048-position KV cache, the top 25% of heads by a predictor (r = 128)
+    "opt13b-attn-heads25": dict(d=5120, H=40, dh=128, S=2048, r=128, dt=1, share=0.25, attn=True),
     # one LLaMA-70B-shaped SwiGLU layer with SiLU kept (functional sparsity), top-k 15%
     "llama70b-silu-topk15": dict(d=8192, f=28672, r=1024, dt=2, glu=True, rho=0.15, mode="topk", share=0.15,
                                  act=1),
@@ -805,6 +808,202 @@ def time_oracle(W, budget_s, max_steps=None):
     return n, el, oracle.threads()
 
 
+def attn_bytes(W, k):
+    """Algorithmic bytes of one head-sparse attention step: predictor, scores,
+    then per selected head its W_q and W_o row blocks and its K and V cache."""
+    d, H, dh, S, r = W["d"], W["H"], W["dh"], W["S"], W["r"]
+    e = 4 if W["dt"] == 0 else 2
+    pred = e * (r * d + H * r) + 4 * (d + r)
+    per_head = e * (2 * dh * d + 2 * S * dh)
+    attn = k * per_head + 4 * k + 4 * d * 2
+    return pred + 8 * H + attn, attn
+
+
+def run_attn(args, W, rank, world):
+    """One token per step: predictor over heads, top-k heads, head-sparse
+    attention (cs_sparse_attention), rotating over layer copies."""
+    import torch
+    import contextual_sparsity_sparse_gb300 as cs
+    import synth
+    import synth.device as synthdev
+    from contextual_sparsity_sparse_gb300 import build as cb
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    cb.build()
+    synthdev.build()
+    d, H, dh, S, r = W["d"], W["H"], W["dh"], W["S"], W["r"]
+    k = synth.ceil_k(H, W["share"])
+    tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}[W["dt"]]
+    copies = []
+    for l in range(NCOPY):
+        t = {}
+        for name, which, rows, cols, sd in (("w_q", 0, H * dh, d, 1 / math.sqrt(d)),
+                                            ("w_o", 1, H * dh, d, 1 / math.sqrt(dh)),
+                                            ("k", 2, H * S, dh, 1.0), ("v", 3, H * S, dh, 1.0),
+                                            ("p_down", synth.P_DOWN, r, d, 1 / math.sqrt(d)),
+                                            ("p_up", synth.P_UP, H, r, 1 / math.sqrt(r))):
+            t[name] = torch.empty((rows, cols), dtype=tdt, device="cuda")
+            synthdev.fill_normal(t[name], 0, synth.tensor_id(100 + l, which), sd)
+        t["k"], t["v"] = t["k"].view(H, S, dh), t["v"].view(H, S, dh)
+        copies.append((cs.AttnLayer(t["w_q"], t["w_o"], H), cs.Predictor(t["p_down"], t["p_up"]), t))
+    X = torch.from_numpy(synth.x_normal(1000 + rank, NX, d)).cuda()
+    s = torch.cuda.Stream()
+    ws = cs.Workspace(d, H, r, stream=s)
+    scores = torch.empty((1, H), device="cuda")
+    idx_all = torch.empty((NX, H), dtype=torch.int32, device="cuda")
+    cnt_all = torch.empty(NX, dtype=torch.int32, device="cuda")
+    Y = torch.empty((NX, d), device="cuda")
+    params = cs.select_params(cs.CS_SEL_TOPK, k)
+
+    def one_step(i):
+        layer, pred, t = copies[i % NCOPY]
+        j = i % NX
+        cs.cs_predict(pred, X[j:j + 1], scores, ws, stream=s)
+        cs.cs_select(scores, params, idx_all[j:j + 1], cnt_all[j:j + 1], ws=ws, stream=s)
+        cs.cs_sparse_attention(layer, X[j], idx_all[j], cnt_all[j:j + 1], t["k"], t["v"], Y[j], ws, stream=s)
+
+    NB = 200
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(3):
+            one_step(i)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(NB):
+                one_step(i)
+    K = max(NB, (args.steps // NB) * NB)
+    Wm = max(3 * NB, (args.warmup // NB) * NB)
+    with torch.cuda.stream(s):
+        for _ in range(Wm // NB):
+            g.replay()
+    s.synchronize()
+    if world > 1:
+        barrier(world)
+    torch.cuda.synchronize()
+    clk = Clocks(dev)
+    clk.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(K // NB):
+            g.replay()
+    e1.record(s)
+    e1.synchronize()
+    clocks = clk.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    barrier(world)
+    assert cs.cs_get_device_error(ws, stream=s) == 0
+
+    # roofline pass: the attention calls of the first NB steps alone (their
+    # head lists computed above), back to back on the same stream
+    def attn_call(i):
+        layer, _, t = copies[i % NCOPY]
+        j = i % NX
+        cs.cs_sparse_attention(layer, X[j], idx_all[j], cnt_all[j:j + 1], t["k"], t["v"], Y[j], ws, stream=s)
+
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g2, stream=s):
+            for i in range(NB):
+                attn_call(i)
+        for _ in range(3):
+            g2.replay()
+    s.synchronize()
+    reps = max(3, K // NB // 4)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(reps):
+            g2.replay()
+    f1.record(s)
+    f1.synchronize()
+    attn_avg_s = f0.elapsed_time(f1) / 1e3 / (reps * NB)
+
+    # e2e: pinned x in, the three calls, y out, every step
+    KE = min(K, 2000)
+    xh = torch.from_numpy(synth.x_normal(2000 + rank, 64, d)).pin_memory()
+    yh = torch.empty((64, d)).pin_memory()
+    xd = torch.empty((1, d), device="cuda")
+    yd = torch.empty(d, device="cuda")
+    idx1 = torch.empty((1, H), dtype=torch.int32, device="cuda")
+    cnt1 = torch.empty(1, dtype=torch.int32, device="cuda")
+
+    def e2e_step(i):
+        layer, pred, t = copies[i % NCOPY]
+        xd.copy_(xh[i % 64: i % 64 + 1], non_blocking=True)
+        cs.cs_predict(pred, xd, scores, ws, stream=s)
+        cs.cs_select(scores, params, idx1, cnt1, ws=ws, stream=s)
+        cs.cs_sparse_attention(layer, xd[0], idx1[0], cnt1, t["k"], t["v"], yd, ws, stream=s)
+        yh[i % 64].copy_(yd, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for i in range(50):
+            e2e_step(i)
+    s.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for i in range(KE):
+            e2e_step(i)
+    s.synchronize()
+    e2e_s = time.perf_counter() - t0
+
+    total_b, attn_b = attn_bytes(W, k)
+    hbm, src = peaks()
+    step_s = ms / 1e3 / K
+    gbs = attn_b / attn_avg_s / 1e9
+    return {
+        "metric": METRIC, "value": replica_value(K, world, ms), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "d": d, "heads": H, "d_head": dh, "kv_positions": S, "r": r,
+                   "k_heads": k, "weights": {0: "f32", 1: "f16", 2: "bf16"}[W["dt"]], "accumulate": "f32",
+                   "batch": 1, "global_batch": world, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {NCOPY} layer copies ({NCOPY * 2 * (H * dh * d + H * S * dh) * (4 if W['dt'] == 0 else 2) / 1e9:.2f} GB) and {NX} inputs rotate",
+                   "step": "cs_predict (one score per head) + cs_select (top-k heads) + cs_sparse_attention, graph of 200 steps"},
+        "clocks": clocks,
+        "gpu_launches": 5 * K,
+        "roofline": {"bound": "hbm", "kernel": "cs_sparse_attention (per-head attention + fixed-order reduce)",
+                     "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
+                     "bytes_per_launch": attn_b, "avg_launch_us": attn_avg_s * 1e6, "traffic": None},
+        "step_roofline": {"bytes_per_step": total_b, "achieved": total_b / step_s / 1e9, "peak": hbm,
+                          "frac": total_b / step_s / 1e9 / hbm, "unit": "GB/s"},
+        "e2e": {"value": world * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * d,
+                "d2h_bytes_per_step": 4 * d, "steps": KE,
+                "how": "Python binding per token: pinned H2D of x, cs_predict, cs_select, cs_sparse_attention, D2H of y; wall clock"},
+    }
+
+
+def time_oracle_attn(W, budget_s, max_steps=None):
+    """Time the oracle's head-sparse step (predict over heads, top-k, attention)."""
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    d, H, dh, S, r, dt = W["d"], W["H"], W["dh"], W["S"], W["r"], W["dt"]
+    k = synth.ceil_k(H, W["share"])
+    mk = lambda which, rows, cols, sd: synth.normal_matrix(0, synth.tensor_id(100, which), rows, cols, sd, dt)
+    A = oracle.AttnLayer(d, H, dh, dt, mk(0, H * dh, d, 1 / math.sqrt(d)), mk(1, H * dh, d, 1 / math.sqrt(dh)))
+    kc = mk(2, H * S, dh, 1.0).reshape(H, S, dh)
+    vc = mk(3, H * S, dh, 1.0).reshape(H, S, dh)
+    P = oracle.Predictor(d, r, H, dt, mk(synth.P_DOWN, r, d, 1 / math.sqrt(d)), mk(synth.P_UP, H, r, 1 / math.sqrt(r)))
+    X = synth.x_normal(3000, 64, d)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _, sc = oracle.predict(P, X[n % 64])
+        heads = oracle.select_topk(sc.astype(np.float32), k)
+        oracle.attention(A, X[n % 64], heads, kc, vc)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps and n >= max_steps):
+            break
+    return n, el, oracle.threads()
+
+
 def main():
     args = parse()
     W = WORKLOADS[args.workload]
@@ -824,6 +1023,21 @@ def main():
                              "sample": f"{tok} tokens of union steps, fp64 CPU oracle (at most 20 s)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
+    if args.impl == "reference" and W.get("attn"):
+        if rank != 0:
+            return
+        time_oracle_attn(W, budget_s=1e9, max_steps=max(1, args.warmup))
+        n, el, cores = time_oracle_attn(W, budget_s=1e9, max_steps=max(1, args.steps))
+        v = n / el
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * el / n, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "d": W["d"], "heads": W["H"], "kv_positions": W["S"]},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} head-sparse attention steps (predict, top-k heads, attention), fp64 CPU oracle"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
     if args.impl == "reference":
         if rank != 0:
             return
@@ -840,7 +1054,9 @@ def main():
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
     init_dist(world)
-    if "L" in W:
+    if W.get("attn"):
+        res = run_attn(args, W, rank, world)
+    elif "L" in W:
         res = run_stack(args, W, rank, world)
     elif "union" in W:
         res = run_union(args, W, rank, world)
@@ -850,6 +1066,10 @@ def main():
         tok, el, cores = time_oracle_union(W, args.cpu_sample_s)
         res["cpu_baseline"] = {"value": tok / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                "sample": f"{tok} tokens of union steps (B={W['union']}) in {el:.1f} s, fp64 CPU oracle on {cores} threads"}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline and W.get("attn"):
+        n, el, cores = time_oracle_attn(W, args.cpu_sample_s)
+        res["cpu_baseline"] = {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "sample": f"{n} head-sparse attention steps in {el:.1f} s, fp64 CPU oracle on {cores} threads"}
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, el, cores = time_oracle(W, args.cpu_sample_s)
         L = W.get("L", 1)

@@ -32,7 +32,7 @@ EXPORTS = ["cs_version", "cs_status_string", "cs_last_error", "cs_workspace_size
            "cs_workspace_init", "cs_get_device_error", "cs_pack_transpose", "cs_predict",
            "cs_select", "cs_sparse_ffn", "cs_exact_ffn", "cs_union_mask", "cs_decode_stack",
            "cs_stack_release", "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows",
-           "cs_hot_order", "cs_fit_scratch_size", "cs_fit_predictor"]
+           "cs_hot_order", "cs_fit_scratch_size", "cs_fit_predictor", "cs_sparse_attention"]
 
 
 class CsError(RuntimeError):
@@ -51,6 +51,11 @@ class _Layer(C.Structure):
     _fields_ = [("d", C.c_int), ("f", C.c_int), ("dtype", C.c_int), ("ld", C.c_int),
                 ("w_gate", C.c_void_p), ("w_up", C.c_void_p), ("w_down_t", C.c_void_p),
                 ("bias", C.c_void_p), ("act", C.c_int)]
+
+
+class _Attn(C.Structure):
+    _fields_ = [("d", C.c_int), ("n_heads", C.c_int), ("d_head", C.c_int), ("dtype", C.c_int),
+                ("w_q", C.c_void_p), ("w_o_t", C.c_void_p)]
 
 
 class _Sel(C.Structure):
@@ -93,6 +98,7 @@ def lib():
                                           P, S, P, P, P]
             L.cs_permute_rows.argtypes = [P, I, I, P, I, I, I, P, I, P]
             L.cs_hot_order.argtypes = [P, I, P]
+            L.cs_sparse_attention.argtypes = [C.POINTER(_Attn), P, P, P, P, P, I, P, P, S, P]
             L.cs_fit_scratch_size.argtypes = [I, I, I, I]
             L.cs_fit_scratch_size.restype = S
             L.cs_fit_predictor.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), P, I, C.c_double, P, S, P]
@@ -100,7 +106,7 @@ def lib():
                          "cs_predict", "cs_select", "cs_sparse_ffn", "cs_exact_ffn",
                          "cs_union_mask", "cs_decode_stack", "cs_stack_release",
                          "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows", "cs_hot_order",
-                         "cs_fit_predictor"):
+                         "cs_fit_predictor", "cs_sparse_attention"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -293,6 +299,28 @@ def cs_hot_order(freq):
     out = torch.empty(fr.numel(), dtype=torch.int32)
     _check(lib().cs_hot_order(fr.data_ptr(), fr.numel(), out.data_ptr()))
     return out
+
+
+class AttnLayer:
+    """Head-sparse attention weights: w_q and w_o_t are [n_heads * d_head, d]
+    CUDA tensors of one dtype (w_o_t is W_o transposed)."""
+
+    def __init__(self, w_q, w_o_t, n_heads):
+        if w_q.shape != w_o_t.shape or w_q.dtype != w_o_t.dtype or w_q.shape[0] % int(n_heads):
+            raise ValueError("w_q and w_o_t must both be [n_heads * d_head, d] of one dtype")
+        self.w_q, self.w_o_t = w_q, w_o_t
+        self.n_heads = int(n_heads)
+        self.d_head = w_q.shape[0] // self.n_heads
+        self.d = w_q.shape[1]
+        self.c = _Attn(self.d, self.n_heads, self.d_head, _dt(w_q), _ptr(w_q), _ptr(w_o_t))
+
+
+def cs_sparse_attention(layer: AttnLayer, x, heads, count, k_cache, v_cache, y, ws: Workspace, stream=None):
+    """y = the selected heads' attention over the KV cache (see include/cs.h);
+    k_cache / v_cache are [n_heads, seq_len, d_head] CUDA tensors."""
+    _check(lib().cs_sparse_attention(C.byref(layer.c), _ptr(x), _ptr(heads), _ptr(count), _ptr(k_cache),
+                                     _ptr(v_cache), int(k_cache.shape[1]), _ptr(y), ws.ptr, ws.nbytes,
+                                     _stream(stream)))
 
 
 def cs_fit_predictor(layer: FfnLayer, pred: Predictor, X, lam, stream=None):

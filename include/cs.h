@@ -306,6 +306,42 @@ cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, c
                           int32_t *idx, int32_t *count);
 
 /*
+ * Attention weights of one layer for head-sparse decoding ([P1] first
+ * section: a small, input-dependent set of heads; [P2] "The Empirical
+ * Foundation": 20-30% of heads contribute per token; [P2] "Implications for
+ * System Design": select the heads to compute per token).  Head h owns rows
+ * h*d_head .. h*d_head + d_head - 1 of both matrices:
+ *   w_q:   [n_heads * d_head, d] device, the query projection;
+ *   w_o_t: [n_heads * d_head, d] device, the output projection transposed
+ *          (row h*d_head + c is column h*d_head + c of W_o).
+ * d a multiple of 16 / element size; d_head a power of two from 16 / element
+ * size to 256; 16-byte aligned pointers.
+ */
+typedef struct cs_attn_layer {
+    int d, n_heads, d_head;
+    cs_dtype dtype;
+    const void *w_q;
+    const void *w_o_t;
+} cs_attn_layer;
+
+/*
+ * Head-sparse attention for one token over a KV cache.  For each of the
+ * count[0] heads listed in heads (ascending ids from cs_select over a
+ * predictor with one output per head):
+ *     q = W_q[h] x,  s_i = q . k_{h,i} / sqrt(d_head),  p = softmax(s),
+ *     o = sum_i p_i v_{h,i},  y = sum_h W_o[:, h] o      (fp32 throughout).
+ *   x: [d] fp32 device (16-byte aligned);  y: [d] fp32 device (output).
+ *   k_cache, v_cache: [n_heads, seq_len, d_head] device in layer->dtype.
+ *   1 <= seq_len <= 16384; n_heads <= the workspace's partial rows (the SM
+ *   count).  The workspace is any cs_workspace_size(d, ...) workspace.
+ * Ids outside [0, n_heads) are skipped and flagged (CS_DEVERR_INDEX); a count
+ * outside [0, n_heads] is clamped and flagged (CS_DEVERR_COUNT).
+ */
+cs_status cs_sparse_attention(const cs_attn_layer *layer, const float *x, const int32_t *heads,
+                              const int32_t *count, const void *k_cache, const void *v_cache, int seq_len,
+                              float *y, void *ws, size_t ws_bytes, cs_stream_t stream);
+
+/*
  * Fits a predictor's up map to its layer, [P2] "The Prediction Problem" (the
  * predictor is trained to reproduce which neurons the layer activates) and
  * [P1] "Precision, recall, and which error hurts".  With pred->p_down fixed,
