@@ -19,7 +19,8 @@
 // (slot, 8-row block) CTAs, one warp per row.  The core kernel gives each
 // head (slot, column chunk) CTAs: each forms the scores of all S keys (one
 // thread per key), a max-subtracted softmax with fixed-order sums and o
-// (threads over (channel, key residue) pairs, combined in a fixed order),
+// (threads over (key residue, 16-byte channel vector) pairs, combined in a
+// fixed order),
 // then its chunk of W_o[:, h] o, four warp groups over the d_head rows added
 // in order.  The chunks of one head repeat the softmax; their K and V come
 // from L2 after the first.  The FFN's fixed-order reduction adds the H
@@ -52,11 +53,6 @@ __device__ __forceinline__ float warp_max_f(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
     return v;
 }
-
-template <typename T> __device__ __forceinline__ float elem_f(T v);
-template <> __device__ __forceinline__ float elem_f<float>(float v) { return v; }
-template <> __device__ __forceinline__ float elem_f<__half>(__half v) { return __half2float(v); }
-template <> __device__ __forceinline__ float elem_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 constexpr int kQRows = 8;       // query rows per CTA (one per warp)
 constexpr int kOVec = 64;       // 16-byte column vectors of the output projection per CTA
@@ -188,19 +184,30 @@ __global__ void __launch_bounds__(kAttnThreads) attn_core_kernel(const AttnK a) 
     __syncthreads();
     const float inv_z = 1.f / s_z;
 
-    // 4. o[c] = sum_i p_i v_i[c] / Z: thread (g, c) takes keys i = g (mod G)
+    // 4. o[c] = sum_i p_i v_i[c] / Z: thread (g, u) takes keys i = g (mod G)
+    //    and the 16-byte vector u of channels; the G groups are added in order
+    //    (d_head / V vectors per row, a power of two, so G * (d_head / V) = 256)
     {
-        const int G = kAttnThreads / dh;
-        const int c = tid % dh, g = tid / dh;
-        const T *vb = reinterpret_cast<const T *>(a.v + (size_t)h * head_bytes);
-        float acc = 0.f;
-        if (g < G)
-            for (int i = g; i < S; i += G) acc = fmaf(s[i], elem_f<T>(vb[(size_t)i * dh + c]), acc);
-        red[tid] = acc;
+        const int nvh = dh / V, G = kAttnThreads / nvh;
+        const int u = tid % nvh, g = tid / nvh;
+        const uint4 *vb = reinterpret_cast<const uint4 *>(a.v + (size_t)h * head_bytes);
+        float acc[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = 0.f;
+        for (int i = g; i < S; i += G) {
+            float w[V];
+            unpack<T>(__ldg(vb + (size_t)i * nvh + u), w);
+            const float pi = s[i];
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = fmaf(pi, w[e], acc[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < V; ++e) red5[(size_t)tid * V + e] = acc[e];   // [g][u][e]
         __syncthreads();
         if (tid < dh) {
+            const int uu = tid / V, ee = tid % V;
             float t = 0.f;
-            for (int gg = 0; gg < G; ++gg) t += red[gg * dh + tid];
+            for (int gg = 0; gg < G; ++gg) t += red5[((size_t)gg * nvh + uu) * V + ee];
             o[tid] = t * inv_z;
         }
         __syncthreads();
