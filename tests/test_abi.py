@@ -121,3 +121,31 @@ def test_select_hot_validation_without_gpu(lib):
     ex = cs.select_params(cs.CS_SEL_EXACT, hot=32)
     assert lib.cs_decode_layer(C.byref(L), None, 1024, 1024, C.byref(ex), 4096, 1 << 20, None,
                                None, None) == 1
+
+
+def test_attention_and_fit_validation_without_gpu(lib):
+    """Bad layouts are refused on the host, before any CUDA call."""
+    fake = 4096
+    A = cs._Attn(512, 8, 64, cs.CS_F16, fake, fake)
+    # d_head not a power of two
+    bad = cs._Attn(512, 8, 48, cs.CS_F16, fake, fake)
+    assert lib.cs_sparse_attention(C.byref(bad), fake, fake, fake, fake, fake, 16, fake, fake, 1 << 20, None) == 1
+    assert b"d_head" in lib.cs_last_error()
+    # misaligned weights
+    mis = cs._Attn(512, 8, 64, cs.CS_F16, fake + 2, fake)
+    assert lib.cs_sparse_attention(C.byref(mis), fake, fake, fake, fake, fake, 16, fake, fake, 1 << 20, None) == 1
+    # seq_len outside [1, 16384] (x and y distinct here)
+    y = 2 * fake
+    assert lib.cs_sparse_attention(C.byref(A), fake, fake, fake, fake, fake, 0, y, fake, 1 << 20, None) == 1
+    assert lib.cs_sparse_attention(C.byref(A), fake, fake, fake, fake, fake, 20000, y, fake, 1 << 20, None) == 3
+    # x aliasing y
+    assert lib.cs_sparse_attention(C.byref(A), fake, fake, fake, fake, fake, 16, fake, fake, 1 << 20, None) == 1
+    # the fit: negative ridge, a predictor for another layer
+    L = cs._Layer(128, 64, cs.CS_F16, 128, 256, 0, 256, 0)
+    P = cs._Pred(128, 8, 64, cs.CS_F16, 0, 0, 256, 256)
+    assert lib.cs_fit_predictor(C.byref(L), C.byref(P), fake, 16, -1.0, fake, 1 << 30, None) == 1
+    P2 = cs._Pred(128, 8, 32, cs.CS_F16, 0, 0, 256, 256)
+    assert lib.cs_fit_predictor(C.byref(L), C.byref(P2), fake, 16, 1.0, fake, 1 << 30, None) == 1
+    assert b"match the layer" in lib.cs_last_error()
+    assert lib.cs_fit_scratch_size(128, 64, 8, 0) == 0
+    assert lib.cs_fit_scratch_size(128, 64, 8, 16) > 16 * 64 * 4
