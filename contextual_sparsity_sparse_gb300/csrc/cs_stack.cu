@@ -281,6 +281,10 @@ cs_status check_models(const cs_ffn_layer *layers, const cs_predictor *preds, in
         set_error("%s: layer 0 has a bad shape or dtype", who);
         return CS_ERR_INVALID;
     }
+    if (!exact && hot >= f) {
+        set_error("%s: the hot prefix (%d) must leave a tail of neurons to predict (f = %d)", who, hot, f);
+        return CS_ERR_INVALID;
+    }
     for (int l = 0; l < L; ++l) {
         const cs_ffn_layer &Ly = layers[l];
         const int ld = Ly.ld ? Ly.ld : Ly.d;

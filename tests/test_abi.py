@@ -118,6 +118,11 @@ def test_select_hot_validation_without_gpu(lib):
     assert lib.cs_decode_layer(C.byref(L), C.byref(P), 1024, 1024, C.byref(sel), 4096, 1 << 20, None,
                                None, None) == 1
     assert b"tail" in lib.cs_last_error()
+    allhot = cs.select_params(cs.CS_SEL_TOPK, 5, hot=64)    # no tail left to predict
+    P0 = cs._Pred(128, 8, 0, cs.CS_F16, 0, 0, 256, 256)
+    assert lib.cs_decode_layer(C.byref(L), C.byref(P0), 1024, 1024, C.byref(allhot), 4096, 1 << 20, None,
+                               None, None) == 1
+    assert b"tail" in lib.cs_last_error()
     ex = cs.select_params(cs.CS_SEL_EXACT, hot=32)
     assert lib.cs_decode_layer(C.byref(L), None, 1024, 1024, C.byref(ex), 4096, 1 << 20, None,
                                None, None) == 1
