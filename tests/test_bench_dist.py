@@ -71,3 +71,23 @@ def test_reference_arm_on_a_nonzero_rank_prints_nothing():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_algorithmic_bytes_match_the_per_unit_accounting():
+    """The roofline numerators: predictor bytes e (r d + f r), and per selected
+    neuron m d e weight bytes plus its id and bias (4 + 4), for the OPT-13B-
+    shaped layer at k = 2048 (26.21 MB of predictor, 41.95 MB of rows)."""
+    import bench
+    W = bench.WORKLOADS["opt13b-topk10"]
+    total, ffn = bench.step_bytes(W, 2048)
+    assert ffn == 2048 * (2 * 5120 * 2 + 8) + 8 * 5120 == 42_000_384
+    pred = 2 * (512 * 5120 + 20480 * 512)
+    assert abs(pred - 26.21e6) < 0.01e6
+    assert total == pred + 4 * (5120 + 512) * 2 + 4 * 20480 + 4 * 2048 + ffn
+    # the hot layout predicts only the tail; the same 2048 rows are gathered
+    th, fh = bench.step_bytes(bench.WORKLOADS["opt13b-hot5-topk5"], 1024)
+    assert fh == ffn and total - th == 2 * 1024 * 512 + 4 * 1024
+    # head-sparse attention: per head 2 d_head d + 2 S d_head elements
+    Wa = bench.WORKLOADS["opt13b-attn-heads25"]
+    ta, aa = bench.attn_bytes(Wa, 10)
+    assert aa == 10 * 2 * (2 * 128 * 5120 + 2 * 2048 * 128) + 4 * 10 + 8 * 5120
