@@ -8,6 +8,8 @@
 // cs_sparse_ffn keeps in the caller's workspace, live here in a file-scope
 // device array instead.  There is no counterpart of this in the method's
 // sources; it only changes where the scratch memory comes from.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "cs_internal.cuh"
@@ -18,14 +20,65 @@ namespace {
 // library, held until the process exits).  A call needs
 // (SM count) * B * roundup(d, 8) of them.
 constexpr size_t kNoAllocFloats = size_t(1) << 21;
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) float g_noalloc_part[kNoAllocFloats];
 __device__ __align__(256) uint32_t g_noalloc_err[64];
 
+// The arrays' device addresses differ per CUDA context (each context loads its
+// own copy of the module), so they are looked up once per context and cached
+// under that context's handle.  The current context is read through the
+// driver entry point that the runtime exposes, so the library does not link
+// the driver library itself.
+struct Slot {
+    CUcontext ctx;
+    float *part;
+    uint32_t *err;
+};
+constexpr int kSlots = 64;
+
 std::mutex g_mu;
-float *g_part_ptr[kMaxDevices] = {};
-uint32_t *g_err_ptr[kMaxDevices] = {};
+Slot g_slots[kSlots] = {};
+int g_nslots = 0;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+// The current context, or null when it cannot be read.
+CUcontext current_context() {
+    static CtxGetCurrentFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<CtxGetCurrentFn>(nullptr);
+        }
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// The arrays' addresses in the current context.
+cudaError_t scratch_addresses(float **part, uint32_t **err) {
+    const CUcontext ctx = current_context();
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (ctx) {
+        for (int i = 0; i < g_nslots; ++i)
+            if (g_slots[i].ctx == ctx) {
+                *part = g_slots[i].part;
+                *err = g_slots[i].err;
+                return cudaSuccess;
+            }
+    }
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(part), g_noalloc_part);
+    if (e != cudaSuccess) return e;
+    e = cudaGetSymbolAddress(reinterpret_cast<void **>(err), g_noalloc_err);
+    if (e != cudaSuccess) return e;
+    // without a readable context every call looks the addresses up again
+    if (ctx && g_nslots < kSlots) g_slots[g_nslots++] = Slot{ctx, *part, *err};
+    return cudaSuccess;
+}
 
 }  // namespace
 
@@ -42,13 +95,6 @@ extern "C" cs_status cs_sparse_ffn_noalloc(const cs_ffn_layer *layer, const floa
         set_error("cs_sparse_ffn_noalloc: B >= 1 and distinct, 4-byte aligned x, y, idx, count are required");
         return CS_ERR_INVALID;
     }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cs_sparse_ffn_noalloc(device)");
-    if (dev < 0 || dev >= kMaxDevices) {
-        set_error("cs_sparse_ffn_noalloc: device ordinal %d out of range", dev);
-        return CS_ERR_UNSUPPORTED;
-    }
     const int G = device_sm_count() > 0 ? device_sm_count() : 1;
     const int dp = (layer->d + 7) & ~7;
     const size_t need = (size_t)G * (size_t)B * (size_t)dp;
@@ -57,24 +103,10 @@ extern "C" cs_status cs_sparse_ffn_noalloc(const cs_ffn_layer *layer, const floa
                   need, G, B, dp, kNoAllocFloats);
         return CS_ERR_UNSUPPORTED;
     }
-    float *part;
-    uint32_t *err;
-    {
-        // the device addresses of the arrays, looked up once per device
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_part_ptr[dev]) {
-            float *pp = nullptr;
-            uint32_t *pe = nullptr;
-            e = cudaGetSymbolAddress(reinterpret_cast<void **>(&pp), g_noalloc_part);
-            if (e != cudaSuccess) return cuda_fail(e, "cs_sparse_ffn_noalloc(symbol address)");
-            e = cudaGetSymbolAddress(reinterpret_cast<void **>(&pe), g_noalloc_err);
-            if (e != cudaSuccess) return cuda_fail(e, "cs_sparse_ffn_noalloc(symbol address)");
-            g_part_ptr[dev] = pp;
-            g_err_ptr[dev] = pe;
-        }
-        part = g_part_ptr[dev];
-        err = g_err_ptr[dev];
-    }
+    float *part = nullptr;
+    uint32_t *err = nullptr;
+    cudaError_t e = scratch_addresses(&part, &err);
+    if (e != cudaSuccess) return cuda_fail(e, "cs_sparse_ffn_noalloc(symbol address)");
     FfnArgs a;
     a.d = layer->d; a.f = layer->f; a.ld = ld; a.B = B; a.dtype = layer->dtype;
     a.w_gate = layer->w_gate; a.w_up = layer->w_up; a.w_down_t = layer->w_down_t; a.bias = layer->bias;
@@ -83,6 +115,8 @@ extern "C" cs_status cs_sparse_ffn_noalloc(const cs_ffn_layer *layer, const floa
     a.err = err;     // device-side error bits are not reported by this entry point
     a.part = part;   // every partial row is fully rewritten, so nothing needs clearing
     a.G = G; a.dp = dp;
+    // tc_x / tc_a stay null: the tensor-core path needs workspace buffers, so
+    // every batch runs on the CUDA-core gather kernel
     e = launch_ffn(a, (cudaStream_t)stream);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_sparse_ffn_noalloc");
 }

@@ -369,16 +369,22 @@ cs_status cs_stack_release(void);
  * cs_sparse_ffn without a workspace, for callers that cannot allocate device
  * memory (for example a plugin running inside a host framework that owns all
  * device allocations and gives it no allocator, or a path where a cudaMalloc
- * may not be issued).  The method's sources have no counterpart of this call:
- * it computes exactly what cs_sparse_ffn computes, with the same arguments
- * minus the workspace.
+ * may not be issued).  The method's sources have no counterpart of this call.
+ * Same arguments as cs_sparse_ffn minus the workspace.  It always runs the
+ * CUDA-core gather kernel, so its y is bit-identical to cs_sparse_ffn's
+ * wherever cs_sparse_ffn takes that kernel too (every fp32 layer, and every
+ * batch below the tensor-core threshold of 4 tokens).  Where cs_sparse_ffn
+ * takes the tensor-core path (fp16 / bf16, d a multiple of 64, 4 <= B <= 32)
+ * the two agree within the library's tolerance (max |difference| / max |y|
+ * below 2e-3) but not bit for bit.
  *
  * Scratch: a fixed device array inside the library (2^21 fp32 values, 8 MiB,
  * held by every GPU that loads the library until the process exits).  A call
  * needs (SM count) * B * roundup(d, 8) values; larger calls return
  * CS_ERR_UNSUPPORTED without enqueuing anything.  The call allocates nothing.
- * The first call on a device looks up the array's device address (once per
- * device), so make that first call before any stream capture begins.
+ * The first call in a CUDA context looks up the array's device address in
+ * that context (cached per context afterwards), so make that first call
+ * before any stream capture begins.
  * Every call shares the one array and it keeps the last call's contents
  * (each call rewrites all of what it reads): calls that overlap on the GPU,
  * on different streams or from different threads, race and must be ordered

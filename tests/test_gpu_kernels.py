@@ -301,12 +301,18 @@ def test_exact_ffn(dt, glu, shape):
     wg = synth.storage_to_f64(H.w_gate, dt)[:, :d]
     eps = 64 * 2.0 ** -24 * (np.abs(wg) @ np.abs(X[0].astype(np.float64)) + np.abs(H.bias))
     n = int(cnt.item())
-    got = set(idx.cpu().numpy()[:n].tolist())
+    gpre = pre.cpu().numpy()
+    gidx = idx.cpu().numpy()[:n]
+    # bit-exact: the oracle's exact mask {g > 0} taken on the GPU's own fp32
+    # pre-activations is the GPU's index list and mask
+    assert np.array_equal(gidx, oracle.select_positive(gpre))
+    assert np.array_equal(mask.cpu().numpy().view(np.uint32), synth.bits_from_bool(gpre > 0))
+    # and every neuron decided beyond fp32 rounding agrees with the fp64 oracle
+    got = set(gidx.tolist())
     sure_in = set(np.flatnonzero(opre > eps).tolist())
     sure_out = set(np.flatnonzero(opre < -eps).tolist())
     assert sure_in <= got and not (got & sure_out)
-    assert np.array_equal(mask.cpu().numpy().view(np.uint32),
-                          synth.bits_from_bool(np.isin(np.arange(f), sorted(got))))
+    assert rel_err(y.cpu().numpy(), oracle.ffn(O, X[0], gidx)) < TOL
     assert rel_err(y.cpu().numpy(), oracle.dense_ffn(O, X[0])) < TOL
 
 

@@ -72,7 +72,7 @@ def test_step_topk(case):
     assert cs.cs_get_device_error(ws) == 0
 
 
-@pytest.mark.parametrize("case", STEP_CASES[:3], ids=[c[0] for c in STEP_CASES[:3]])
+@pytest.mark.parametrize("case", STEP_CASES[:4], ids=[c[0] for c in STEP_CASES[:4]])
 def test_step_threshold(case):
     name, d, f, r, dt, glu, rho = case
     H = HostLayer(d, f, r, dt, glu=glu, seed=0, rho=rho)
