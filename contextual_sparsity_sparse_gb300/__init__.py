@@ -245,19 +245,30 @@ def cs_union_mask(masks, f, umask, uidx, ucount, ws: Workspace | None = None, st
                                ws.ptr if ws else None, ws.nbytes if ws else 0, _stream(stream)))
 
 
+class StackArgs:
+    """The layer and predictor arrays of a stack, marshalled once, for
+    repeated cs_decode_stack calls."""
+
+    def __init__(self, layers, preds):
+        self.L = len(layers)
+        self.layers = (_Layer * self.L)(*[l.c for l in layers])
+        self.preds = (_Pred * self.L)(*[p.c for p in preds]) if preds is not None else None
+
+
 def cs_decode_stack(layers, preds, x, resid_scale, params, mode, ws: Workspace, s_main=None,
                     s_pred=None, trace_count=None, trace_idx=None):
-    L = len(layers)
-    larr = (_Layer * L)(*[l.c for l in layers])
-    parr = (_Pred * L)(*[p.c for p in preds]) if preds is not None else None
+    """x_0 -> x_L in place (see include/cs.h).  x may be a CUDA tensor or a
+    pinned CPU tensor.  layers may also be a StackArgs (preds then unused)."""
+    sa = layers if isinstance(layers, StackArgs) else StackArgs(layers, preds)
     sp = None if s_pred is None else _stream(s_pred)
-    _check(lib().cs_decode_stack(larr, parr, L, _ptr(x), float(resid_scale), C.byref(params),
+    d = sa.layers[0].d
+    _check(lib().cs_decode_stack(sa.layers, sa.preds, sa.L, _io_ptr(x, d), float(resid_scale), C.byref(params),
                                  int(mode), _stream(s_main), sp, ws.ptr, ws.nbytes,
                                  _ptr(trace_count), _ptr(trace_idx)))
 
 
 def _io_ptr(t, n):
-    """x or y of cs_decode_layer: a CUDA tensor or a pinned CPU tensor, fp32,
+    """x or y of cs_decode_layer / cs_decode_stack: a CUDA tensor or a pinned CPU tensor, fp32,
     contiguous, holding at least n values (the library itself refuses
     pageable host memory)."""
     if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() < n:

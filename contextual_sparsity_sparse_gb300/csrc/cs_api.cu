@@ -67,6 +67,7 @@ WsLayout ws_layout(int d, int f, int r, int B, int num_sms) {
     L.st_count = off;  off += 256;
     L.st_h = off;      off += align256(sizeof(float) * (size_t)r);
     L.io_y = off;      off += align256(sizeof(float) * (size_t)L.dp);
+    L.io_x = off;      off += align256(sizeof(float) * (size_t)L.dp);
     L.tc = off;        off += tc_workspace_bytes(d, f, B);
     L.total = off;
     return L;

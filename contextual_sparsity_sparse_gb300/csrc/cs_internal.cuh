@@ -32,6 +32,7 @@ struct WsLayout {
     size_t st_count = 0;    // [2] int32 stack counts
     size_t st_h = 0;        // [r] fp32 stack predictor bottleneck
     size_t io_y = 0;        // [dp] fp32 single-layer step: y staged for a host copy
+    size_t io_x = 0;        // [dp] fp32 stack: x staged for host copies
     size_t bt_a = 0;        // [Bmax, fu] fp32 batched activations
     size_t tc = 0;          // tensor-core path buffers (tc_workspace_bytes), 0 bytes when B < 2
     size_t total = 0;

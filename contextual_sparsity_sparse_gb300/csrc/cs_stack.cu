@@ -382,12 +382,12 @@ cs_status run_cached(const StackPlan &p, cudaStream_t sm, cudaStream_t sp_key, c
 // Where a pointer given for x or y lives: device (or managed) memory is used
 // in place, page-locked host memory is staged through the workspace, and
 // pageable host memory is refused (its copies cannot be asynchronous).
-cs_status io_kind(const void *ptr, bool *host, const char *what) {
+cs_status io_kind(const void *ptr, bool *host, const char *who, const char *what) {
     cudaPointerAttributes at = {};
     cudaError_t e = cudaPointerGetAttributes(&at, ptr);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        set_error("cs_decode_layer: %s: %s", what, cudaGetErrorString(e));
+        set_error("%s: %s: %s", who, what, cudaGetErrorString(e));
         return CS_ERR_INVALID;
     }
     if (at.type == cudaMemoryTypeHost) {
@@ -398,7 +398,7 @@ cs_status io_kind(const void *ptr, bool *host, const char *what) {
         *host = false;
         return CS_OK;
     }
-    set_error("cs_decode_layer: %s is pageable host memory; use device or page-locked host memory", what);
+    set_error("%s: %s is pageable host memory; use device or page-locked host memory", who, what);
     return CS_ERR_INVALID;
 }
 
@@ -432,10 +432,13 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
         set_error("cs_decode_stack: workspace is null or not 256-byte aligned");
         return CS_ERR_WORKSPACE;
     }
+    bool x_host = false;
+    st = io_kind(x, &x_host, who, "x");
+    if (st != CS_OK) return st;
     const int d = layers[0].d, f = layers[0].f, r = exact ? 1 : preds[0].r;
     StackPlan p;
     p.layers = layers; p.preds = preds; p.L = L; p.d = d; p.f = f; p.r = r;
-    p.x = x; p.scale = resid_scale; p.sel = *params; p.mode = mode;
+    p.scale = resid_scale; p.sel = *params; p.mode = mode;
     p.ws = static_cast<char *>(ws);
     p.lay = ws_layout(d, f, r, 1, device_sm_count());
     p.trace_count = trace_count; p.trace_idx = trace_idx;
@@ -443,14 +446,25 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
         set_error("cs_decode_stack: workspace too small: %zu bytes given, %zu needed", ws_bytes, p.lay.total);
         return CS_ERR_WORKSPACE;
     }
+    // a host x goes through the workspace's staging row, so the graph never
+    // names a host address
+    p.x = x_host ? reinterpret_cast<float *>(p.ws + p.lay.io_x) : x;
 
     cudaStream_t sm = (cudaStream_t)s_main;
     cudaStream_t sp = (cudaStream_t)s_pred;
+    const size_t x_bytes = sizeof(float) * (size_t)d;
+    if (x_host) {
+        cudaError_t e = cudaMemcpyAsync(p.x, x, x_bytes, cudaMemcpyHostToDevice, sm);
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(x copy in)");
+    }
     const bool two = mode == CS_STACK_LOOKAHEAD && !exact && sp && sp != sm;
-    return run_cached(p, sm, two ? sp : nullptr, who, [&]() {
+    st = run_cached(p, sm, two ? sp : nullptr, who, [&]() {
         Events E;
         return enqueue_stack(p, sm, two ? sp : sm, E);
     });
+    if (st != CS_OK || !x_host) return st;
+    cudaError_t e = cudaMemcpyAsync(x, p.x, x_bytes, cudaMemcpyDeviceToHost, sm);
+    return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_decode_stack(x copy out)");
 }
 
 cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, const float *x, float *y,
@@ -478,9 +492,9 @@ cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, c
         return CS_ERR_WORKSPACE;
     }
     bool x_host = false, y_host = false;
-    st = io_kind(x, &x_host, "x");
+    st = io_kind(x, &x_host, who, "x");
     if (st != CS_OK) return st;
-    st = io_kind(y, &y_host, "y");
+    st = io_kind(y, &y_host, who, "y");
     if (st != CS_OK) return st;
 
     const int d = layer->d, f = layer->f, r = exact ? 1 : pred->r;

@@ -264,14 +264,20 @@ cs_status cs_union_mask(const uint32_t *masks, int B, int f, uint32_t *umask, in
  *               on s_main.
  *   params->mode == CS_SEL_EXACT: A_l = {j : |act(g_j)| > params->tau} at x_l
  *               (g_j > 0 for relu at tau = 0); preds unused.
- *   x: [d] fp32 device, input x_0 and output x_L.
+ *   x: [d] fp32, input x_0 and output x_L: device memory, or page-locked
+ *      host memory (cudaHostAlloc, cudaHostRegister, torch pin_memory), which
+ *      is copied in and out through the workspace with asynchronous copies on
+ *      s_main (x holds x_L once s_main has passed this call).  Pageable host
+ *      memory is refused (CS_ERR_INVALID).
  *   layers, preds: host arrays of L structs (same d, f, r and dtype).
  *   trace_count: [L] int32 device or NULL; trace_idx: [L, f] int32 device or
  *   NULL -- per-layer selected counts and ascending ids.
  * The whole sequence is captured into a CUDA graph on the first call for a
  * given set of arguments and replayed afterwards (unless s_main is already
  * capturing, in which case the kernels are enqueued into the caller's
- * capture).  The workspace must hold cs_workspace_size(d, f, r, 1) bytes.
+ * capture); the copies of a host x run outside the graph, so its address may
+ * change from call to call without a new capture.  The workspace must hold
+ * cs_workspace_size(d, f, r, 1) bytes.
  */
 cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds, int L, float *x,
                           float resid_scale, const cs_select_params *params, cs_stack_mode mode,

@@ -91,3 +91,23 @@ def test_algorithmic_bytes_match_the_per_unit_accounting():
     Wa = bench.WORKLOADS["opt13b-attn-heads25"]
     ta, aa = bench.attn_bytes(Wa, 10)
     assert aa == 10 * 2 * (2 * 128 * 5120 + 2 * 2048 * 128) + 4 * 10 + 8 * 5120
+
+
+def test_stack_and_exact_bytes_match_the_per_unit_accounting():
+    """The LLaMA-70B-shaped stack moves 22.95 GB per token (80 layers of
+    75.50 MB of predictor and 4301 gated rows of 3 d e bytes); the exact-mask
+    step reads every gate row (f d e = 209.7 MB) plus the chosen down rows."""
+    import bench
+    import synth
+    W = bench.WORKLOADS["llama70b-stack-lookahead"]
+    k = synth.ceil_k(W["f"], W["share"])
+    assert k == 4301
+    total, ffn = bench.step_bytes(W, k)
+    assert ffn == k * (3 * 8192 * 2 + 8) + 8 * 8192
+    assert abs(2 * (1024 * 8192 + 28672 * 1024) - 75.50e6) < 0.01e6
+    assert abs(80 * total - 22.95e9) < 0.03e9
+    We = bench.WORKLOADS["opt13b-exact"]
+    te, fe = bench.step_bytes(We, 2048)
+    assert fe == 2048 * (5120 * 2 + 8) + 8 * 5120
+    assert te == 2 * 20480 * 5120 + 4 * (5120 + 20480) + 4 * 20480 + 4 * 2048 + fe
+    assert abs(te - 230.7e6) < 0.3e6

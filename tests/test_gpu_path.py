@@ -210,3 +210,29 @@ def test_stack_inside_caller_capture():
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(x.cpu().numpy().view(np.uint32), ref.cpu().numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("L", [3, 4])
+def test_stack_with_pinned_host_x(L):
+    """x_0 in page-locked host memory: copied in and x_L copied back by the
+    call; the result is the device-x call's, bit for bit, and several host
+    buffers replay one cached graph.  Pageable host memory is refused."""
+    d, f, r = 512, 2048, 64
+    Hs, layers, preds = stack_inputs(L, d, f, r, synth.BF16, glu=True)
+    ws = cs.Workspace(d, f, r)
+    sm, sp = torch.cuda.Stream(), torch.cuda.Stream()
+    params = cs.select_params(cs.CS_SEL_TOPK, 205)
+    for seed in (15, 16):
+        X = synth.x_normal(seed, 1, d)[0]
+        ref = torch.from_numpy(X.copy()).cuda()
+        torch.cuda.synchronize()
+        cs.cs_decode_stack(layers, preds, ref, 0.1, params, cs.CS_STACK_LOOKAHEAD, ws, s_main=sm, s_pred=sp)
+        sm.synchronize()
+        xh = torch.from_numpy(X.copy()).pin_memory()
+        cs.cs_decode_stack(layers, preds, xh, 0.1, params, cs.CS_STACK_LOOKAHEAD, ws, s_main=sm, s_pred=sp)
+        sm.synchronize()
+        assert np.array_equal(xh.numpy().view(np.uint32), ref.cpu().numpy().view(np.uint32))
+    with pytest.raises(cs.CsError):
+        cs.cs_decode_stack(layers, preds, torch.from_numpy(X.copy()), 0.1, params, cs.CS_STACK_LOOKAHEAD, ws,
+                           s_main=sm, s_pred=sp)
+    assert cs.cs_get_device_error(ws) == 0
