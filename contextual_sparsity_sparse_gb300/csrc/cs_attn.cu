@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_q_kernel(const AttnK a) {
         const float4 *xv = reinterpret_cast<const float4 *>(a.x + (size_t)v * V);
 #pragma unroll
         for (int e = 0; e < V; e += 4) {
-            const float4 x4 = __ldg(xv + e / 4);
+            const float4 x4 = ld_dep(xv + e / 4);
             acc = fmaf(w[e], x4.x, acc);
             acc = fmaf(w[e + 1], x4.y, acc);
             acc = fmaf(w[e + 2], x4.z, acc);

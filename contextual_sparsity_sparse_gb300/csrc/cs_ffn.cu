@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) ffn_gather_kernel(const FfnK a
     pdl_launch_dependents();  // one wave: the next kernel may get resident now
     pdl_wait();  // idx, count and x come from earlier kernels
 
-    int n = *a.count;
+    int n = ld_dep(a.count);
     if (n < 0 || n > a.f) {
         if (tid == 0 && c == 0 && blockIdx.y == 0) atomicOr(a.err, CS_DEVERR_COUNT);
         n = n < 0 ? 0 : a.f;
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) ffn_gather_kernel(const FfnK a
     const int n0 = (int)((long long)n * c / G);
     const int cnt = min(kChunkMax, (int)((long long)n * (c + 1) / G) - n0);
     // stage the chunk's ids so issuing copies never waits on a global load
-    for (int m = tid; m < cnt; m += nthr) s_idx[m] = __ldg(a.idx + n0 + m);
+    for (int m = tid; m < cnt; m += nthr) s_idx[m] = ld_dep(a.idx + n0 + m);
     __syncthreads();
     // the chunk's bias (or pre-activation) values, copied once
     {
@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) ffn_gather_kernel(const FfnK a
         for (int m = tid; m < cnt; m += nthr) {
             int j = s_idx[m];
             j = (j >= 0 && j < a.f) ? j : 0;
-            if (addsrc) cp4(smem_addr(&s_add[m]), addsrc + j);
+            if (PRE) s_add[m] = ld_dep(a.preact + j);  // written by the pre-activation kernel
+            else if (addsrc) cp4(smem_addr(&s_add[m]), addsrc + j);
             else s_add[m] = 0.f;
         }
     }
@@ -170,13 +171,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) ffn_gather_kernel(const FfnK a
             if (live && vok[i] && xvec && col0 + V <= a.d) {
 #pragma unroll
                 for (int e = 0; e < V; e += 4) {
-                    const float4 v4 = __ldg(reinterpret_cast<const float4 *>(xb + col0 + e));
+                    const float4 v4 = ld_dep(reinterpret_cast<const float4 *>(xb + col0 + e));
                     xr[t][i][e] = v4.x; xr[t][i][e + 1] = v4.y; xr[t][i][e + 2] = v4.z; xr[t][i][e + 3] = v4.w;
                 }
             } else {
 #pragma unroll
                 for (int e = 0; e < V; ++e)
-                    xr[t][i][e] = (live && vok[i] && col0 + e < a.d) ? __ldg(xb + col0 + e) : 0.f;
+                    xr[t][i][e] = (live && vok[i] && col0 + e < a.d) ? ld_dep(xb + col0 + e) : 0.f;
             }
         }
     }
@@ -343,12 +344,12 @@ ffn_reduce_kernel(const float *__restrict__ part, int G, int B, int d, int dp,
 #pragma unroll
         for (int u = 0; u < kRedUnroll; ++u) {
             const int c = warp + kRedWarps * u;
-            t[u] = c < G ? __ldg(reinterpret_cast<const float2 *>(p + c * stride)) : make_float2(0.f, 0.f);
+            t[u] = c < G ? ld_dep(reinterpret_cast<const float2 *>(p + c * stride)) : make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < kRedUnroll; ++u) { acc.x += t[u].x; acc.y += t[u].y; }
         for (int c = warp + kRedWarps * kRedUnroll; c < G; c += kRedWarps) {
-            const float2 v = __ldg(reinterpret_cast<const float2 *>(p + c * stride));
+            const float2 v = ld_dep(reinterpret_cast<const float2 *>(p + c * stride));
             acc.x += v.x;
             acc.y += v.y;
         }

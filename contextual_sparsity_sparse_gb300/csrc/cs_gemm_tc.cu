@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
     const int Q = U > 0 ? (int)(sk_start(c + 1, U, P) - u0) : 0;
     const bool bf = Tc<T>::kBf16;
     const uint32_t idesc = umma_idesc(bf, true, NP);
-    const int last = n > 0 ? __ldg(a.idx + n - 1) : 0;
+    const int last = n > 0 ? ld_dep(a.idx + n - 1) : 0;
     // unit cursors (column group, k-block): one division here, then +1 steps
     struct Cur {
         int g, kb;
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
 #pragma unroll
         for (int it = 0; it < kRowsPerThread; ++it) {
             const int p = kb * kKB + tid / kCh + it * (kTcThreads / kCh);
-            j[it] = (live && p < n) ? __ldg(a.idx + p) : last;
+            j[it] = (live && p < n) ? ld_dep(a.idx + p) : last;
         }
     };
     int jcur[kRowsPerThread], jnext[kRowsPerThread];

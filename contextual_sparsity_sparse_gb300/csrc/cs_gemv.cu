@@ -86,10 +86,10 @@ __global__ void __launch_bounds__(kThreads) stream_gemv_kernel(const GemvK a) {
             const float4 *src = reinterpret_cast<const float4 *>(a.v + (size_t)b * a.ncols);
 #pragma unroll 8
             for (int c = tid; c < ncp / 4; c += kThreads)
-                reinterpret_cast<float4 *>(dst)[c] = c * 4 < a.ncols ? __ldg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(dst)[c] = c * 4 < a.ncols ? ld_dep(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
             for (int c = tid; c < ncp; c += kThreads)
-                dst[c] = (b < a.B && c < a.ncols) ? __ldg(a.v + (size_t)b * a.ncols + c) : 0.f;
+                dst[c] = (b < a.B && c < a.ncols) ? ld_dep(a.v + (size_t)b * a.ncols + c) : 0.f;
         }
     }
     __syncthreads();
@@ -149,6 +149,136 @@ __global__ void __launch_bounds__(kThreads) stream_gemv_kernel(const GemvK a) {
     }
 }
 
+// One token (B = 1): weights streamed straight into registers with coalesced
+// 16-byte loads, v held in registers, no shared-memory staging.  A round is RU
+// rows; the first round's weights are loaded before waiting on the previous
+// kernel (they do not depend on it), and each round's loads are issued before
+// the previous round's reductions, so loads stay in flight across them.
+//   SPLIT = false (rows of at most 256 vectors): a warp per row, lane l takes
+//     vectors l + 32 i (i < NV); warp w's round takes RU consecutive rows.
+//   SPLIT = true (longer rows): every row is spread over the CTA, thread t
+//     takes vectors t + 256 i (i < NV); per round each warp sums its share of
+//     the RU rows, one barrier publishes the warp sums, and thread u adds row
+//     u's eight warp sums in warp order.
+// Each vector of a thread has its own accumulator, added in order at the end
+// of the row, so results are bit-reproducible.
+template <typename T, int EPI, bool SPLIT, int NV, int RU>
+__global__ void __launch_bounds__(kThreads) gemv_reg_kernel(const GemvK a) {
+    constexpr int V = Vec<T>::N;
+    __shared__ float red[2][SPLIT ? RU : 1][kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = blockIdx.x * a.rows_per_cta;
+    const int r1 = min(a.nrows, r0 + a.rows_per_cta);
+    const int nvec = (a.ncols * (int)sizeof(T) + 15) / 16;
+    const int per_round = SPLIT ? RU : kWarps * RU;
+    const int nround = r0 < r1 ? (r1 - r0 + per_round - 1) / per_round : 0;
+
+    int vv[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) vv[i] = SPLIT ? tid + i * kThreads : lane + 32 * i;
+    auto row_of = [&](int k, int u) { return SPLIT ? r0 + k * RU + u : r0 + (k * kWarps + warp) * RU + u; };
+
+    uint4 w[RU][NV];
+    auto load = [&](int k) {
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+            const int row = min(row_of(k, u), r1 - 1);   // rows past the block repeat its last
+            const uint4 *rp = reinterpret_cast<const uint4 *>(a.W + (size_t)row * a.ldb);
+#pragma unroll
+            for (int i = 0; i < NV; ++i) w[u][i] = vv[i] < nvec ? __ldg(rp + vv[i]) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    if (nround > 0) load(0);
+
+    pdl_launch_dependents();  // one wave: the next kernel may start its prologue
+    pdl_wait();               // v comes from the previous kernel
+
+    // this thread's slice of v (zero past ncols); weights past ncols in a
+    // row's last vector are zeroed in the dot product (row padding may hold
+    // anything)
+    float xr[NV][V];
+    int ne[NV];
+    const bool x4 = (reinterpret_cast<uintptr_t>(a.v) & 15) == 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c0 = vv[i] * V;
+        ne[i] = a.ncols - c0;
+        if (vv[i] < nvec && x4 && c0 + V <= a.ncols) {
+#pragma unroll
+            for (int e = 0; e < V; e += 4) {
+                const float4 t = ld_dep(reinterpret_cast<const float4 *>(a.v + c0 + e));
+                xr[i][e] = t.x; xr[i][e + 1] = t.y; xr[i][e + 2] = t.z; xr[i][e + 3] = t.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; ++e) xr[i][e] = (vv[i] < nvec && c0 + e < a.ncols) ? ld_dep(a.v + c0 + e) : 0.f;
+        }
+    }
+
+    for (int k = 0; k < nround; ++k) {
+        float part[RU];
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+            float acc[NV];
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                float f[V];
+                unpack<T>(w[u][i], f);
+                if (ne[i] < V) {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) f[e] = e < ne[i] ? f[e] : 0.f;
+                }
+                acc[i] = 0.f;
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[i] = fmaf(f[e], xr[i][e], acc[i]);
+            }
+            part[u] = acc[0];
+#pragma unroll
+            for (int i = 1; i < NV; ++i) part[u] += acc[i];
+        }
+        if (k + 1 < nround) load(k + 1);   // in flight during the reductions
+#pragma unroll
+        for (int u = 0; u < RU; ++u) part[u] = warp_sum(part[u]);
+        if (SPLIT) {
+            if (lane == 0) {
+#pragma unroll
+                for (int u = 0; u < RU; ++u) red[k & 1][u][warp] = part[u];
+            }
+            __syncthreads();
+            const int row = row_of(k, tid);
+            if (tid < RU && row < r1) {
+                float sum = 0.f;
+#pragma unroll
+                for (int q = 0; q < kWarps; ++q) sum += red[k & 1][tid][q];
+                if (EPI == EPI_RELU) sum = fmaxf(sum, 0.f);
+                if (EPI == EPI_BIAS && a.bias) sum += a.bias[row];
+                a.out[row] = sum;
+            }
+        } else if (lane == 0) {
+#pragma unroll
+            for (int u = 0; u < RU; ++u) {
+                const int row = row_of(k, u);
+                if (row < r1) {
+                    float sum = part[u];
+                    if (EPI == EPI_RELU) sum = fmaxf(sum, 0.f);
+                    if (EPI == EPI_BIAS && a.bias) sum += a.bias[row];
+                    a.out[row] = sum;
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int EPI, bool SPLIT, int NV, int RU>
+cudaError_t run_reg(const GemvK &k0, cudaStream_t s) {
+    GemvK k = k0;
+    int sms = device_sm_count();
+    sms = sms < 1 ? 1 : sms;
+    k.rows_per_cta = std::max(1, (k.nrows + 2 * sms - 1) / (2 * sms));   // two CTAs per SM
+    dim3 grid((k.nrows + k.rows_per_cta - 1) / k.rows_per_cta);
+    return launch(gemv_reg_kernel<T, EPI, SPLIT, NV, RU>, grid, dim3(kThreads), 0, s, pdl_enabled(), k);
+}
+
 template <typename T, int TB, int EPI>
 cudaError_t run_tb(const GemvK &k0, cudaStream_t s, size_t per_cta) {
     GemvK k = k0;
@@ -170,8 +300,24 @@ cudaError_t run_tb(const GemvK &k0, cudaStream_t s, size_t per_cta) {
     return launch(fn, grid, dim3(kThreads), smem, s, pdl_enabled(), k);
 }
 
+constexpr size_t kGemvCta = 110 * 1024;       // two CTAs per SM
+constexpr size_t kGemvCtaSmall = 60 * 1024;   // beside a gather CTA
+
 template <typename T, int EPI>
 cudaError_t run_gemv(const GemvK &k, cudaStream_t s, size_t per_cta) {
+    // one token, on the whole GPU: the register-streaming kernel (the small
+    // shared-memory shape, which runs beside a gather CTA, keeps the staged
+    // kernel: its CTAs need few registers)
+    const int nvec = (k.ncols * (int)sizeof(T) + 15) / 16;
+    if (k.B == 1 && per_cta == kGemvCta) {
+        if (nvec <= 32) return run_reg<T, EPI, false, 1, 4>(k, s);
+        if (nvec <= 64) return run_reg<T, EPI, false, 2, 4>(k, s);
+        if (nvec <= 128) return run_reg<T, EPI, false, 4, 4>(k, s);
+        if (nvec <= 256) return run_reg<T, EPI, false, 8, 2>(k, s);
+        if (nvec <= 512) return run_reg<T, EPI, true, 2, 4>(k, s);
+        if (nvec <= 1024) return run_reg<T, EPI, true, 4, 4>(k, s);
+        if (nvec <= 2048) return run_reg<T, EPI, true, 8, 2>(k, s);
+    }
     // tokens per CTA: as many as fit beside the weight buffers (weights are
     // re-streamed for each group of TB tokens)
     const size_t row_f = (size_t)((k.ncols + 7) & ~7) * 4;
@@ -180,8 +326,6 @@ cudaError_t run_gemv(const GemvK &k, cudaStream_t s, size_t per_cta) {
     return run_tb<T, 1, EPI>(k, s, per_cta);
 }
 
-constexpr size_t kGemvCta = 110 * 1024;       // two CTAs per SM
-constexpr size_t kGemvCtaSmall = 60 * 1024;   // beside a gather CTA
 
 template <int EPI>
 cudaError_t dispatch(cs_dtype dt, const GemvK &k, cudaStream_t s, size_t per_cta = kGemvCta) {

@@ -106,6 +106,18 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 
 // ----------------------------------------------------------------------------
+// Loads of data that an earlier kernel of the stream wrote (scores, index
+// lists, counts, activations, partial sums).  With programmatic dependent
+// launch this kernel may start before that kernel ends, so such loads must
+// stay after pdl_wait().  __ldg is a non-coherent load that the compiler may
+// treat as invariant and hoist above the wait (it did, once its loads were
+// fully unrolled); these are plain loads, which the wait's memory clobber
+// keeps after it.  Weights and other data that no kernel writes keep __ldg.
+// ----------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ T ld_dep(const T *p) { return *p; }
+
+// ----------------------------------------------------------------------------
 // mbarrier + bulk async copy (TMA engine, non-tensor form)
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

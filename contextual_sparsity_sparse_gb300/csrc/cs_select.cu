@@ -159,11 +159,11 @@ select_row_kernel(const float *__restrict__ scores, int f, int k, float tau,
 #pragma unroll
     for (int q = 0; q < ET; q += 4) {
         if (vec && q + 4 <= ne) {
-            const float4 t = __ldg(reinterpret_cast<const float4 *>(s + j0 + q));
+            const float4 t = ld_dep(reinterpret_cast<const float4 *>(s + j0 + q));
             v[q] = t.x; v[q + 1] = t.y; v[q + 2] = t.z; v[q + 3] = t.w;
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[q + e] = q + e < ne ? __ldg(s + j0 + q + e) : 0.f;
+            for (int e = 0; e < 4; ++e) v[q + e] = q + e < ne ? ld_dep(s + j0 + q + e) : 0.f;
         }
     }
 
@@ -451,11 +451,11 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
 #pragma unroll
     for (int q = 0; q < ET; q += 4) {
         if (vec && q + 4 <= ne) {
-            const float4 t = __ldg(reinterpret_cast<const float4 *>(s + beg + j0 + q));
+            const float4 t = ld_dep(reinterpret_cast<const float4 *>(s + beg + j0 + q));
             v[q] = t.x; v[q + 1] = t.y; v[q + 2] = t.z; v[q + 3] = t.w;
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[q + e] = q + e < ne ? __ldg(s + beg + j0 + q + e) : 0.f;
+            for (int e = 0; e < 4; ++e) v[q + e] = q + e < ne ? ld_dep(s + beg + j0 + q + e) : 0.f;
         }
     }
 
@@ -642,7 +642,7 @@ select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
                 if (tid < 256) S.rhist[tid] = 0u;
                 __syncthreads();
                 for (int j = tid; j < f; j += kClT) {
-                    const float x = __ldg(s + j);
+                    const float x = ld_dep(s + j);
                     if (bucket_fast(x, scale, off) == B_) {
                         const uint32_t key = score_key(x);
                         if ((key & pmask) == prefix) atomicAdd(&S.rhist[(key >> shift) & 255u], 1u);
