@@ -27,6 +27,7 @@
 // (One-dimensional bulk copies were measured slower for rows of ~10 KB: the
 // copy engine of an SM streams far below its share of HBM bandwidth.)
 #include <algorithm>
+#include <cstdlib>
 #include <utility>
 
 #include "cs_internal.cuh"
@@ -42,19 +43,6 @@ constexpr int kStageMax = 16;             // ring slots (ng * sg)
 constexpr size_t kRingBudget = 200 * 1024;
 constexpr int kChunkMax = 2048;           // ids per CTA (f <= kChunkMax * grid)
 
-struct FfnK {
-    const uint8_t *w_gate, *w_up, *w_down_t;
-    const float *bias, *x, *preact;
-    const int32_t *idx, *count;
-    float *part;
-    uint32_t *err;
-    int d, f, B, dp;
-    int ldb;        // row pitch in bytes
-    int nvec;       // 16-byte vectors per row
-    int ng;         // neurons per group
-    int sg;         // groups in the ring (2 or 3)
-    int act;        // the gate's activation (CS_ACT_*)
-};
 
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -392,6 +380,15 @@ cudaError_t pick_mode(const FfnArgs &a, const FfnK &k, size_t smem, cudaStream_t
     return pre ? pick_maxv<T, TB, false, true>(a, k, smem, s) : pick_maxv<T, TB, false, false>(a, k, smem, s);
 }
 
+// The specialised one-token gather (cs_ffn1.cu) is used unless CS_GATHER1=0.
+bool gather1_enabled() {
+    static const bool on = [] {
+        const char *v = getenv("CS_GATHER1");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+
 template <typename T>
 cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     const int esz = (int)sizeof(T);
@@ -430,7 +427,11 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     static_assert(3 * kNgMax <= kStageMax, "ring slots");
     const size_t smem = (size_t)k.ng * k.sg * per_neuron;
     const int tb = a.B >= 2 ? 2 : 1;
-    cudaError_t e = tb == 2 ? pick_mode<T, 2>(a, k, smem, s) : pick_mode<T, 1>(a, k, smem, s);
+    cudaError_t e;
+    if (gather1_applies(k, a.B) && gather1_enabled())
+        e = launch_gather1(a.dtype, k, smem, a.G, a.w_up != nullptr, a.preact != nullptr, s);
+    else
+        e = tb == 2 ? pick_mode<T, 2>(a, k, smem, s) : pick_mode<T, 1>(a, k, smem, s);
     if (e != cudaSuccess) return e;
     dim3 g((a.d + 63) / 64, a.B);
     return launch(ffn_reduce_kernel, g, dim3(kRedWarps * 32), 0, s, pdl_enabled(),

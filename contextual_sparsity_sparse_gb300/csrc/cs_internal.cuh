@@ -357,6 +357,24 @@ struct FfnArgs {
 };
 cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s);
 
+// Arguments of the gather kernels (one CTA per SM over a chunk of the list).
+struct FfnK {
+    const uint8_t *w_gate, *w_up, *w_down_t;
+    const float *bias, *x, *preact;
+    const int32_t *idx, *count;
+    float *part;
+    uint32_t *err;
+    int d, f, B, dp;
+    int ldb;        // row pitch in bytes
+    int nvec;       // 16-byte vectors per row
+    int ng;         // neurons per group
+    int sg;         // groups in the ring (2 or 3)
+    int act;        // the gate's activation (CS_ACT_*)
+};
+// The one-token gather with a compile-time group size (cs_ffn1.cu).
+bool gather1_applies(const FfnK &k, int B);
+cudaError_t launch_gather1(cs_dtype dt, const FfnK &k, size_t smem, int G, bool glu, bool pre, cudaStream_t s);
+
 // y[b, :] = (resid[b, :] + scale *) sum_{c < G} part[c, b, :], fixed order
 cudaError_t launch_ffn_reduce(const float *part, int G, int B, int d, int dp, const float *resid, float scale,
                               float *y, cudaStream_t s);
