@@ -13,18 +13,27 @@
 //     q = W_q[h] x,  s_i = q . k_i / sqrt(d_head),  p = softmax(s),
 //     o = sum_i p_i v_i,  y += W_o[:, h] o.
 //
-// GB300 mapping.  Grids span every head slot (the launch never depends on the
-// device-side count): slot m < count takes head idx[m], the others skip or
-// write zero partials.  The query kernel spreads each head's W_q rows over
-// (slot, 8-row block) CTAs, one warp per row.  The core kernel gives each
-// head (slot, column chunk) CTAs: each forms the scores of all S keys (one
-// thread per key), a max-subtracted softmax with fixed-order sums and o
-// (threads over (key residue, 16-byte channel vector) pairs, combined in a
-// fixed order),
-// then its chunk of W_o[:, h] o, four warp groups over the d_head rows added
-// in order.  The chunks of one head repeat the softmax; their K and V come
-// from L2 after the first.  The FFN's fixed-order reduction adds the H
-// partials, so y is bit-reproducible.
+// GB300 mapping: four kernels chained with programmatic dependent launch.
+// Grids span every head slot (the launch never depends on the device-side
+// count): slot m < count takes head idx[m], the others exit or write zero
+// partials.
+//  1. query: (slot, block of four W_q rows) CTAs; each row is spread over the
+//     CTA (thread t takes 16-byte vectors t + 256 i), x in registers, one
+//     block reduction per four rows.
+//  2. attend, split over the keys (flash-decoding): a (slot, split) CTA owns
+//     2048 / (vectors per key) keys, i.e. 32 KB of K and 32 KB of V, all of it
+//     loaded into registers before waiting for the query; it forms its
+//     scores, their maximum m, l = sum e^(s - m) and the unnormalised
+//     o = sum e^(s - m) v, and writes (m, l, o).
+//  3. combine and project: a (slot, 64-vector column chunk) CTA merges the
+//     head's splits in split order (M = max m, L = sum l e^(m - M),
+//     o = sum o_s e^(m - M) / L) and applies its chunk of W_o[:, h] o (four
+//     row groups added in order), the first rows loaded before the wait.
+//  4. the FFN's fixed-order reduction adds the per-slot partials.
+// Kernels 1-3 let their dependents launch only after their own wait, so when
+// kernels 2 and 3 start the selection that wrote the head list has finished
+// and they may read it, and fetch K, V and W_o rows, before their wait.  All
+// sums run in fixed orders, so y is bit-reproducible.
 #include <algorithm>
 
 #include "cs_internal.cuh"
@@ -36,15 +45,25 @@ namespace {
 constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kAttnMaxS = 16384;
+constexpr int kSplitVec = 2048;   // 16-byte vectors of K (and of V) per split: 8 per thread
+constexpr int kKV = kSplitVec / kAttnThreads;
+constexpr int kQRows = 4;         // W_q rows per query CTA
+constexpr int kOVec = 64;         // 16-byte column vectors of the output projection per CTA
+constexpr int kOGroups = kAttnThreads / kOVec;
+constexpr int kOPre = 4;          // W_o rows per thread loaded before the wait
 
 struct AttnK {
     const uint8_t *w_q, *w_o_t, *k, *v;
     const float *x;
     const int32_t *idx, *count;
-    float *part;    // [H, dp] per-head partial outputs
+    float *part;    // [H, dp] per-slot partial outputs
     float *qbuf;    // [H, dh] queries of the slots
+    float *split;   // [H, ns, dh + 2] per-split (m, l, o)
     uint32_t *err;
     int d, H, dh, S, dp;
+    int nvk;        // 16-byte vectors per key (and per W_q / W_o row block column)
+    int sc;         // keys per split
+    int ns;         // splits
     size_t row_bytes;   // d * element size
 };
 
@@ -54,19 +73,16 @@ __device__ __forceinline__ float warp_max_f(float v) {
     return v;
 }
 
-constexpr int kQRows = 8;       // query rows per CTA (one per warp)
-constexpr int kOVec = 64;       // 16-byte column vectors of the output projection per CTA
-constexpr int kOGroups = kAttnThreads / kOVec;
-
 // The head of slot m, or -1 (slot beyond the count, or an id out of range).
+// flag: this CTA reports a bad count or id in the error word.
 __device__ __forceinline__ int slot_head(const AttnK &a, int m, bool flag) {
-    int n = *a.count;
+    int n = ld_dep(a.count);
     if (n < 0 || n > a.H) {
         if (flag && m == 0 && threadIdx.x == 0) atomicOr(a.err, CS_DEVERR_COUNT);
         n = n < 0 ? 0 : a.H;
     }
     if (m >= n) return -1;
-    const int h = a.idx[m];
+    const int h = ld_dep(a.idx + m);
     if (h < 0 || h >= a.H) {
         if (flag && threadIdx.x == 0) atomicOr(a.err, CS_DEVERR_INDEX);
         return -1;
@@ -74,172 +90,266 @@ __device__ __forceinline__ int slot_head(const AttnK &a, int m, bool flag) {
     return h;
 }
 
-// 1. q of the head in slot m, rows p*8 .. p*8+7 (one warp per row, lanes over
-//    16-byte vectors of the row), scaled by 1/sqrt(d_head), into qbuf[m, :].
-template <typename T>
+// 1. rows r0 .. r0+3 of q for the head in slot m (scaled by 1/sqrt(d_head)).
+template <typename T, int NV>
 __global__ void __launch_bounds__(kAttnThreads) attn_q_kernel(const AttnK a) {
     constexpr int V = Vec<T>::N;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int m = blockIdx.x;
-    pdl_launch_dependents();
-    pdl_wait();  // the head list comes from the selection
+    __shared__ float red[kQRows][kAttnWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m = blockIdx.x, r0 = blockIdx.y * kQRows;
+    pdl_wait();               // the head list comes from the selection
+    pdl_launch_dependents();  // (after the wait: dependents may read the head list)
     const int h = slot_head(a, m, blockIdx.y == 0);
-    const int c = blockIdx.y * kQRows + warp;
-    if (h < 0 || c >= a.dh) return;
+    if (h < 0) return;
     const int nv = a.d / V;
-    const uint4 *row = reinterpret_cast<const uint4 *>(a.w_q + ((size_t)h * a.dh + c) * a.row_bytes);
-    float acc = 0.f;
-    for (int v = lane; v < nv; v += 32) {
-        float w[V];
-        unpack<T>(__ldg(row + v), w);
-        const float4 *xv = reinterpret_cast<const float4 *>(a.x + (size_t)v * V);
+    uint4 w[kQRows][NV];
 #pragma unroll
-        for (int e = 0; e < V; e += 4) {
-            const float4 x4 = ld_dep(xv + e / 4);
-            acc = fmaf(w[e], x4.x, acc);
-            acc = fmaf(w[e + 1], x4.y, acc);
-            acc = fmaf(w[e + 2], x4.z, acc);
-            acc = fmaf(w[e + 3], x4.w, acc);
+    for (int u = 0; u < kQRows; ++u) {
+        const int row = min(r0 + u, a.dh - 1);
+        const uint4 *rp = reinterpret_cast<const uint4 *>(a.w_q + ((size_t)h * a.dh + row) * a.row_bytes);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int v = tid + i * kAttnThreads;
+            w[u][i] = v < nv ? __ldg(rp + v) : make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) a.qbuf[(size_t)m * a.dh + c] = acc * (1.f / sqrtf((float)a.dh));
+    float xr[NV][V];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int v = tid + i * kAttnThreads;
+#pragma unroll
+        for (int e = 0; e < V; e += 4) {
+            const float4 t = v < nv ? ld_dep(reinterpret_cast<const float4 *>(a.x + (size_t)v * V + e))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            xr[i][e] = t.x; xr[i][e + 1] = t.y; xr[i][e + 2] = t.z; xr[i][e + 3] = t.w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kQRows; ++u) {
+        float acc[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            float f[V];
+            unpack<T>(w[u][i], f);
+            acc[i] = 0.f;
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[i] = fmaf(f[e], xr[i][e], acc[i]);
+        }
+        float t = acc[0];
+#pragma unroll
+        for (int i = 1; i < NV; ++i) t += acc[i];
+        t = warp_sum(t);
+        if (lane == 0) red[u][warp] = t;
+    }
+    __syncthreads();
+    if (tid < kQRows && r0 + tid < a.dh) {
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < kAttnWarps; ++q) t += red[tid][q];
+        a.qbuf[(size_t)m * a.dh + r0 + tid] = t * (1.f / sqrtf((float)a.dh));
+    }
 }
 
-// 2-5. For the head in slot m: scores of the S keys, softmax, o, and this
-//      CTA's chunk p of kOVec column vectors of the output projection.  Every
-//      chunk of a head repeats steps 2-4 (its K and V come from L2 after the
-//      first), so the output projection spreads over many SMs.
+// 2. split s of the keys of the head in slot m: (max, sum, unnormalised o).
+//    Thread t holds vectors e = t + 256 j (j < 8) of the split's K block and
+//    of its V block: key e / nvk, channel vector t % nvk (the same for every
+//    j, since nvk divides 256).
 template <typename T>
-__global__ void __launch_bounds__(kAttnThreads) attn_core_kernel(const AttnK a) {
+__global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const AttnK a) {
     constexpr int V = Vec<T>::N;
-    extern __shared__ __align__(16) float sm[];
-    const int dh = a.dh, d = a.d, S = a.S;
-    float *q = sm;                              // [dh]
-    float *o = q + dh;                          // [dh]
-    float *red = o + dh;                        // [kAttnThreads]
-    float *red5 = red + kAttnThreads;           // [kOGroups][kOVec][V]
-    float *s = red5 + kOGroups * kOVec * V;     // [S]
-    __shared__ float wred[kAttnWarps];
-    __shared__ float s_max, s_z;
+    __shared__ float sc[kSplitVec];               // the split's scores (at most 2048 keys)
+    __shared__ float red[kAttnWarps];
+    __shared__ float ored[kAttnThreads * V];      // [thread][channel] partial o
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int m = blockIdx.x, p = blockIdx.y;
-    const int nv = d / V;
-    const int v0 = p * kOVec, v1 = min(nv, v0 + kOVec);
-    float *part = a.part + (size_t)m * a.dp;
-
+    const int m = blockIdx.x, s = blockIdx.y;
+    const int nvk = a.nvk, u = tid % nvk;
+    const int k0 = s * a.sc;                      // first key of the split
+    const int nk = min(a.sc, a.S - k0);           // keys in the split
+    const int h = slot_head(a, m, false);         // the selection has finished (see above)
+    uint4 kr[kKV], vr[kKV];
+    if (h >= 0) {
+        const size_t head = (size_t)h * a.S * nvk;          // in vectors
+        const uint4 *kb = reinterpret_cast<const uint4 *>(a.k) + head + (size_t)k0 * nvk;
+        const uint4 *vb = reinterpret_cast<const uint4 *>(a.v) + head + (size_t)k0 * nvk;
+        const int nvec = nk * nvk;
+#pragma unroll
+        for (int j = 0; j < kKV; ++j) {
+            const int e = tid + j * kAttnThreads;
+            kr[j] = e < nvec ? __ldg(kb + e) : make_uint4(0u, 0u, 0u, 0u);
+            vr[j] = e < nvec ? __ldg(vb + e) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    pdl_wait();               // q comes from the query kernel
     pdl_launch_dependents();
-    pdl_wait();  // q comes from the query kernel
-    const int h = slot_head(a, m, false);
+    if (h < 0) return;
+    float qr[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) qr[e] = ld_dep(a.qbuf + (size_t)m * a.dh + u * V + e);
+
+    // scores: each key's nvk vectors lie in consecutive threads (nvk <= 32:
+    // one warp; nvk = 64: two warps, added through shared memory)
+    const int lpk = min(nvk, 32);
+#pragma unroll
+    for (int j = 0; j < kKV; ++j) {
+        float f[V];
+        unpack<T>(kr[j], f);
+        float t = 0.f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) t = fmaf(qr[e], f[e], t);
+        for (int o = lpk >> 1; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+        const int e = tid + j * kAttnThreads, key = e / nvk;
+        if (nvk <= 32) {
+            if ((lane & (lpk - 1)) == 0 && key < nk) sc[key] = t;
+        } else {
+            // nvk = 64: warps 2w and 2w + 1 hold the halves of one key
+            if (lane == 0) ored[warp + j * kAttnWarps] = t;
+        }
+    }
+    __syncthreads();
+    if (nvk > 32) {
+        // key (j, w2) of the 8 x 4 keys: halves from warps 2 w2 and 2 w2 + 1
+        if (tid < kKV * kAttnWarps / 2) {
+            const int j = tid / (kAttnWarps / 2), w2 = tid % (kAttnWarps / 2);
+            const int key = (j * kAttnThreads + w2 * 64) / 64;
+            if (key < nk) sc[key] = ored[2 * w2 + j * kAttnWarps] + ored[2 * w2 + 1 + j * kAttnWarps];
+        }
+        __syncthreads();
+    }
+    // the split's maximum and e^(s - m), summed in a fixed order
+    float mx = -INFINITY;
+    for (int i = tid; i < nk; i += kAttnThreads) mx = fmaxf(mx, sc[i]);
+    mx = warp_max_f(mx);
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int q = 1; q < kAttnWarps; ++q) mx = fmaxf(mx, red[q]);
+    __syncthreads();
+    float lz = 0.f;
+    for (int i = tid; i < nk; i += kAttnThreads) {
+        const float p = expf(sc[i] - mx);
+        sc[i] = p;
+        lz += p;
+    }
+    lz = warp_sum(lz);
+    if (lane == 0) red[warp] = lz;
+    __syncthreads();
+    // o: each thread adds its keys' p v over its channel vector, then the
+    // 256 / nvk threads of one channel vector are added in thread order
+    float acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kKV; ++j) {
+        const int key = (tid + j * kAttnThreads) / nvk;
+        const float p = key < nk ? sc[key] : 0.f;
+        float f[V];
+        unpack<T>(vr[j], f);
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(p, f[e], acc[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) ored[tid * V + e] = acc[e];
+    __syncthreads();
+    float *out = a.split + ((size_t)m * a.ns + s) * (a.dh + 2);
+    if (tid < a.dh) {
+        const int uu = tid / V, ee = tid % V;
+        float t = 0.f;
+        for (int g = uu; g < kAttnThreads; g += nvk) t += ored[g * V + ee];
+        out[2 + tid] = t;
+    }
+    if (tid == 0) {
+        float l = 0.f;
+#pragma unroll
+        for (int q = 0; q < kAttnWarps; ++q) l += red[q];
+        out[0] = mx;
+        out[1] = l;
+    }
+}
+
+// 3. merge the splits of the head in slot m, then columns [v0*V, v1*V) of
+//    its partial: group g sums rows c = g (mod 4), groups added in order.
+template <typename T>
+__global__ void __launch_bounds__(kAttnThreads) attn_out_kernel(const AttnK a) {
+    constexpr int V = Vec<T>::N;
+    __shared__ float o[256];
+    __shared__ float wgt[kAttnMaxS / 16 + 1];     // e^(m_s - M) per split
+    __shared__ float s_inv;
+    __shared__ float red5[kOGroups * kOVec * V];
+    const int tid = threadIdx.x;
+    const int m = blockIdx.x, p = blockIdx.y;
+    const int dh = a.dh, nv = a.d / V;
+    const int v0 = p * kOVec, v1 = min(nv, v0 + kOVec);
+    const int g = tid / kOVec, vl = tid % kOVec, v = v0 + vl;
+    float *part = a.part + (size_t)m * a.dp;
+    const int h = slot_head(a, m, false);         // the selection has finished
+    uint4 wpre[kOPre];
+    if (h >= 0 && v < v1) {
+#pragma unroll
+        for (int r = 0; r < kOPre; ++r) {
+            const int c = g + r * kOGroups;
+            wpre[r] = c < dh ? __ldg(reinterpret_cast<const uint4 *>(a.w_o_t + ((size_t)h * dh + c) * a.row_bytes) + v)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    pdl_wait();               // the splits come from the attend kernel
+    pdl_launch_dependents();
     if (h < 0) {
         for (int c = v0 * V + tid; c < v1 * V; c += kAttnThreads) part[c] = 0.f;
         return;
     }
-    for (int c = tid; c < dh; c += kAttnThreads) q[c] = a.qbuf[(size_t)m * dh + c];
-    __syncthreads();
-
-    // 2. scores and their maximum
-    const int kv = dh / V;
-    const size_t head_bytes = (size_t)S * dh * sizeof(T);
-    const uint8_t *kb = a.k + (size_t)h * head_bytes;
-    float lmax = -INFINITY;
-    for (int i = tid; i < S; i += kAttnThreads) {
-        const uint4 *kr = reinterpret_cast<const uint4 *>(kb + (size_t)i * dh * sizeof(T));
-        float acc = 0.f;
-        for (int v = 0; v < kv; ++v) {
-            float w[V];
-            unpack<T>(__ldg(kr + v), w);
-#pragma unroll
-            for (int e = 0; e < V; ++e) acc = fmaf(q[v * V + e], w[e], acc);
+    const float *sp = a.split + (size_t)m * a.ns * (dh + 2);
+    if (tid == 0) {
+        float M = -INFINITY;
+        for (int s = 0; s < a.ns; ++s) M = fmaxf(M, ld_dep(sp + (size_t)s * (dh + 2)));
+        float L = 0.f;
+        for (int s = 0; s < a.ns; ++s) {
+            const float w = expf(ld_dep(sp + (size_t)s * (dh + 2)) - M);
+            wgt[s] = w;
+            L += ld_dep(sp + (size_t)s * (dh + 2) + 1) * w;
         }
-        s[i] = acc;
-        lmax = fmaxf(lmax, acc);
-    }
-    lmax = warp_max_f(lmax);
-    if (lane == 0) wred[warp] = lmax;
-    __syncthreads();
-    if (warp == 0) {
-        float v = lane < kAttnWarps ? wred[lane] : -INFINITY;
-        v = warp_max_f(v);
-        if (lane == 0) s_max = v;
+        s_inv = 1.f / L;
     }
     __syncthreads();
-    const float mx = s_max;
-
-    // 3. p_i = e^(s_i - max) and their sum, in a fixed order
-    float lz = 0.f;
-    for (int i = tid; i < S; i += kAttnThreads) {
-        const float pe = expf(s[i] - mx);
-        s[i] = pe;
-        lz += pe;
-    }
-    lz = warp_sum(lz);
-    if (lane == 0) wred[warp] = lz;
-    __syncthreads();
-    if (warp == 0) {
-        float v = lane < kAttnWarps ? wred[lane] : 0.f;
-        v = warp_sum(v);
-        if (lane == 0) s_z = v;
+    if (tid < dh) {
+        float t = 0.f;
+        for (int s = 0; s < a.ns; ++s) t += ld_dep(sp + (size_t)s * (dh + 2) + 2 + tid) * wgt[s];
+        o[tid] = t * s_inv;
     }
     __syncthreads();
-    const float inv_z = 1.f / s_z;
-
-    // 4. o[c] = sum_i p_i v_i[c] / Z: thread (g, u) takes keys i = g (mod G)
-    //    and the 16-byte vector u of channels; the G groups are added in order
-    //    (d_head / V vectors per row, a power of two, so G * (d_head / V) = 256)
-    {
-        const int nvh = dh / V, G = kAttnThreads / nvh;
-        const int u = tid % nvh, g = tid / nvh;
-        const uint4 *vb = reinterpret_cast<const uint4 *>(a.v + (size_t)h * head_bytes);
-        float acc[V];
+    float acc[V];
 #pragma unroll
-        for (int e = 0; e < V; ++e) acc[e] = 0.f;
-        for (int i = g; i < S; i += G) {
-            float w[V];
-            unpack<T>(__ldg(vb + (size_t)i * nvh + u), w);
-            const float pi = s[i];
+    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+    if (v < v1) {
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = fmaf(pi, w[e], acc[e]);
-        }
-#pragma unroll
-        for (int e = 0; e < V; ++e) red5[(size_t)tid * V + e] = acc[e];   // [g][u][e]
-        __syncthreads();
-        if (tid < dh) {
-            const int uu = tid / V, ee = tid % V;
-            float t = 0.f;
-            for (int gg = 0; gg < G; ++gg) t += red5[((size_t)gg * nvh + uu) * V + ee];
-            o[tid] = t * inv_z;
-        }
-        __syncthreads();
-    }
-
-    // 5. columns [v0*V, v1*V) of this head's partial: group g sums rows
-    //    c = g (mod kOGroups), then the groups are added in order
-    {
-        const int g = tid / kOVec, vl = tid % kOVec, v = v0 + vl;
-        float acc[V];
-#pragma unroll
-        for (int e = 0; e < V; ++e) acc[e] = 0.f;
-        if (v < v1) {
-            for (int c = g; c < dh; c += kOGroups) {
-                const uint4 *row = reinterpret_cast<const uint4 *>(a.w_o_t + ((size_t)h * dh + c) * a.row_bytes);
-                float w[V];
-                unpack<T>(__ldg(row + v), w);
+        for (int r = 0; r < kOPre; ++r) {
+            const int c = g + r * kOGroups;
+            if (c < dh) {
+                float f[V];
+                unpack<T>(wpre[r], f);
                 const float oc = o[c];
 #pragma unroll
-                for (int e = 0; e < V; ++e) acc[e] = fmaf(oc, w[e], acc[e]);
+                for (int e = 0; e < V; ++e) acc[e] = fmaf(oc, f[e], acc[e]);
             }
         }
+        for (int c = g + kOPre * kOGroups; c < dh; c += kOGroups) {
+            float f[V];
+            unpack<T>(__ldg(reinterpret_cast<const uint4 *>(a.w_o_t + ((size_t)h * dh + c) * a.row_bytes) + v), f);
+            const float oc = o[c];
 #pragma unroll
-        for (int e = 0; e < V; ++e) red5[((size_t)g * kOVec + vl) * V + e] = acc[e];
-        __syncthreads();
-        if (g == 0 && v < v1) {
+            for (int e = 0; e < V; ++e) acc[e] = fmaf(oc, f[e], acc[e]);
+        }
+    }
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                float t = 0.f;
-                for (int gg = 0; gg < kOGroups; ++gg) t += red5[((size_t)gg * kOVec + vl) * V + e];
-                part[(size_t)v * V + e] = t;
-            }
+    for (int e = 0; e < V; ++e) red5[((size_t)g * kOVec + vl) * V + e] = acc[e];
+    __syncthreads();
+    if (g == 0 && v < v1) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            float t = 0.f;
+#pragma unroll
+            for (int gg = 0; gg < kOGroups; ++gg) t += red5[((size_t)gg * kOVec + vl) * V + e];
+            part[(size_t)v * V + e] = t;
         }
     }
 }
@@ -247,15 +357,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_core_kernel(const AttnK a) 
 template <typename T>
 cudaError_t run_attn(const AttnK &k, cudaStream_t s) {
     constexpr int V = Vec<T>::N;
-    cudaError_t e = launch(attn_q_kernel<T>, dim3(k.H, (k.dh + kQRows - 1) / kQRows), dim3(kAttnThreads), 0, s,
-                           pdl_enabled(), k);
-    if (e != cudaSuccess) return e;
-    const size_t smem = sizeof(float) * ((size_t)2 * k.dh + kAttnThreads + (size_t)kOGroups * kOVec * V + k.S);
-    auto fn = attn_core_kernel<T>;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     const int nv = k.d / V;
-    return launch(fn, dim3(k.H, (nv + kOVec - 1) / kOVec), dim3(kAttnThreads), smem, s, pdl_enabled(), k);
+    const dim3 gq(k.H, (k.dh + kQRows - 1) / kQRows);
+    cudaError_t e;
+    if (nv <= kAttnThreads) e = launch(attn_q_kernel<T, 1>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
+    else if (nv <= 2 * kAttnThreads) e = launch(attn_q_kernel<T, 2>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
+    else if (nv <= 4 * kAttnThreads) e = launch(attn_q_kernel<T, 4>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
+    else e = launch(attn_q_kernel<T, 8>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
+    if (e != cudaSuccess) return e;
+    e = launch(attn_split_kernel<T>, dim3(k.H, k.ns), dim3(kAttnThreads), 0, s, pdl_enabled(), k);
+    if (e != cudaSuccess) return e;
+    return launch(attn_out_kernel<T>, dim3(k.H, (nv + kOVec - 1) / kOVec), dim3(kAttnThreads), 0, s, pdl_enabled(),
+                  k);
 }
 
 }  // namespace
@@ -298,11 +411,17 @@ cs_status cs_sparse_attention(const cs_attn_layer *layer, const float *x, const 
         set_error("cs_sparse_attention: workspace too small: %zu bytes given, %zu needed", ws_bytes, WL.total);
         return CS_ERR_WORKSPACE;
     }
-    // H partial rows, then the H queries, inside the workspace's G partial rows
-    const size_t q_rows = ((size_t)L.n_heads * L.d_head + WL.dp - 1) / WL.dp;
-    if ((size_t)L.n_heads + q_rows > (size_t)WL.G) {
-        set_error("cs_sparse_attention: %d heads of %d need more than the %d partial rows of the workspace",
-                  L.n_heads, L.d_head, WL.G);
+    // inside the workspace's G partial rows: H partial rows, the H queries,
+    // then per head its splits' (max, sum, o)
+    const int nvk = L.d_head * esz / 16;
+    const int sc = kSplitVec / nvk;
+    const int ns = (seq_len + sc - 1) / sc;
+    const size_t need = (size_t)L.n_heads * WL.dp + (size_t)L.n_heads * L.d_head +
+                        (size_t)L.n_heads * ns * (L.d_head + 2);
+    if (need > (size_t)WL.G * WL.dp || L.d / V > 8 * kAttnThreads) {
+        set_error("cs_sparse_attention: %d heads of %d over %d positions (d=%d) need more than the %d x %d "
+                  "partial values of the workspace, or d is too wide", L.n_heads, L.d_head, seq_len, L.d, WL.G,
+                  WL.dp);
         return CS_ERR_UNSUPPORTED;
     }
     AttnK k;
@@ -315,6 +434,10 @@ cs_status cs_sparse_attention(const cs_attn_layer *layer, const float *x, const 
     k.count = count;
     k.part = reinterpret_cast<float *>(static_cast<char *>(ws) + WL.part);
     k.qbuf = k.part + (size_t)L.n_heads * WL.dp;
+    k.split = k.qbuf + (size_t)L.n_heads * L.d_head;
+    k.nvk = nvk;
+    k.sc = sc;
+    k.ns = ns;
     k.err = static_cast<uint32_t *>(ws);
     k.d = L.d;
     k.H = L.n_heads;
