@@ -273,7 +273,8 @@ template <typename T>
 __global__ void __launch_bounds__(kAttnThreads) attn_out_kernel(const AttnK a) {
     constexpr int V = Vec<T>::N;
     __shared__ float o[256];
-    __shared__ float wgt[kAttnMaxS / 16 + 1];     // e^(m_s - M) per split
+    __shared__ float wgt[kAttnMaxS / 32];         // m_s, then e^(m_s - M), per split
+    __shared__ float lsum[kAttnMaxS / 32];        // l_s per split
     __shared__ float s_inv;
     __shared__ float red5[kOGroups * kOVec * V];
     const int tid = threadIdx.x;
@@ -299,14 +300,21 @@ __global__ void __launch_bounds__(kAttnThreads) attn_out_kernel(const AttnK a) {
         return;
     }
     const float *sp = a.split + (size_t)m * a.ns * (dh + 2);
+    // the splits' maxima and sums, one thread per split, then M and L by warp
+    // 0 in split order
+    for (int s = tid; s < a.ns; s += kAttnThreads) {
+        wgt[s] = ld_dep(sp + (size_t)s * (dh + 2));
+        lsum[s] = ld_dep(sp + (size_t)s * (dh + 2) + 1);
+    }
+    __syncthreads();
     if (tid == 0) {
         float M = -INFINITY;
-        for (int s = 0; s < a.ns; ++s) M = fmaxf(M, ld_dep(sp + (size_t)s * (dh + 2)));
+        for (int s = 0; s < a.ns; ++s) M = fmaxf(M, wgt[s]);
         float L = 0.f;
         for (int s = 0; s < a.ns; ++s) {
-            const float w = expf(ld_dep(sp + (size_t)s * (dh + 2)) - M);
+            const float w = expf(wgt[s] - M);
             wgt[s] = w;
-            L += ld_dep(sp + (size_t)s * (dh + 2) + 1) * w;
+            L += lsum[s] * w;
         }
         s_inv = 1.f / L;
     }
@@ -332,12 +340,27 @@ __global__ void __launch_bounds__(kAttnThreads) attn_out_kernel(const AttnK a) {
                 for (int e = 0; e < V; ++e) acc[e] = fmaf(oc, f[e], acc[e]);
             }
         }
-        for (int c = g + kOPre * kOGroups; c < dh; c += kOGroups) {
-            float f[V];
-            unpack<T>(__ldg(reinterpret_cast<const uint4 *>(a.w_o_t + ((size_t)h * dh + c) * a.row_bytes) + v), f);
-            const float oc = o[c];
+        // the remaining rows eight at a time, all eight loads in flight
+        const uint4 *col = reinterpret_cast<const uint4 *>(a.w_o_t + (size_t)h * dh * a.row_bytes) + v;
+        const size_t rstride = a.row_bytes / 16;
+        for (int c0 = g + kOPre * kOGroups; c0 < dh; c0 += 8 * kOGroups) {
+            uint4 wr[8];
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = fmaf(oc, f[e], acc[e]);
+            for (int r = 0; r < 8; ++r) {
+                const int c = c0 + r * kOGroups;
+                wr[r] = c < dh ? __ldg(col + (size_t)c * rstride) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int c = c0 + r * kOGroups;
+                if (c < dh) {
+                    float f[V];
+                    unpack<T>(wr[r], f);
+                    const float oc = o[c];
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[e] = fmaf(oc, f[e], acc[e]);
+                }
+            }
         }
     }
 #pragma unroll
