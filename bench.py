@@ -262,14 +262,15 @@ def src_sha(path):
 
 
 def profile_traffic(kernel, workload):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source
-    is unchanged since the capture; else None."""
+    """DRAM bytes per launch from a committed ncu summary, if every kernel
+    source it was captured on is unchanged since; else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             t = json.load(fh)
         e = t[kernel][workload]
-        if e["source_sha"] != src_sha(os.path.join(ROOT, e["source"])):
-            return None
+        for path, sha in e["sources"].items():
+            if sha != src_sha(os.path.join(ROOT, path)):
+                return None
         return e["traffic_bytes"]
     except Exception:
         return None
@@ -1102,7 +1103,8 @@ def run_attn(args, W, rank, world):
         "roofline": {"bound": "hbm", "kernel": "cs_sparse_attention (per-head attention + fixed-order reduce)",
                      "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
-                     "bytes_per_launch": attn_b, "avg_launch_us": attn_avg_s * 1e6, "traffic": None},
+                     "bytes_per_launch": attn_b, "avg_launch_us": attn_avg_s * 1e6,
+                     "traffic": profile_traffic("cs_sparse_attention", args.workload)},
         "step_roofline": {"bytes_per_step": total_b, "achieved": total_b / step_s / 1e9, "peak": hbm,
                           "frac": total_b / step_s / 1e9 / hbm, "unit": "GB/s"},
         "e2e": {"value": world * KE / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * d,
