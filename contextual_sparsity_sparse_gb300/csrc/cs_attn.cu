@@ -96,10 +96,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_q_kernel(const AttnK a) {
     constexpr int V = Vec<T>::N;
     __shared__ float red[kQRows][kAttnWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int m = blockIdx.x, r0 = blockIdx.y * kQRows;
+    const int m = blockIdx.y, r0 = blockIdx.x * kQRows;
     pdl_wait();               // the head list comes from the selection
     pdl_launch_dependents();  // (after the wait: dependents may read the head list)
-    const int h = slot_head(a, m, blockIdx.y == 0);
+    const int h = slot_head(a, m, blockIdx.x == 0);
     if (h < 0) return;
     const int nv = a.d / V;
     uint4 w[kQRows][NV];
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const AttnK a)
     __shared__ float red[kAttnWarps];
     __shared__ float ored[kAttnThreads * V];      // [thread][channel] partial o
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int m = blockIdx.x, s = blockIdx.y;
+    const int m = blockIdx.y, s = blockIdx.x;
     const int nvk = a.nvk, u = tid % nvk;
     const int k0 = s * a.sc;                      // first key of the split
     const int nk = min(a.sc, a.S - k0);           // keys in the split
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_out_kernel(const AttnK a) {
     __shared__ float s_inv;
     __shared__ float red5[kOGroups * kOVec * V];
     const int tid = threadIdx.x;
-    const int m = blockIdx.x, p = blockIdx.y;
+    const int m = blockIdx.y, p = blockIdx.x;
     const int dh = a.dh, nv = a.d / V;
     const int v0 = p * kOVec, v1 = min(nv, v0 + kOVec);
     const int g = tid / kOVec, vl = tid % kOVec, v = v0 + vl;
@@ -381,16 +381,18 @@ template <typename T>
 cudaError_t run_attn(const AttnK &k, cudaStream_t s) {
     constexpr int V = Vec<T>::N;
     const int nv = k.d / V;
-    const dim3 gq(k.H, (k.dh + kQRows - 1) / kQRows);
+    // slot in y: the launch order runs through every CTA of slot 0 first, so
+    // the CTAs of the count selected slots come first and fill the first wave
+    const dim3 gq((k.dh + kQRows - 1) / kQRows, k.H);
     cudaError_t e;
     if (nv <= kAttnThreads) e = launch(attn_q_kernel<T, 1>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     else if (nv <= 2 * kAttnThreads) e = launch(attn_q_kernel<T, 2>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     else if (nv <= 4 * kAttnThreads) e = launch(attn_q_kernel<T, 4>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     else e = launch(attn_q_kernel<T, 8>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     if (e != cudaSuccess) return e;
-    e = launch(attn_split_kernel<T>, dim3(k.H, k.ns), dim3(kAttnThreads), 0, s, pdl_enabled(), k);
+    e = launch(attn_split_kernel<T>, dim3(k.ns, k.H), dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     if (e != cudaSuccess) return e;
-    return launch(attn_out_kernel<T>, dim3(k.H, (nv + kOVec - 1) / kOVec), dim3(kAttnThreads), 0, s, pdl_enabled(),
+    return launch(attn_out_kernel<T>, dim3((nv + kOVec - 1) / kOVec, k.H), dim3(kAttnThreads), 0, s, pdl_enabled(),
                   k);
 }
 
@@ -472,7 +474,9 @@ cs_status cs_sparse_attention(const cs_attn_layer *layer, const float *x, const 
     cudaError_t e = L.dtype == CS_F32 ? run_attn<float>(k, s)
                     : L.dtype == CS_F16 ? run_attn<__half>(k, s)
                                         : run_attn<__nv_bfloat16>(k, s);
-    if (e == cudaSuccess) e = launch_ffn_reduce(k.part, L.n_heads, 1, L.d, WL.dp, nullptr, 1.f, y, s);
+    // the reduction adds the partial rows of the selected slots only (the
+    // count is read on the device and clamped to the head count)
+    if (e == cudaSuccess) e = launch_ffn_reduce(k.part, L.n_heads, 1, L.d, WL.dp, nullptr, 1.f, y, s, count);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_sparse_attention");
 }
 

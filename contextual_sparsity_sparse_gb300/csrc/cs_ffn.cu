@@ -314,15 +314,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) ffn_gather_kernel(const FfnK a
 constexpr int kRedWarps = 16;
 constexpr int kRedUnroll = 16;   // partials per warp kept in flight (G <= 256 in one pass)
 
+// gcount (optional, device): only the first min(G, *gcount) partials are
+// added (the rest are known to be zero).
 __global__ void __launch_bounds__(kRedWarps * 32)
-ffn_reduce_kernel(const float *__restrict__ part, int G, int B, int d, int dp,
-                  const float *__restrict__ resid, float scale, float *__restrict__ y) {
+ffn_reduce_kernel(const float *part, int G, int B, int d, int dp,
+                  const float *resid, float scale, float *__restrict__ y, const int32_t *gcount) {
     __shared__ float2 red[kRedWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int col = blockIdx.x * 64 + 2 * lane;
     const int b = blockIdx.y;
     pdl_launch_dependents();
     pdl_wait();
+    if (gcount) {
+        const int n = ld_dep(gcount);
+        G = n < 0 ? 0 : n < G ? n : G;
+    }
     float2 acc = make_float2(0.f, 0.f);
     if (col < d) {
         // col + 1 < dp (dp is a multiple of 8), so the pair load stays inside the row
@@ -413,10 +419,7 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     const int nrow = (a.preact ? 0 : 1) + (a.w_up ? 1 : 0) + 1;
     const size_t per_neuron = (size_t)nrow * k.nvec * 16;
     // ring of sg groups of ng neurons: as deep as the budget allows
-    const size_t budget = a.ring_bytes ? std::min(a.ring_bytes, kRingBudget) : kRingBudget;
-    int nst = (int)(budget / per_neuron);
-    // a reduced ring keeps at least two neurons
-    if (a.ring_bytes && nst < 2) nst = 2;
+    const int nst = (int)(kRingBudget / per_neuron);
     if (nst < 2) return cudaErrorInvalidValue;
     // three ring groups keep one group in flight while two are in use
     if (nst >= 3 * kNgMax) { k.ng = kNgMax; k.sg = 3; }
@@ -435,7 +438,8 @@ cudaError_t run_ffn(const FfnArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     dim3 g((a.d + 63) / 64, a.B);
     return launch(ffn_reduce_kernel, g, dim3(kRedWarps * 32), 0, s, pdl_enabled(),
-                  static_cast<const float *>(a.part), a.G, a.B, a.d, a.dp, a.resid, a.scale, a.y);
+                  static_cast<const float *>(a.part), a.G, a.B, a.d, a.dp, a.resid, a.scale, a.y,
+                  static_cast<const int32_t *>(nullptr));
 }
 
 }  // namespace
@@ -447,9 +451,10 @@ int ffn_max_d(cs_dtype t) {
 }
 
 cudaError_t launch_ffn_reduce(const float *part, int G, int B, int d, int dp, const float *resid, float scale,
-                              float *y, cudaStream_t s) {
+                              float *y, cudaStream_t s, const int32_t *gcount) {
     dim3 g((d + 63) / 64, B);
-    return launch(ffn_reduce_kernel, g, dim3(kRedWarps * 32), 0, s, pdl_enabled(), part, G, B, d, dp, resid, scale, y);
+    return launch(ffn_reduce_kernel, g, dim3(kRedWarps * 32), 0, s, pdl_enabled(), part, G, B, d, dp, resid, scale, y,
+                  gcount);
 }
 
 cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s) {

@@ -301,15 +301,12 @@ cudaError_t run_tb(const GemvK &k0, cudaStream_t s, size_t per_cta) {
 }
 
 constexpr size_t kGemvCta = 110 * 1024;       // two CTAs per SM
-constexpr size_t kGemvCtaSmall = 60 * 1024;   // beside a gather CTA
 
 template <typename T, int EPI>
 cudaError_t run_gemv(const GemvK &k, cudaStream_t s, size_t per_cta) {
-    // one token, on the whole GPU: the register-streaming kernel (the small
-    // shared-memory shape, which runs beside a gather CTA, keeps the staged
-    // kernel: its CTAs need few registers)
+    // one token: the register-streaming kernel
     const int nvec = (k.ncols * (int)sizeof(T) + 15) / 16;
-    if (k.B == 1 && per_cta == kGemvCta) {
+    if (k.B == 1) {
         if (nvec <= 32) return run_reg<T, EPI, false, 1, 4>(k, s);
         if (nvec <= 64) return run_reg<T, EPI, false, 2, 4>(k, s);
         if (nvec <= 128) return run_reg<T, EPI, false, 4, 4>(k, s);
@@ -350,8 +347,7 @@ cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s) {
     k.B = a.B;
     k.out = a.h;
     k.err = a.err;
-    const size_t per_cta = a.small_smem ? kGemvCtaSmall : kGemvCta;
-    cudaError_t e = dispatch<EPI_RELU>(a.dtype, k, s, per_cta);
+    cudaError_t e = dispatch<EPI_RELU>(a.dtype, k, s);
     if (e != cudaSuccess) return e;
     // P2: s[b, j] = sum_i P_up[j, i] h[b, i]
     k.W = static_cast<const uint8_t *>(a.p_up);
@@ -360,7 +356,7 @@ cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s) {
     k.nrows = a.f;
     k.v = a.h;
     k.out = a.scores;
-    return dispatch<EPI_NONE>(a.dtype, k, s, per_cta);
+    return dispatch<EPI_NONE>(a.dtype, k, s);
 }
 
 cudaError_t launch_gemv_batch(cs_dtype dt, const void *W, int ldb_bytes, int ncols, int nrows, const float *v,

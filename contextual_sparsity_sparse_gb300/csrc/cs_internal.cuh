@@ -112,7 +112,9 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // stay after pdl_wait().  __ldg is a non-coherent load that the compiler may
 // treat as invariant and hoist above the wait (it did, once its loads were
 // fully unrolled); these are plain loads, which the wait's memory clobber
-// keeps after it.  Weights and other data that no kernel writes keep __ldg.
+// keeps after it (the pointers they read through are not __restrict__, which
+// would let the compiler treat them as read-only in the same way).  Weights
+// and other data that no kernel writes keep __ldg.
 // ----------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ T ld_dep(const T *p) { return *p; }
@@ -308,7 +310,6 @@ struct PredictArgs {
     float *h;      // [B, r]
     float *scores; // [B, f]
     uint32_t *err = nullptr;
-    bool small_smem = false;  // ~60 KB per CTA, to share SMs with a gather CTA
 };
 cudaError_t launch_predict(const PredictArgs &a, cudaStream_t s);
 // out[b, row] = epi(sum_c W[row, c] v[b, c]) for rows < nrows and B tokens of
@@ -351,7 +352,6 @@ struct FfnArgs {
     float *part;            // workspace partials
     int G, dp;
     int act = CS_ACT_RELU;  // the gate's activation
-    size_t ring_bytes = 0;  // gather ring budget; 0 = the default (most of an SM's shared memory)
     void *tc_x = nullptr;   // tensor-core path: [NP, d] split activations (or null)
     void *tc_a = nullptr;   // tensor-core path: [NP, roundup(f, 128)] split activations (or null)
 };
@@ -375,9 +375,10 @@ struct FfnK {
 bool gather1_applies(const FfnK &k, int B);
 cudaError_t launch_gather1(cs_dtype dt, const FfnK &k, size_t smem, int G, bool glu, bool pre, cudaStream_t s);
 
-// y[b, :] = (resid[b, :] + scale *) sum_{c < G} part[c, b, :], fixed order
+// y[b, :] = (resid[b, :] + scale *) sum_{c < G'} part[c, b, :], fixed order;
+// G' = G, or min(G, *gcount) when gcount (device) is given
 cudaError_t launch_ffn_reduce(const float *part, int G, int B, int d, int dp, const float *resid, float scale,
-                              float *y, cudaStream_t s);
+                              float *y, cudaStream_t s, const int32_t *gcount = nullptr);
 
 // Tensor-core (tcgen05) batched path for dense unions: fp16 / bf16 weights,
 // d a multiple of 64, 2 <= B <= kTcMaxB.

@@ -124,7 +124,7 @@ __device__ __forceinline__ void rank_flags(float s, float pv, bool pnan, bool &g
 
 template <int ET, int KIND>
 __global__ void __launch_bounds__(kRowThreads, 1)
-select_row_kernel(const float *__restrict__ scores, int f, int k, float tau,
+select_row_kernel(const float *scores, int f, int k, float tau,
                   int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
                   uint32_t *__restrict__ mask, int hot) {
     __shared__ __align__(16) uint32_t hist[kBuckets];
@@ -415,7 +415,7 @@ __device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t *wsum, ui
 
 template <int ET, int KIND>
 __global__ void __launch_bounds__(kClT, 1)
-select_cl_kernel(const float *__restrict__ scores, int f, int k, float tau,
+select_cl_kernel(const float *scores, int f, int k, float tau,
                  int32_t *__restrict__ idx, int ld_idx, int32_t *__restrict__ count,
                  uint32_t *__restrict__ mask, int hot) {
     namespace cg = cooperative_groups;

@@ -18,6 +18,7 @@
 // (predictor, selection, gathered FFN; y without the residual): its five
 // kernels become one cached graph, and x / y in page-locked host memory are
 // staged through the workspace by copies issued around the graph launch.
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -82,16 +83,12 @@ void sel_out(const StackPlan &p, const Bufs &b, int l, int32_t **idx, int32_t **
     else *cnt = b.cnt_slot[l & 1];
 }
 
-// shared: the predictor runs beside the gather kernel of the other stream, so
-// its CTAs take a smaller share of shared memory
-cudaError_t predict_select(const StackPlan &p, const Bufs &b, int l, const float *xin, cudaStream_t s,
-                           bool shared = false) {
+cudaError_t predict_select(const StackPlan &p, const Bufs &b, int l, const float *xin, cudaStream_t s) {
     const cs_predictor &P = p.preds[l];
     PredictArgs a;
     a.d = P.d; a.r = P.r; a.f = P.f; a.B = 1; a.dtype = P.dtype;
     a.ld_down = P.ld_down; a.ld_up = P.ld_up; a.p_down = P.p_down; a.p_up = P.p_up;
     a.x = xin; a.h = b.h; a.scores = b.scores; a.err = b.err;
-    a.small_smem = shared;
     cudaError_t e = launch_predict(a, s);
     if (e != cudaSuccess) return e;
     // the predictor scores neurons hot .. f-1; the selection adds 0 .. hot-1
@@ -104,24 +101,8 @@ cudaError_t predict_select(const StackPlan &p, const Bufs &b, int l, const float
     return launch_select(sa, s);
 }
 
-// In the two-stream pipeline the gather kernel of layer l and the predictor of
-// layer l+1 run at the same time.  When three neurons' rows fit in 96 KB, the
-// gather takes an 88 KB ring and the predictor ~60 KB CTAs, so that both have
-// a CTA on every SM and stream from HBM together (measured +4.5% tokens/s on
-// the 48-layer d=7168 stack).  Wider rows keep the full ring and the default
-// predictor (measured: sharing slowed the d=8192 gated stack by 7%).
-constexpr size_t kSharedRing = 88 * 1024;
-bool share_sms(const cs_ffn_layer &Ly) {
-    const size_t es = dtype_size(Ly.dtype);
-    const size_t rows = (Ly.w_up ? 3 : 2);
-    const size_t per_neuron = rows * (((size_t)Ly.d * es + 15) / 16 * 16);
-    return 3 * per_neuron <= 96 * 1024;
-}
-
-// shared: the FFN shares the GPU with the predictor on the second stream, so its
-// ring leaves room on every SM for one predictor CTA
 cudaError_t ffn_step(const StackPlan &p, const Bufs &b, int l, const float *xin, float *xout,
-                     const float *preact, cudaStream_t s, bool shared = false) {
+                     const float *preact, cudaStream_t s) {
     const cs_ffn_layer &Ly = p.layers[l];
     FfnArgs a;
     a.d = Ly.d; a.f = Ly.f; a.ld = Ly.ld ? Ly.ld : Ly.d; a.B = 1; a.dtype = Ly.dtype;
@@ -136,7 +117,6 @@ cudaError_t ffn_step(const StackPlan &p, const Bufs &b, int l, const float *xin,
     a.resid = p.layer_only ? nullptr : xin;
     a.scale = p.layer_only ? 1.f : p.scale;
     a.err = b.err; a.part = b.part; a.G = p.lay.G; a.dp = p.lay.dp;
-    if (shared) a.ring_bytes = kSharedRing;
     return launch_ffn(a, s);
 }
 
@@ -208,16 +188,16 @@ cudaError_t enqueue_stack(const StackPlan &p, cudaStream_t sm, cudaStream_t sp, 
         auto ev_x = [&](int l) { return E.ev[2 + L + l]; };
         TRY(cudaEventRecord(ev_fork, sm));
         TRY(cudaStreamWaitEvent(sp, ev_fork, 0));
-        TRY(predict_select(p, b, 0, b.xb[0], sp, share_sms(p.layers[0])));
+        TRY(predict_select(p, b, 0, b.xb[0], sp));
         TRY(cudaEventRecord(ev_sel(0), sp));
         for (int l = 0; l < L; ++l) {
             if (l + 1 < L) {
                 if (l > 0) TRY(cudaStreamWaitEvent(sp, ev_x(l), 0));
-                TRY(predict_select(p, b, l + 1, b.xb[l & 1], sp, share_sms(p.layers[l + 1])));
+                TRY(predict_select(p, b, l + 1, b.xb[l & 1], sp));
                 TRY(cudaEventRecord(ev_sel(l + 1), sp));
             }
             TRY(cudaStreamWaitEvent(sm, ev_sel(l), 0));
-            TRY(ffn_step(p, b, l, b.xb[l & 1], b.xb[(l + 1) & 1], nullptr, sm, share_sms(p.layers[l])));
+            TRY(ffn_step(p, b, l, b.xb[l & 1], b.xb[(l + 1) & 1], nullptr, sm));
             TRY(cudaEventRecord(ev_x(l + 1), sm));
         }
         TRY(cudaEventRecord(ev_join, sp));

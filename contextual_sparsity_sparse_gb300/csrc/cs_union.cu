@@ -3,8 +3,8 @@
 // Union source: "Contextual Sparsity and Activation Predictors", section "When
 // it breaks": the tokens of a batch have different active sets and the layer
 // must read their union.  umask = OR over tokens; uidx = set bits ascending.
-// One CTA: each thread ORs a contiguous run of words, a block scan places the
-// run's ids.
+// One CTA: each thread ORs a contiguous run of words (kept in registers when
+// it holds at most four), a block scan places the run's ids.
 //
 // Packer source: "Contextual Sparsity: Activation-Aware LLM Inference and the
 // Deja Vu Paradigm", section "Kernel-Level Implementation" (indexing into the
@@ -19,9 +19,25 @@ namespace cs {
 namespace {
 
 constexpr int kUnionThreads = 1024;
+constexpr int kUnionWords = 4;   // words per thread kept in registers (f <= 131072)
+
+// OR of word w over the B masks, eight loads in flight at a time.
+__device__ __forceinline__ uint32_t or_word(const uint32_t *masks, int B, int words, int w) {
+    uint32_t acc = 0;
+    int b = 0;
+    for (; b + 8 <= B; b += 8) {
+        uint32_t t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = ld_dep(masks + (size_t)(b + i) * words + w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc |= t[i];
+    }
+    for (; b < B; ++b) acc |= ld_dep(masks + (size_t)b * words + w);
+    return acc;
+}
 
 __global__ void __launch_bounds__(kUnionThreads)
-union_kernel(const uint32_t *__restrict__ masks, int B, int f, uint32_t *__restrict__ umask,
+union_kernel(const uint32_t *masks, int B, int f, uint32_t *__restrict__ umask,
              int32_t *__restrict__ uidx, int32_t *__restrict__ ucount) {
     __shared__ int wsum[32];
     const int tid = threadIdx.x;
@@ -29,19 +45,50 @@ union_kernel(const uint32_t *__restrict__ masks, int B, int f, uint32_t *__restr
     const int E = (words + kUnionThreads - 1) / kUnionThreads;
     const int beg = min(tid * E, words), end = min(beg + E, words);
     const uint32_t tail = (f & 31) ? ((1u << (f & 31)) - 1u) : 0xffffffffu;
+    pdl_launch_dependents();
     pdl_wait();
+    if (E <= kUnionWords) {
+        // one pass: this thread's words stay in registers between the count
+        // and the writes
+        uint32_t u[kUnionWords];
+        int n = 0;
+#pragma unroll
+        for (int e = 0; e < kUnionWords; ++e) {
+            const int w = beg + e;
+            u[e] = 0;
+            if (w < end) {
+                u[e] = or_word(masks, B, words, w);
+                if (w == words - 1) u[e] &= tail;
+                n += __popc(u[e]);
+            }
+        }
+        int total;
+        int pos = block_excl_scan(n, wsum, &total);
+#pragma unroll
+        for (int e = 0; e < kUnionWords; ++e) {
+            const int w = beg + e;
+            if (w < end) {
+                uint32_t x = u[e];
+                umask[w] = x;
+                while (x) {
+                    uidx[pos++] = w * 32 + __ffs(x) - 1;
+                    x &= x - 1;
+                }
+            }
+        }
+        if (tid == 0) *ucount = total;
+        return;
+    }
     int n = 0;
     for (int w = beg; w < end; ++w) {
-        uint32_t u = 0;
-        for (int b = 0; b < B; ++b) u |= masks[(size_t)b * words + w];
+        uint32_t u = or_word(masks, B, words, w);
         if (w == words - 1) u &= tail;
         n += __popc(u);
     }
     int total;
     int pos = block_excl_scan(n, wsum, &total);
     for (int w = beg; w < end; ++w) {
-        uint32_t u = 0;
-        for (int b = 0; b < B; ++b) u |= masks[(size_t)b * words + w];
+        uint32_t u = or_word(masks, B, words, w);
         if (w == words - 1) u &= tail;
         umask[w] = u;
         while (u) {
