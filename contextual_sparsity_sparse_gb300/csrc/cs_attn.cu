@@ -28,7 +28,9 @@
 //  3. combine and project: a (slot, 64-vector column chunk) CTA merges the
 //     head's splits in split order (M = max m, L = sum l e^(m - M),
 //     o = sum o_s e^(m - M) / L) and applies its chunk of W_o[:, h] o (four
-//     row groups added in order), the first rows loaded before the wait.
+//     row groups added in order); a thread's rows (all of them up to
+//     d_head 128) are loaded before the wait, so they stream in while the
+//     attend kernel runs.
 //  4. the FFN's fixed-order reduction adds the per-slot partials.
 // Kernels 1-3 let their dependents launch only after their own wait, so when
 // kernels 2 and 3 start the selection that wrote the head list has finished
@@ -50,7 +52,7 @@ constexpr int kKV = kSplitVec / kAttnThreads;
 constexpr int kQRows = 4;         // W_q rows per query CTA
 constexpr int kOVec = 64;         // 16-byte column vectors of the output projection per CTA
 constexpr int kOGroups = kAttnThreads / kOVec;
-constexpr int kOPre = 4;          // W_o rows per thread loaded before the wait
+constexpr int kOPre = 32;         // W_o rows per thread loaded before the wait (all of them up to d_head 128)
 
 struct AttnK {
     const uint8_t *w_q, *w_o_t, *k, *v;
