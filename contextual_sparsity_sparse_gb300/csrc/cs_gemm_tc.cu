@@ -31,10 +31,15 @@
 //                    rows staged as the MN-major operand (64 neurons x 128
 //                    columns per stage), AS as the K-major operand; per-split
 //                    partial y written for the fixed-order reduce kernel
-// A stage is refilled two k-blocks after its MMAs were issued; their
-// completion is tracked by tcgen05.commit on one mbarrier per stage.  Every
-// wait is bounded: on a timeout the kernel records CS_DEVERR_TIMEOUT, stops
-// issuing, lets its copies land and frees its tensor memory.
+// The gate kernel runs warp-specialised: seven producer warps copy stages in
+// with per-thread cp.async and arrive on the stage's "full" mbarrier when
+// their copies land (cp.async.mbarrier.arrive), and one warp issues the MMAs
+// and commits them to the stage's "empty" mbarrier, which releases it to the
+// producers; no block barrier per stage.  The down kernel refills a stage two
+// k-blocks after its MMAs were issued, their completion tracked by
+// tcgen05.commit on one mbarrier per stage.  Every wait is bounded: on a
+// timeout the kernel records CS_DEVERR_TIMEOUT, stops issuing, lets its copies
+// land and frees its tensor memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -187,6 +192,17 @@ __device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity) {
     return mbar_wait(bar, parity, 1000000000ull);
 }
 
+// arrive on bar once all of this thread's earlier cp.async copies have landed
+// (the barrier's expected count includes this arrival)
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Gate-GEMM warp roles: warps 0 .. kProdWarps-1 copy stages in, warp
+// kProdWarps issues the MMAs.
+constexpr int kProdWarps = 7;
+constexpr int kProd = kProdWarps * 32;
+
 // ---- gate (and up) GEMM + activation, stream-K ----------------------------------
 // Work units are (tile t of 128 union neurons, k-block of KS elements of d),
 // t-major; CTA c of P takes units [U c / P, U (c+1) / P).  With at most 2P
@@ -224,7 +240,8 @@ __device__ __forceinline__ void gate_act_out(const TcArgs &a, const float (&g)[N
 template <typename T, bool GLU, int NP, int KS>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
-    __shared__ __align__(8) uint64_t bars[8];
+    __shared__ __align__(8) uint64_t full[8];    // stage landed: kProd cp.async arrivals
+    __shared__ __align__(8) uint64_t empty[8];   // stage's MMAs done: one tcgen05.commit
     __shared__ uint32_t tmem_base;
     __shared__ int s_idx[kGateSegMax * kTileM];
     __shared__ int s_last[kGateSegMax];
@@ -242,7 +259,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) 
 
     if (warp == 0) tmem_alloc(&tmem_base, ncols);
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], kProd);
+            mbar_init(&empty[s], 1);
+        }
         mbar_fence_init();
     }
     tc_fence_before();
@@ -292,13 +312,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) 
     };
     Cur ic{0, kb_first};   // unit of the next issue
 
-    // copies of the next unit into stage q % S; the lanes of a warp cover
-    // contiguous bytes of a row (KS * 2 bytes per row); called with q in order
-    auto issue = [&](int q) {
-        if (q < Q) {
-            const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
+    // Producers (warps 0 .. kProdWarps-1) copy unit q into stage q % S once
+    // the MMAs of unit q - S have released it, and arrive on full[q % S] when
+    // their copies land; the MMA warp waits for full, issues the stage's MMAs
+    // and commits them to empty.  No block barrier per stage: the producers
+    // run up to S stages ahead.  The lanes of a warp cover contiguous bytes of
+    // a row (KS * 2 bytes per row).
+    bool ok = true;
+    if (warp < kProdWarps) {
+        for (int q = 0; q < Q; ++q) {
+            const int sq = q % S;
+            // the whole warp stops together if a wait gives up
+            if (q >= S && !__all_sync(kFull, stage_wait(&empty[sq], (uint32_t)((q / S - 1) & 1)))) {
+                ok = false;
+                break;
+            }
+            const uint32_t st = sbase + (uint32_t)(sq * kStageBytes);
             const size_t koff = (size_t)ic.kb * KS * 2;
-            for (int i = tid; i < kTileM * 8 * KA; i += kTcThreads) {
+            for (int i = tid; i < kTileM * 8 * KA; i += kProd) {
                 const int r = i / (8 * KA), ch = i % (8 * KA);
                 const uint32_t off = (uint32_t)((ch >> 3) * kTileBytes) + kmaj_off(r, ch & 7);
                 const size_t roff = (size_t)s_idx[ic.lt * kTileM + r] * a.ldb + koff + ch * 16;
@@ -306,46 +337,48 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gate_kernel(const TcArgs a) 
                 if (GLU) cp16t(st + kWBytes + off, a.w_up + roff);
             }
             const uint32_t sx = st + kA * kWBytes;
-            for (int i = tid; i < NP * 8 * KA; i += kTcThreads) {
+            for (int i = tid; i < NP * 8 * KA; i += kProd) {
                 const int r = i / (8 * KA), ch = i % (8 * KA);
                 cp16t(sx + (uint32_t)((ch >> 3) * kXAtom) + kmaj_off(r, ch & 7),
                       reinterpret_cast<const uint8_t *>(a.xs) + (size_t)r * a.dk * 2 + koff + ch * 16);
             }
+            cp_async_arrive(&full[sq]);
             step(ic);
         }
-        cp_async_commit();
-    };
-
-    for (int q = 0; q < S - 2; ++q) issue(q);
-    bool ok = true;
-    Cur cc{0, kb_first};   // unit being multiplied
-    for (int q = 0; q < Q; ++q) {
-        // every decision to stop is taken by the whole block at a barrier
-        bool mine = q < 2 || stage_wait(&bars[(q - 2) % S], (uint32_t)(((q - 2) / S) & 1));
-        if (mine) issue(q + S - 2);  // stage of step q - 2, whose MMAs have completed
-        cp_async_wait_upto(S - 2);   // step q complete: S - 2 later groups may be pending
-        fence_async_smem();
-        if (!__syncthreads_and(mine)) { ok = false; break; }
-        if (tid == 0) {
+    } else {
+        // the MMA warp: every lane waits (so the warp stays converged), lane 0
+        // issues; the copies were made visible to the tensor cores' async
+        // proxy by the proxy fence after the wait
+        Cur cc{0, kb_first};   // unit being multiplied
+        for (int q = 0; q < Q; ++q) {
+            const int sq = q % S;
+            if (!__all_sync(kFull, stage_wait(&full[sq], (uint32_t)((q / S) & 1)))) { ok = false; break; }
+            fence_async_smem();
             tc_fence_after();
-            const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
-            const uint32_t sx = st + kA * kWBytes;
-            const uint32_t acc = tmem + (uint32_t)(cc.lt * kSetCols);
-            const bool fresh = q == 0 || cc.kb == 0;
+            if (lane == 0) {
+                const uint32_t st = sbase + (uint32_t)(sq * kStageBytes);
+                const uint32_t sx = st + kA * kWBytes;
+                const uint32_t acc = tmem + (uint32_t)(cc.lt * kSetCols);
+                const bool fresh = q == 0 || cc.kb == 0;
 #pragma unroll
-            for (int kk = 0; kk < KS / 16; ++kk) {
-                const uint32_t ka = (uint32_t)(kk >> 2), kin = (uint32_t)((kk & 3) * 32);
-                const uint64_t bd = umma_desc(sx + ka * kXAtom + kin, 16, 1024);
-                umma(acc, umma_desc(st + ka * kTileBytes + kin, 16, 1024), bd, idesc, !(fresh && kk == 0));
-                if (GLU)
-                    umma(acc + NP, umma_desc(st + kWBytes + ka * kTileBytes + kin, 16, 1024), bd, idesc,
-                         !(fresh && kk == 0));
+                for (int kk = 0; kk < KS / 16; ++kk) {
+                    const uint32_t ka = (uint32_t)(kk >> 2), kin = (uint32_t)((kk & 3) * 32);
+                    const uint64_t bd = umma_desc(sx + ka * kXAtom + kin, 16, 1024);
+                    umma(acc, umma_desc(st + ka * kTileBytes + kin, 16, 1024), bd, idesc, !(fresh && kk == 0));
+                    if (GLU)
+                        umma(acc + NP, umma_desc(st + kWBytes + ka * kTileBytes + kin, 16, 1024), bd, idesc,
+                             !(fresh && kk == 0));
+                }
+                umma_commit(&empty[sq]);
             }
-            umma_commit(&bars[q % S]);
+            __syncwarp();
+            step(cc);
         }
-        step(cc);
     }
-    if (ok && Q > 0) ok = __syncthreads_and(stage_wait(&bars[(Q - 1) % S], (uint32_t)(((Q - 1) / S) & 1)));
+    // every decision to stop is taken by the whole block at a barrier; then
+    // everyone waits for the last unit's MMAs
+    ok = __syncthreads_and(ok);
+    if (ok && Q > 0) ok = __syncthreads_and(stage_wait(&empty[(Q - 1) % S], (uint32_t)(((Q - 1) / S) & 1)));
     tc_fence_after();
 
     // segments: a whole tile -> activation now; a part -> piece slot (c, sg)
