@@ -489,7 +489,8 @@ __device__ __forceinline__ int sk_owner(long long u, long long U, int P) {
 template <typename T, int NP, int MT>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
-    __shared__ __align__(8) uint64_t bars[8];
+    __shared__ __align__(8) uint64_t full[8];    // stage landed: kProd cp.async arrivals
+    __shared__ __align__(8) uint64_t empty[8];   // stage's MMAs done: one tcgen05.commit
     __shared__ uint32_t tmem_base;
     constexpr int kCols = kTileM * MT;                      // output rows of a column group
     constexpr int kWBytes = MT * kTileBytes;                // 64 rows x kCols columns
@@ -503,7 +504,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
 
     if (warp == 0) tmem_alloc(&tmem_base, ncols);
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], kProd);
+            mbar_init(&empty[s], 1);
+        }
         mbar_fence_init();
     }
     tc_fence_before();
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
     pdl_launch_dependents();
     pdl_wait();  // AS comes from the gate kernel
 
-    int n = *a.count;
+    int n = ld_dep(a.count);
     if (n < 0 || n > a.f) n = n < 0 ? 0 : a.f;
     const int NG = (a.d + kCols - 1) / kCols;
     const int NKB = (n + kKB - 1) / kKB;
@@ -533,34 +537,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
     auto step = [&](Cur &u) {
         if (++u.kb == NKB) { u.kb = 0; ++u.g; }
     };
-    // a row of a stage is 16 * MT chunks, covered by consecutive lanes; thread
-    // t handles rows t / (16 MT) + i * 256 / (16 MT); their ids for the next
-    // step are loaded one step ahead
+    // A stage row is 16 * MT chunks covered by consecutive producer lanes.
+    // Warp-specialised like the gate kernel: producers (warps 0 .. 6) copy
+    // unit q into stage q % S once the MMAs of unit q - S released it and
+    // arrive on full[q % S] when their copies land; warp 7 issues the MMAs
+    // and commits them to empty[q % S].
     constexpr int kCh = 16 * MT;
-    constexpr int kRowsPerThread = kKB * kCh / kTcThreads;
-    auto row_ids = [&](bool live, int kb, int (&j)[kRowsPerThread]) {
+    constexpr int kPer = (kKB * kCh + kProd - 1) / kProd;   // chunks per producer thread and stage
+    bool ok = true;
+    int seg = 0;           // slot (and accumulator set) of the last column group
+    if (warp < kProdWarps) {
+        // the row ids of a stage's chunks are loaded one stage ahead, so no
+        // copy waits for its id
+        int jcur[kPer], jnext[kPer];
+        auto row_ids = [&](bool live, int kb, int (&j)[kPer]) {
 #pragma unroll
-        for (int it = 0; it < kRowsPerThread; ++it) {
-            const int p = kb * kKB + tid / kCh + it * (kTcThreads / kCh);
-            j[it] = (live && p < n) ? ld_dep(a.idx + p) : last;
-        }
-    };
-    int jcur[kRowsPerThread], jnext[kRowsPerThread];
-    Cur ic = first;   // unit of the next issue
-    Cur pc = first;   // unit after it (its row ids are prefetched)
-    step(pc);
-    row_ids(Q > 0, ic.kb, jcur);
-
-    // called with q = 0, 1, 2, ... in order
-    auto issue = [&](int q) {
-        row_ids(q + 1 < Q, pc.kb, jnext);
-        if (q < Q) {
-            const int kb = ic.kb, m0 = ic.g * kCols;
-            const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
+            for (int it = 0; it < kPer; ++it) {
+                const int p = kb * kKB + (tid + it * kProd) / kCh;
+                j[it] = (live && p < n) ? ld_dep(a.idx + p) : last;
+            }
+        };
+        Cur ic = first, pc = first;   // unit of the next issue, and the one after it
+        step(pc);
+        row_ids(Q > 0, ic.kb, jcur);
+        for (int q = 0; q < Q; ++q) {
+            const int sq = q % S;
+            if (q >= S && !__all_sync(kFull, stage_wait(&empty[sq], (uint32_t)((q / S - 1) & 1)))) {
+                ok = false;
+                break;
+            }
+            const int m0 = ic.g * kCols;
+            const uint32_t st = sbase + (uint32_t)(sq * kStageBytes);
             // 64 gathered rows x kCols columns (256 * MT bytes) of W_down^T
 #pragma unroll
-            for (int it = 0; it < kRowsPerThread; ++it) {
-                const int i = tid + it * kTcThreads;
+            for (int it = 0; it < kPer; ++it) {
+                const int i = tid + it * kProd;
+                if (i >= kKB * kCh) break;
                 const int k = i / kCh, ch = i % kCh;
                 int j = jcur[it];
                 j = (j >= 0 && j < a.f) ? j : 0;
@@ -573,58 +585,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_down_kernel(const TcArgs a) 
                 }
             }
             const uint32_t sx = st + kWBytes;
-            const size_t koff = (size_t)kb * kKB * 2;
-            for (int i = tid; i < NP * 8; i += kTcThreads) {
+            const size_t koff = (size_t)ic.kb * kKB * 2;
+            for (int i = tid; i < NP * 8; i += kProd) {
                 const int r = i >> 3, ch = i & 7;
                 cp16t(sx + kmaj_off(r, ch), reinterpret_cast<const uint8_t *>(a.as) + (size_t)r * a.kp * 2 + koff + ch * 16);
             }
-        }
-        cp_async_commit();
+            // plain shared stores (the zero columns) are ordered before the
+            // arrival by this fence; the copies by the arrival itself
+            fence_async_smem();
+            cp_async_arrive(&full[sq]);
+            row_ids(q + 1 < Q, pc.kb, jnext);
 #pragma unroll
-        for (int it = 0; it < kRowsPerThread; ++it) jcur[it] = jnext[it];
-        step(ic);
-        step(pc);
-    };
-
-    for (int q = 0; q < S - 2; ++q) issue(q);
-    bool ok = true;
-    Cur cc = first;        // unit being multiplied
-    int seg = 0;           // slot (and accumulator set) of the current column group
-    bool fresh = true;     // the next MMA starts a new accumulation
-    for (int q = 0; q < Q; ++q) {
-        bool mine = q < 2 || stage_wait(&bars[(q - 2) % S], (uint32_t)(((q - 2) / S) & 1));
-        if (mine) issue(q + S - 2);
-        cp_async_wait_upto(S - 2);
-        fence_async_smem();
-        if (!__syncthreads_and(mine)) { ok = false; break; }
-        if (tid == 0) {
+            for (int it = 0; it < kPer; ++it) jcur[it] = jnext[it];
+            step(ic);
+            step(pc);
+        }
+    } else {
+        Cur cc = first;        // unit being multiplied
+        bool fresh = true;     // the next MMA starts a new accumulation
+        for (int q = 0; q < Q; ++q) {
+            const int sq = q % S;
+            if (!__all_sync(kFull, stage_wait(&full[sq], (uint32_t)((q / S) & 1)))) { ok = false; break; }
+            fence_async_smem();
             tc_fence_after();
-            const uint32_t st = sbase + (uint32_t)((q % S) * kStageBytes);
-            const uint32_t sx = st + kWBytes;
-            const uint32_t acc = tmem + (uint32_t)(seg * kSegCols);
-            constexpr uint32_t kSbo = 2048 * MT;   // bytes between 8-row k groups
+            if (lane == 0) {
+                const uint32_t st = sbase + (uint32_t)(sq * kStageBytes);
+                const uint32_t sx = st + kWBytes;
+                const uint32_t acc = tmem + (uint32_t)(seg * kSegCols);
+                constexpr uint32_t kSbo = 2048 * MT;   // bytes between 8-row k groups
 #pragma unroll
-            for (int kk = 0; kk < kKB / 16; ++kk) {
-                const uint64_t bd = umma_desc(sx + kk * 32, 16, 1024);
+                for (int kk = 0; kk < kKB / 16; ++kk) {
+                    const uint64_t bd = umma_desc(sx + kk * 32, 16, 1024);
 #pragma unroll
-                for (int t = 0; t < MT; ++t)
-                    umma(acc + (uint32_t)(t * NP), umma_desc(st + t * 2048 + kk * 2 * kSbo, 1024, kSbo), bd, idesc,
-                         !(fresh && kk == 0));
+                    for (int t = 0; t < MT; ++t)
+                        umma(acc + (uint32_t)(t * NP), umma_desc(st + t * 2048 + kk * 2 * kSbo, 1024, kSbo), bd,
+                             idesc, !(fresh && kk == 0));
+                }
+                umma_commit(&empty[sq]);
             }
-            umma_commit(&bars[q % S]);
+            __syncwarp();
+            fresh = false;
+            // a range covers at most two column groups: the second accumulates
+            // into the second set, so no MMA has to finish before it starts
+            if (cc.kb == NKB - 1 && q < Q - 1) {
+                ++seg;
+                fresh = true;
+            }
+            step(cc);
         }
-        fresh = false;
-        // a range covers at most two column groups: the second accumulates
-        // into the second set, so no MMA has to finish before it starts
-        if (cc.kb == NKB - 1 && q < Q - 1) {
-            ++seg;
-            fresh = true;
-        }
-        step(cc);
     }
-    // every segment's partial sums to its slot, once the last MMAs are done
-    if (ok && Q > 0) ok = __syncthreads_and(stage_wait(&bars[(Q - 1) % S], (uint32_t)(((Q - 1) / S) & 1)));
+    // the number of column groups the range covers (the MMA warp's seg)
+    {
+        __shared__ int s_seg;
+        if (tid == kProd) s_seg = seg;
+        ok = __syncthreads_and(ok);
+        seg = s_seg;
+    }
+    if (ok && Q > 0) ok = __syncthreads_and(stage_wait(&empty[(Q - 1) % S], (uint32_t)(((Q - 1) / S) & 1)));
     tc_fence_after();
+    // every segment's partial sums to its slot, once the last MMAs are done
     if (ok && Q > 0 && warp < 4) {
         for (int sg = 0; sg <= seg; ++sg) {
             const size_t slot = (size_t)(c * 2 + sg) * a.B;
