@@ -156,21 +156,40 @@ __device__ __forceinline__ uint32_t tmem_cols(int c) {
 }
 
 // ---- X -> [hi; lo] rows ------------------------------------------------------
+// A thread converts 8 consecutive columns of one token (16-byte stores of
+// its hi and lo rows); rows past 2B are zero.  dk = d is a multiple of 64.
 template <typename T>
 __global__ void tc_split_kernel(const TcArgs a, int np, int ncount) {
     pdl_launch_dependents();
     pdl_wait();
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncount; i += gridDim.x * blockDim.x) a.tile_count[i] = 0u;
-    const size_t total = (size_t)np * a.dk;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-        const int n = (int)(i / a.dk), c = (int)(i % a.dk);
-        uint16_t out = 0;
-        if (c < a.d && n < 2 * a.B) {
-            const float v = a.x[(size_t)(n >> 1) * a.d + c];
-            const uint16_t hi = Tc<T>::bits(v);
-            out = (n & 1) ? Tc<T>::bits(v - Tc<T>::val(hi)) : hi;
+    const int gt = blockIdx.x * blockDim.x + threadIdx.x, gs = gridDim.x * blockDim.x;
+    for (int i = gt; i < ncount; i += gs) a.tile_count[i] = 0u;
+    const int c8 = a.dk / 8;
+    const bool x4 = (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
+    for (int i = gt; i < (np / 2) * c8; i += gs) {
+        const int b = i / c8, c0 = (i % c8) * 8;
+        uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+        if (b < a.B) {
+            float v[8];
+            const float *src = a.x + (size_t)b * a.d + c0;
+            if (x4) {
+                const float4 p = ld_dep(reinterpret_cast<const float4 *>(src));
+                const float4 q = ld_dep(reinterpret_cast<const float4 *>(src + 4));
+                v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w; v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = ld_dep(src + e);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const uint16_t h0 = Tc<T>::bits(v[e]), h1 = Tc<T>::bits(v[e + 1]);
+                const uint16_t l0 = Tc<T>::bits(v[e] - Tc<T>::val(h0)), l1 = Tc<T>::bits(v[e + 1] - Tc<T>::val(h1));
+                hi[e / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+                lo[e / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+            }
         }
-        a.xs[i] = out;
+        *reinterpret_cast<uint4 *>(a.xs + (size_t)(2 * b) * a.dk + c0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(a.xs + (size_t)(2 * b + 1) * a.dk + c0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
 }
 
@@ -739,8 +758,8 @@ cudaError_t run_tc(const FfnArgs &f, cudaStream_t s) {
 
     // 1. X -> [hi; lo]
     a.stages = 0;
-    cudaError_t e = launch(tc_split_kernel<T>, dim3(std::min(sms, (NP * a.dk + 255) / 256)), dim3(256), 0, s,
-                           pdl_enabled(), a, NP, 2 * sms);
+    cudaError_t e = launch(tc_split_kernel<T>, dim3(std::min(4 * sms, (NP / 2 * a.dk / 8 + 255) / 256)), dim3(256), 0,
+                           s, pdl_enabled(), a, NP, 2 * sms);
     if (e != cudaSuccess) return e;
 
     // 2. gate (and up) GEMM + activation, stream-K over (128-neuron tile,

@@ -21,10 +21,18 @@ namespace {
 constexpr int kUnionThreads = 1024;
 constexpr int kUnionWords = 4;   // words per thread kept in registers (f <= 131072)
 
-// OR of word w over the B masks, eight loads in flight at a time.
+// OR of word w over the B masks, 32 (then 8) loads in flight at a time: one
+// CTA does the whole union, so it is bound by load latency, not bandwidth.
 __device__ __forceinline__ uint32_t or_word(const uint32_t *masks, int B, int words, int w) {
     uint32_t acc = 0;
     int b = 0;
+    for (; b + 32 <= B; b += 32) {
+        uint32_t t[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) t[i] = ld_dep(masks + (size_t)(b + i) * words + w);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc |= t[i];
+    }
     for (; b + 8 <= B; b += 8) {
         uint32_t t[8];
 #pragma unroll
