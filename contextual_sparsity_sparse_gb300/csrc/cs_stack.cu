@@ -16,8 +16,14 @@
 //
 // The same machinery serves cs_decode_layer, one layer's step for one token
 // (predictor, selection, gathered FFN; y without the residual): its five
-// kernels become one cached graph, and x / y in page-locked host memory are
-// staged through the workspace by copies issued around the graph launch.
+// kernels become one cached graph.
+//
+// x / y in page-locked host memory are read and written by the graph itself:
+// a small copy kernel at each end of the graph reaches the host buffer through
+// its device mapping (GB300's host memory sits behind NVLink-C2C), and the
+// cached graph's two copy nodes are pointed at each call's buffers by a node
+// parameter update, so no copy-engine transfer is issued per call.  Without a
+// device mapping the buffers are staged by copies around the graph launch.
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -49,7 +55,43 @@ struct StackPlan {
     int32_t *trace_count, *trace_idx;
     bool layer_only = false;  // single-layer step: y = FFN(x), no residual
     float *y = nullptr;       // its output
+    // device mappings of the caller's page-locked host x (read into p.x
+    // first) and host y (or the stack's x, written from p.y / p.x last)
+    const float *io_src = nullptr;
+    float *io_dst = nullptr;
 };
+
+constexpr int kIoThreads = 256;
+
+struct IoCopy {
+    const float *src;
+    float *dst;
+    int n;
+};
+
+dim3 io_grid(int n) { return dim3((unsigned)((n + 4 * kIoThreads - 1) / (4 * kIoThreads))); }
+
+// dst[0, n) = src[0, n), four floats per thread (16-byte accesses when both
+// ends allow them).  DIR 0 is the graph's first node (host x in), DIR 1 its
+// last (y, or the stack's x, out); the two instantiations tell the nodes apart.
+template <int DIR>
+__global__ void __launch_bounds__(kIoThreads) io_copy_kernel(const IoCopy a) {
+    pdl_launch_dependents();
+    pdl_wait();  // DIR 1 reads what the reduction wrote
+    const int i = (blockIdx.x * kIoThreads + threadIdx.x) * 4;
+    if (i >= a.n) return;
+    const bool v16 = ((reinterpret_cast<uintptr_t>(a.src) | reinterpret_cast<uintptr_t>(a.dst)) & 15u) == 0;
+    if (v16 && i + 4 <= a.n) {
+        *reinterpret_cast<float4 *>(a.dst + i) = ld_dep(reinterpret_cast<const float4 *>(a.src + i));
+    } else {
+        for (int j = i; j < a.n && j < i + 4; ++j) a.dst[j] = ld_dep(a.src + j);
+    }
+}
+
+cudaError_t launch_io(int dir, const IoCopy &a, cudaStream_t s) {
+    return launch(dir == 0 ? io_copy_kernel<0> : io_copy_kernel<1>, io_grid(a.n), dim3(kIoThreads), 0, s,
+                  pdl_enabled(), a);
+}
 
 struct Bufs {
     float *xb[2];
@@ -164,6 +206,7 @@ struct Events {
 cudaError_t enqueue_stack(const StackPlan &p, cudaStream_t sm, cudaStream_t sp, Events &E) {
     const Bufs b = bufs_of(p);
     const int L = p.L;
+    if (p.io_src) TRY(launch_io(0, IoCopy{p.io_src, p.x, p.d}, sm));
     if (p.sel.mode == CS_SEL_EXACT) {
         for (int l = 0; l < L; ++l) TRY(exact_step(p, b, l, b.xb[l & 1], b.xb[(l + 1) & 1], sm));
     } else if (p.mode == CS_STACK_SEQUENTIAL || sp == sm) {
@@ -203,6 +246,7 @@ cudaError_t enqueue_stack(const StackPlan &p, cudaStream_t sm, cudaStream_t sp, 
         TRY(cudaEventRecord(ev_join, sp));
         TRY(cudaStreamWaitEvent(sm, ev_join, 0));
     }
+    if (p.io_dst) return launch_io(1, IoCopy{b.xb[L & 1], p.io_dst, p.d}, sm);
     if (L & 1)
         TRY(cudaMemcpyAsync(p.x, b.xb[1], sizeof(float) * (size_t)p.d, cudaMemcpyDeviceToDevice, sm));
     return cudaSuccess;
@@ -211,15 +255,27 @@ cudaError_t enqueue_stack(const StackPlan &p, cudaStream_t sm, cudaStream_t sp, 
 // Enqueue one layer's step for one token: y = FFN(x, select(P(x))).
 cudaError_t enqueue_layer(const StackPlan &p, cudaStream_t s) {
     const Bufs b = bufs_of(p);
-    if (p.sel.mode == CS_SEL_EXACT) return exact_step(p, b, 0, p.x, p.y, s);
-    TRY(predict_select(p, b, 0, p.x, s));
-    return ffn_step(p, b, 0, p.x, p.y, nullptr, s);
+    if (p.io_src) TRY(launch_io(0, IoCopy{p.io_src, p.x, p.d}, s));
+    if (p.sel.mode == CS_SEL_EXACT) TRY(exact_step(p, b, 0, p.x, p.y, s));
+    else {
+        TRY(predict_select(p, b, 0, p.x, s));
+        TRY(ffn_step(p, b, 0, p.x, p.y, nullptr, s));
+    }
+    if (p.io_dst) TRY(launch_io(1, IoCopy{p.y, p.io_dst, p.d}, s));
+    return cudaSuccess;
 }
 
 struct CacheEntry {
     cudaGraphExec_t exec = nullptr;
+    cudaGraph_t graph = nullptr;      // kept while its copy nodes are updated
+    cudaGraphNode_t io_node[2] = {nullptr, nullptr};
+    IoCopy io_args[2] = {};
     int device = -1;
 };
+
+// Set when a captured graph's copy nodes could not be found (its kernel
+// nodes do not report their functions): host I/O then uses copies.
+bool g_io_nodes_unusable = false;
 
 std::mutex g_mu;
 std::unordered_map<std::string, CacheEntry> g_cache;
@@ -243,13 +299,71 @@ std::string plan_key(const StackPlan &p, cudaStream_t sp, int dev) {
     put(&p.y, sizeof p.y);
     const bool same = sp == nullptr;
     put(&same, sizeof same);
+    // the copy nodes' host addresses change per call; only their presence
+    // shapes the graph
+    const bool io[2] = {p.io_src != nullptr, p.io_dst != nullptr};
+    put(io, sizeof io);
     return k;
 }
 
+void destroy_entry(CacheEntry &ce) {
+    if (ce.exec) cudaGraphExecDestroy(ce.exec);
+    if (ce.graph) cudaGraphDestroy(ce.graph);
+    ce.exec = nullptr;
+    ce.graph = nullptr;
+}
+
 void clear_cache_locked() {
-    for (auto &kv : g_cache)
-        if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    for (auto &kv : g_cache) destroy_entry(kv.second);
     g_cache.clear();
+}
+
+// The copy nodes of a captured graph and their current arguments.
+cudaError_t find_io_nodes(CacheEntry &ce) {
+    size_t n = 0;
+    TRY(cudaGraphGetNodes(ce.graph, nullptr, &n));
+    std::vector<cudaGraphNode_t> nodes(n);
+    TRY(cudaGraphGetNodes(ce.graph, nodes.data(), &n));
+    const void *fn[2] = {reinterpret_cast<const void *>(io_copy_kernel<0>),
+                         reinterpret_cast<const void *>(io_copy_kernel<1>)};
+    for (size_t i = 0; i < n; ++i) {
+        cudaGraphNodeType t;
+        TRY(cudaGraphNodeGetType(nodes[i], &t));
+        if (t != cudaGraphNodeTypeKernel) continue;
+        cudaKernelNodeParams kp = {};
+        TRY(cudaGraphKernelNodeGetParams(nodes[i], &kp));
+        for (int dir = 0; dir < 2; ++dir) {
+            if (kp.func == fn[dir] && kp.kernelParams) {
+                ce.io_node[dir] = nodes[i];
+                ce.io_args[dir] = *static_cast<const IoCopy *>(kp.kernelParams[0]);
+            }
+        }
+    }
+    return cudaSuccess;
+}
+
+// Point the cached graph's copy nodes at this call's host buffers.
+cudaError_t update_io(CacheEntry &ce, const StackPlan &p) {
+    const float *src[2] = {p.io_src, nullptr};
+    float *dst[2] = {nullptr, p.io_dst};
+    for (int dir = 0; dir < 2; ++dir) {
+        if (!ce.io_node[dir]) continue;
+        IoCopy a = ce.io_args[dir];
+        if (dir == 0) a.src = src[0];
+        else a.dst = dst[1];
+        if (a.src == ce.io_args[dir].src && a.dst == ce.io_args[dir].dst) continue;
+        cudaKernelNodeParams kp = {};
+        kp.func = dir == 0 ? reinterpret_cast<void *>(io_copy_kernel<0>) : reinterpret_cast<void *>(io_copy_kernel<1>);
+        kp.gridDim = io_grid(a.n);
+        kp.blockDim = dim3(kIoThreads);
+        kp.sharedMemBytes = 0;
+        void *args[] = {&a};
+        kp.kernelParams = args;
+        kp.extra = nullptr;
+        TRY(cudaGraphExecKernelNodeSetParams(ce.exec, ce.io_node[dir], &kp));
+        ce.io_args[dir] = a;
+    }
+    return cudaSuccess;
 }
 
 // Shape and layout checks shared by the stack and the single-layer step.
@@ -320,8 +434,12 @@ cs_status check_params(const cs_select_params *params, const char *who) {
 
 // Enqueue the plan directly when the caller is capturing (or on the legacy
 // stream), else replay its cached graph, capturing it on first use.
+// With copy nodes (p.io_src / p.io_dst), *io_refused is set instead when the
+// nodes of a captured graph cannot be located; the caller then stages its
+// host buffers with copies.
 template <typename Enq>
-cs_status run_cached(const StackPlan &p, cudaStream_t sm, cudaStream_t sp_key, const char *who, Enq enq) {
+cs_status run_cached(const StackPlan &p, cudaStream_t sm, cudaStream_t sp_key, const char *who, Enq enq,
+                     bool *io_refused = nullptr) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (sm) {
         cudaError_t e = cudaStreamIsCapturing(sm, &cap);
@@ -335,6 +453,11 @@ cs_status run_cached(const StackPlan &p, cudaStream_t sm, cudaStream_t sp_key, c
     cudaGetDevice(&dev);
     const std::string key = plan_key(p, sp_key, dev);
     std::lock_guard<std::mutex> lock(g_mu);
+    const bool io = p.io_src || p.io_dst;
+    if (io && g_io_nodes_unusable) {
+        *io_refused = true;
+        return CS_OK;
+    }
     auto it = g_cache.find(key);
     if (it == g_cache.end()) {
         if (g_cache.size() >= kMaxCached) clear_cache_locked();
@@ -350,21 +473,37 @@ cs_status run_cached(const StackPlan &p, cudaStream_t sm, cudaStream_t sp_key, c
         if (e != cudaSuccess) return cuda_fail(e, who);
         CacheEntry ce;
         ce.device = dev;
+        ce.graph = graph;
         e = cudaGraphInstantiate(&ce.exec, graph, 0);
-        cudaGraphDestroy(graph);
-        if (e != cudaSuccess) return cuda_fail(e, who);
+        if (e == cudaSuccess && io) e = find_io_nodes(ce);
+        if (e != cudaSuccess) {
+            destroy_entry(ce);
+            return cuda_fail(e, who);
+        }
+        if (io && ((p.io_src && !ce.io_node[0]) || (p.io_dst && !ce.io_node[1]))) {
+            destroy_entry(ce);
+            g_io_nodes_unusable = true;
+            *io_refused = true;
+            return CS_OK;
+        }
+        if (!io) {
+            cudaGraphDestroy(ce.graph);
+            ce.graph = nullptr;
+        }
         it = g_cache.emplace(key, ce).first;
     }
-    cudaError_t e = cudaGraphLaunch(it->second.exec, sm);
+    cudaError_t e = io ? update_io(it->second, p) : cudaSuccess;
+    if (e == cudaSuccess) e = cudaGraphLaunch(it->second.exec, sm);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, who);
 }
 
 // Where a pointer given for x or y lives: device (or managed) memory is used
 // in place, page-locked host memory is staged through the workspace, and
 // pageable host memory is refused (its copies cannot be asynchronous).
-cs_status io_kind(const void *ptr, bool *host, const char *who, const char *what) {
+cs_status io_kind(const void *ptr, bool *host, void **mapped, const char *who, const char *what) {
     cudaPointerAttributes at = {};
     cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+    *mapped = nullptr;
     if (e != cudaSuccess) {
         cudaGetLastError();
         set_error("%s: %s: %s", who, what, cudaGetErrorString(e));
@@ -372,6 +511,7 @@ cs_status io_kind(const void *ptr, bool *host, const char *who, const char *what
     }
     if (at.type == cudaMemoryTypeHost) {
         *host = true;
+        *mapped = at.devicePointer;   // null when the memory is not mapped
         return CS_OK;
     }
     if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
@@ -413,7 +553,8 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
         return CS_ERR_WORKSPACE;
     }
     bool x_host = false;
-    st = io_kind(x, &x_host, who, "x");
+    void *xm = nullptr;
+    st = io_kind(x, &x_host, &xm, who, "x");
     if (st != CS_OK) return st;
     const int d = layers[0].d, f = layers[0].f, r = exact ? 1 : preds[0].r;
     StackPlan p;
@@ -426,22 +567,32 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
         set_error("cs_decode_stack: workspace too small: %zu bytes given, %zu needed", ws_bytes, p.lay.total);
         return CS_ERR_WORKSPACE;
     }
-    // a host x goes through the workspace's staging row, so the graph never
-    // names a host address
+    // a host x goes through the workspace's staging row
     p.x = x_host ? reinterpret_cast<float *>(p.ws + p.lay.io_x) : x;
 
     cudaStream_t sm = (cudaStream_t)s_main;
     cudaStream_t sp = (cudaStream_t)s_pred;
+    const bool two = mode == CS_STACK_LOOKAHEAD && !exact && sp && sp != sm;
+    auto enq = [&]() {
+        Events E;
+        return enqueue_stack(p, sm, two ? sp : sm, E);
+    };
+    if (x_host && xm) {
+        // the graph's first and last nodes read and write it in place
+        p.io_src = static_cast<const float *>(xm);
+        p.io_dst = static_cast<float *>(xm);
+        bool refused = false;
+        st = run_cached(p, sm, two ? sp : nullptr, who, enq, &refused);
+        if (st != CS_OK || !refused) return st;
+        p.io_src = nullptr;
+        p.io_dst = nullptr;
+    }
     const size_t x_bytes = sizeof(float) * (size_t)d;
     if (x_host) {
         cudaError_t e = cudaMemcpyAsync(p.x, x, x_bytes, cudaMemcpyHostToDevice, sm);
         if (e != cudaSuccess) return cuda_fail(e, "cs_decode_stack(x copy in)");
     }
-    const bool two = mode == CS_STACK_LOOKAHEAD && !exact && sp && sp != sm;
-    st = run_cached(p, sm, two ? sp : nullptr, who, [&]() {
-        Events E;
-        return enqueue_stack(p, sm, two ? sp : sm, E);
-    });
+    st = run_cached(p, sm, two ? sp : nullptr, who, enq);
     if (st != CS_OK || !x_host) return st;
     cudaError_t e = cudaMemcpyAsync(x, p.x, x_bytes, cudaMemcpyDeviceToHost, sm);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_decode_stack(x copy out)");
@@ -472,9 +623,10 @@ cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, c
         return CS_ERR_WORKSPACE;
     }
     bool x_host = false, y_host = false;
-    st = io_kind(x, &x_host, who, "x");
+    void *xm = nullptr, *ym = nullptr;
+    st = io_kind(x, &x_host, &xm, who, "x");
     if (st != CS_OK) return st;
-    st = io_kind(y, &y_host, who, "y");
+    st = io_kind(y, &y_host, &ym, who, "y");
     if (st != CS_OK) return st;
 
     const int d = layer->d, f = layer->f, r = exact ? 1 : pred->r;
@@ -490,17 +642,28 @@ cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, c
         return CS_ERR_WORKSPACE;
     }
     // host x and y go through the stack's ping-pong buffer and the y staging
-    // buffer, so the graph never names a host address
+    // buffer
     p.x = x_host ? reinterpret_cast<float *>(p.ws + p.lay.st_x) : const_cast<float *>(x);
     p.y = y_host ? reinterpret_cast<float *>(p.ws + p.lay.io_y) : y;
 
     cudaStream_t s = (cudaStream_t)stream;
+    auto enq = [&]() { return enqueue_layer(p, s); };
+    if ((x_host || y_host) && (!x_host || xm) && (!y_host || ym)) {
+        // the graph's first and last nodes read x and write y in place
+        p.io_src = x_host ? static_cast<const float *>(xm) : nullptr;
+        p.io_dst = y_host ? static_cast<float *>(ym) : nullptr;
+        bool refused = false;
+        st = run_cached(p, s, nullptr, who, enq, &refused);
+        if (st != CS_OK || !refused) return st;
+        p.io_src = nullptr;
+        p.io_dst = nullptr;
+    }
     const size_t xy_bytes = sizeof(float) * (size_t)d;
     if (x_host) {
         cudaError_t e = cudaMemcpyAsync(p.x, x, xy_bytes, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e, "cs_decode_layer(x copy)");
     }
-    st = run_cached(p, s, nullptr, who, [&]() { return enqueue_layer(p, s); });
+    st = run_cached(p, s, nullptr, who, enq);
     if (st != CS_OK) return st;
     if (y_host) {
         cudaError_t e = cudaMemcpyAsync(y, p.y, xy_bytes, cudaMemcpyDeviceToHost, s);

@@ -265,18 +265,19 @@ cs_status cs_union_mask(const uint32_t *masks, int B, int f, uint32_t *umask, in
  *   params->mode == CS_SEL_EXACT: A_l = {j : |act(g_j)| > params->tau} at x_l
  *               (g_j > 0 for relu at tau = 0); preds unused.
  *   x: [d] fp32, input x_0 and output x_L: device memory, or page-locked
- *      host memory (cudaHostAlloc, cudaHostRegister, torch pin_memory), which
- *      is copied in and out through the workspace with asynchronous copies on
- *      s_main (x holds x_L once s_main has passed this call).  Pageable host
- *      memory is refused (CS_ERR_INVALID).
+ *      host memory (cudaHostAlloc, cudaHostRegister, torch pin_memory).  A
+ *      host x is read by the graph's first kernel and written by its last
+ *      through the buffer's device mapping (with asynchronous copies on s_main
+ *      around the graph when it has none); x holds x_L once s_main has passed
+ *      this call.  Pageable host memory is refused (CS_ERR_INVALID).
  *   layers, preds: host arrays of L structs (same d, f, r and dtype).
  *   trace_count: [L] int32 device or NULL; trace_idx: [L, f] int32 device or
  *   NULL -- per-layer selected counts and ascending ids.
  * The whole sequence is captured into a CUDA graph on the first call for a
  * given set of arguments and replayed afterwards (unless s_main is already
  * capturing, in which case the kernels are enqueued into the caller's
- * capture); the copies of a host x run outside the graph, so its address may
- * change from call to call without a new capture.  The workspace must hold
+ * capture); a host x's address may change from call to call without a new
+ * capture (the graph's two copy kernels are re-pointed).  The workspace must hold
  * cs_workspace_size(d, f, r, 1) bytes.
  */
 cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds, int L, float *x,
@@ -293,16 +294,17 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
  *      for relu at tau = 0); pred may be NULL.
  *   x: [d] fp32 input;  y: [d] fp32 output.  Each may be device memory or
  *      page-locked host memory (cudaHostAlloc, cudaHostRegister, torch
- *      pin_memory).  Host data is staged through the workspace with
- *      asynchronous copies on `stream`, so a host y holds the result once the
- *      stream has passed this call.  Pageable host memory is refused
- *      (CS_ERR_INVALID) because its copies would not be asynchronous.
+ *      pin_memory).  A host x is read by the graph's first kernel and a
+ *      host y written by its last, through the buffers' device mappings
+ *      (staged with asynchronous copies on `stream` when they have none), so
+ *      a host y holds the result once the stream has passed this call.
+ *      Pageable host memory is refused (CS_ERR_INVALID).
  *   idx: [f] int32 device or NULL; count: int32 device scalar or NULL (both
  *      or neither) -- the selected ids, ascending, and their number.
  * The kernels are captured into a CUDA graph on the first call for a given
- * set of arguments and replayed afterwards; the copies of host x and y run
- * outside the graph, so host addresses may change from call to call without
- * a new capture.  A stream that is already capturing, or the legacy stream
+ * set of arguments and replayed afterwards; host addresses may change from
+ * call to call without a new capture (the graph's copy kernels are
+ * re-pointed).  A stream that is already capturing, or the legacy stream
  * (NULL), gets the kernels enqueued directly.  The workspace must hold
  * cs_workspace_size(d, f, r, 1) bytes.  This call uses the same workspace
  * regions as cs_decode_stack, so the two must not overlap on one workspace.

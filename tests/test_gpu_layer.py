@@ -120,7 +120,7 @@ def test_layer_threshold_and_no_outputs():
     assert np.array_equal(y.cpu().numpy().view(np.uint32), y2.cpu().numpy().view(np.uint32))
 
 
-@pytest.mark.parametrize("io", ["device", "pinned"])
+@pytest.mark.parametrize("io", ["device", "pinned", "pinned_x", "pinned_y"])
 def test_layer_exact_matches_exact_ffn(io):
     d, f = 1000, 3001
     H = HostLayer(d, f, 0, synth.BF16, glu=True, seed=8)
@@ -130,10 +130,11 @@ def test_layer_exact_matches_exact_ffn(io):
     ws = cs.Workspace(d, f, 1, stream=s)
     idx = torch.empty(f, dtype=torch.int32, device="cuda")
     cnt = torch.empty(1, dtype=torch.int32, device="cuda")
-    if io == "device":
-        x, y = torch.from_numpy(X[0].copy()).cuda(), torch.empty(d, device="cuda")
-    else:
-        x, y = torch.from_numpy(X[0].copy()).pin_memory(), torch.empty(d).pin_memory()
+    # pinned_x / pinned_y: one end in page-locked host memory, the other on
+    # the device
+    xp, yp = io in ("pinned", "pinned_x"), io in ("pinned", "pinned_y")
+    x = torch.from_numpy(X[0].copy()).pin_memory() if xp else torch.from_numpy(X[0].copy()).cuda()
+    y = torch.empty(d).pin_memory() if yp else torch.empty(d, device="cuda")
     torch.cuda.synchronize()
     cs.cs_decode_layer(layer, None, x, y, cs.select_params(cs.CS_SEL_EXACT), ws, stream=s,
                        idx=idx, count=cnt)
