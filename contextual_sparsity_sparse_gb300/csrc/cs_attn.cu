@@ -17,9 +17,9 @@
 // Grids span every head slot (the launch never depends on the device-side
 // count): slot m < count takes head idx[m], the others exit or write zero
 // partials.
-//  1. query: (slot, block of four W_q rows) CTAs; each row is spread over the
+//  1. query: (slot, block of five W_q rows) CTAs; each row is spread over the
 //     CTA (thread t takes 16-byte vectors t + 256 i), x in registers, one
-//     block reduction per four rows.
+//     block reduction per five rows.
 //  2. attend, split over the keys (flash-decoding): a (slot, split) CTA owns
 //     2048 / (vectors per key) keys, i.e. 32 KB of K and 32 KB of V, all of it
 //     loaded into registers before waiting for the query; it forms its
@@ -28,9 +28,9 @@
 //  3. combine and project: a (slot, 64-vector column chunk) CTA merges the
 //     head's splits in split order (M = max m, L = sum l e^(m - M),
 //     o = sum o_s e^(m - M) / L) and applies its chunk of W_o[:, h] o (four
-//     row groups added in order); a thread's rows (all of them up to
-//     d_head 128) are loaded before the wait, so they stream in while the
-//     attend kernel runs.
+//     row groups added in order); a thread's first 24 rows (96 of d_head 128)
+//     are loaded before the wait, so they stream in while the attend kernel
+//     runs (all 32 would need registers that keep an attend CTA off the SM).
 //  4. the FFN's fixed-order reduction adds the per-slot partials.
 // Kernels 1-3 let their dependents launch only after their own wait, so when
 // kernels 2 and 3 start the selection that wrote the head list has finished
@@ -49,10 +49,10 @@ constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kAttnMaxS = 16384;
 constexpr int kSplitVec = 2048;   // 16-byte vectors of K (and of V) per split: 8 per thread
 constexpr int kKV = kSplitVec / kAttnThreads;
-constexpr int kQRows = 4;         // W_q rows per query CTA
+constexpr int kQRows = 5;         // W_q rows per query CTA (10 heads of 128 rows: 260 CTAs, one wave)
 constexpr int kOVec = 64;         // 16-byte column vectors of the output projection per CTA
 constexpr int kOGroups = kAttnThreads / kOVec;
-constexpr int kOPre = 32;         // W_o rows per thread loaded before the wait (all of them up to d_head 128)
+constexpr int kOPre = 24;         // W_o rows per thread loaded before the wait (the registers leave room for an attend CTA)
 
 struct AttnK {
     const uint8_t *w_q, *w_o_t, *k, *v;
@@ -92,7 +92,7 @@ __device__ __forceinline__ int slot_head(const AttnK &a, int m, bool flag) {
     return h;
 }
 
-// 1. rows r0 .. r0+3 of q for the head in slot m (scaled by 1/sqrt(d_head)).
+// 1. rows r0 .. r0+4 of q for the head in slot m (scaled by 1/sqrt(d_head)).
 template <typename T, int NV>
 __global__ void __launch_bounds__(kAttnThreads) attn_q_kernel(const AttnK a) {
     constexpr int V = Vec<T>::N;
@@ -389,6 +389,7 @@ cudaError_t run_attn(const AttnK &k, cudaStream_t s) {
     cudaError_t e;
     if (nv <= kAttnThreads) e = launch(attn_q_kernel<T, 1>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     else if (nv <= 2 * kAttnThreads) e = launch(attn_q_kernel<T, 2>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
+    else if (nv <= 3 * kAttnThreads) e = launch(attn_q_kernel<T, 3>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     else if (nv <= 4 * kAttnThreads) e = launch(attn_q_kernel<T, 4>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     else e = launch(attn_q_kernel<T, 8>, gq, dim3(kAttnThreads), 0, s, pdl_enabled(), k);
     if (e != cudaSuccess) return e;
