@@ -778,7 +778,7 @@ def run_union(args, W, rank, world):
     d, f, B = W["d"], W["f"], W["union"]
     words = (f + 31) // 32
     tdt = torch.bfloat16 if W["dt"] == 2 else torch.float16
-    NCU, NM = 3, 32
+    NCU, NM = args.ncopy or 3, 32
     copies = []
     for l in range(NCU):
         t = {}
@@ -1099,7 +1099,7 @@ def run_attn(args, W, rank, world):
                    "l2": f"inputs larger than L2: {NCOPY} layer copies ({NCOPY * 2 * (H * dh * d + H * S * dh) * (4 if W['dt'] == 0 else 2) / 1e9:.2f} GB) and {NX} inputs rotate",
                    "step": "cs_predict (one score per head) + cs_select (top-k heads) + cs_sparse_attention, graphs of up to 200 steps"},
         "clocks": clocks,
-        "gpu_launches": 6 * K,   # predictor (2), select, query, core, reduce
+        "gpu_launches": 7 * K,   # predictor (2), select, query, attend, output, reduce
         "roofline": {"bound": "hbm", "kernel": "cs_sparse_attention (per-head attention + fixed-order reduce)",
                      "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",

@@ -3,8 +3,8 @@
 // Union source: "Contextual Sparsity and Activation Predictors", section "When
 // it breaks": the tokens of a batch have different active sets and the layer
 // must read their union.  umask = OR over tokens; uidx = set bits ascending.
-// One CTA: each thread ORs a contiguous run of words (kept in registers when
-// it holds at most four), a block scan places the run's ids.
+// Two kernels over 128-word blocks: the OR (one word per thread), then the
+// ids, each block placing its own after the set bits of the words before it.
 //
 // Packer source: "Contextual Sparsity: Activation-Aware LLM Inference and the
 // Deja Vu Paradigm", section "Kernel-Level Implementation" (indexing into the
@@ -18,11 +18,9 @@ namespace cs {
 
 namespace {
 
-constexpr int kUnionThreads = 1024;
-constexpr int kUnionWords = 4;   // words per thread kept in registers (f <= 131072)
+constexpr int kUnionThreads = 128;   // words (one per thread) per CTA
 
-// OR of word w over the B masks, 32 (then 8) loads in flight at a time: one
-// CTA does the whole union, so it is bound by load latency, not bandwidth.
+// OR of word w over the B masks, 32 (then 8) loads in flight at a time.
 __device__ __forceinline__ uint32_t or_word(const uint32_t *masks, int B, int words, int w) {
     uint32_t acc = 0;
     int b = 0;
@@ -44,68 +42,50 @@ __device__ __forceinline__ uint32_t or_word(const uint32_t *masks, int B, int wo
     return acc;
 }
 
-__global__ void __launch_bounds__(kUnionThreads)
-union_kernel(const uint32_t *masks, int B, int f, uint32_t *__restrict__ umask,
-             int32_t *__restrict__ uidx, int32_t *__restrict__ ucount) {
-    __shared__ int wsum[32];
-    const int tid = threadIdx.x;
-    const int words = (f + 31) >> 5;
-    const int E = (words + kUnionThreads - 1) / kUnionThreads;
-    const int beg = min(tid * E, words), end = min(beg + E, words);
-    const uint32_t tail = (f & 31) ? ((1u << (f & 31)) - 1u) : 0xffffffffu;
+// 1. umask: one word per thread (bits past f cleared).
+__global__ void __launch_bounds__(kUnionThreads) union_or_kernel(const uint32_t *masks, int B, int f,
+                                                                  uint32_t *umask) {
     pdl_launch_dependents();
-    pdl_wait();
-    if (E <= kUnionWords) {
-        // one pass: this thread's words stay in registers between the count
-        // and the writes
-        uint32_t u[kUnionWords];
-        int n = 0;
-#pragma unroll
-        for (int e = 0; e < kUnionWords; ++e) {
-            const int w = beg + e;
-            u[e] = 0;
-            if (w < end) {
-                u[e] = or_word(masks, B, words, w);
-                if (w == words - 1) u[e] &= tail;
-                n += __popc(u[e]);
-            }
-        }
-        int total;
-        int pos = block_excl_scan(n, wsum, &total);
-#pragma unroll
-        for (int e = 0; e < kUnionWords; ++e) {
-            const int w = beg + e;
-            if (w < end) {
-                uint32_t x = u[e];
-                umask[w] = x;
-                while (x) {
-                    uidx[pos++] = w * 32 + __ffs(x) - 1;
-                    x &= x - 1;
-                }
-            }
-        }
-        if (tid == 0) *ucount = total;
-        return;
-    }
-    int n = 0;
-    for (int w = beg; w < end; ++w) {
+    pdl_wait();  // the masks may come from an earlier kernel
+    const int words = (f + 31) >> 5;
+    const int w = blockIdx.x * kUnionThreads + threadIdx.x;
+    if (w < words) {
         uint32_t u = or_word(masks, B, words, w);
-        if (w == words - 1) u &= tail;
-        n += __popc(u);
-    }
-    int total;
-    int pos = block_excl_scan(n, wsum, &total);
-    for (int w = beg; w < end; ++w) {
-        uint32_t u = or_word(masks, B, words, w);
-        if (w == words - 1) u &= tail;
+        if (w == words - 1 && (f & 31)) u &= (1u << (f & 31)) - 1u;
         umask[w] = u;
-        while (u) {
-            const int bit = __ffs(u) - 1;
-            uidx[pos++] = w * 32 + bit;
-            u &= u - 1;
-        }
     }
-    if (tid == 0) *ucount = total;
+}
+
+// 2. uidx: a CTA's ids start after the set bits of all earlier words (summed
+//    here from umask); a block scan places each word's ids, each warp stages
+//    its run in shared memory and stores it with coalesced writes.  The last
+//    CTA writes the count.
+__global__ void __launch_bounds__(kUnionThreads) union_ids_kernel(const uint32_t *umask, int f, int32_t *uidx,
+                                                                  int32_t *ucount) {
+    __shared__ int32_t stage[kUnionThreads / 32][32 * 32];   // a warp's ids: at most 32 per lane
+    __shared__ int wsum[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int words = (f + 31) >> 5;
+    const int w0 = blockIdx.x * kUnionThreads;
+    pdl_launch_dependents();
+    pdl_wait();  // umask comes from the OR kernel
+    int part = 0;
+    for (int w = tid; w < w0; w += kUnionThreads) part += __popc(ld_dep(umask + w));
+    int before;
+    (void)block_excl_scan(part, wsum, &before);
+    const int w = w0 + tid;
+    const uint32_t u = w < words ? ld_dep(umask + w) : 0u;
+    const int n = __popc(u);
+    int total;
+    const int pos = block_excl_scan(n, wsum, &total);
+    const int wbase = __shfl_sync(kFull, pos, 0);
+    int *st = stage[warp];
+    int o = pos - wbase;
+    for (uint32_t x = u; x; x &= x - 1) st[o++] = w * 32 + __ffs(x) - 1;
+    __syncwarp();
+    const int run = __shfl_sync(kFull, pos - wbase + n, 31);
+    for (int q = lane; q < run; q += 32) uidx[before + wbase + q] = st[q];
+    if (blockIdx.x == gridDim.x - 1 && tid == 0) *ucount = before + total;
 }
 
 template <typename S> __device__ __forceinline__ float load_as_float(const void *p, size_t i);
@@ -164,8 +144,12 @@ cudaError_t pick_dst(const void *src, int rows, int cols, int ld_src, void *dst,
 }  // namespace
 
 cudaError_t launch_union(const UnionArgs &a, cudaStream_t s) {
-    return launch(union_kernel, dim3(1), dim3(kUnionThreads), 0, s, pdl_enabled(), a.masks, a.B, a.f,
-                  a.umask, a.uidx, a.ucount);
+    const int words = (a.f + 31) >> 5;
+    const dim3 g((words + kUnionThreads - 1) / kUnionThreads);
+    cudaError_t e = launch(union_or_kernel, g, dim3(kUnionThreads), 0, s, pdl_enabled(), a.masks, a.B, a.f, a.umask);
+    if (e != cudaSuccess) return e;
+    return launch(union_ids_kernel, g, dim3(kUnionThreads), 0, s, pdl_enabled(),
+                  static_cast<const uint32_t *>(a.umask), a.f, a.uidx, a.ucount);
 }
 
 cudaError_t launch_transpose(const void *src, cs_dtype st, int rows, int cols, int ld_src, void *dst,
