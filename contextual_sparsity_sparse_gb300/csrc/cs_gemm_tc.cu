@@ -701,26 +701,50 @@ template <int MT>
 __global__ void __launch_bounds__(256) tc_reduce_kernel(const TcArgs a, int P, const float *resid, float scale,
                                                        float *y) {
     constexpr int kCols = kTileM * MT;
+    static_assert(kCols == 256, "a CTA's 256 outputs form one column group");
+    constexpr int kMaxSlots = 256;      // partial slots per group: at most the CTAs (the path needs G <= 256)
+    __shared__ int s_slot[kMaxSlots];   // the group's partial slots, in CTA order
+    __shared__ int s_n;
     pdl_launch_dependents();
     pdl_wait();
-    const int m = blockIdx.x * 256 + threadIdx.x, b = blockIdx.y;
-    if (m >= a.d) return;
-    int n = *a.count;
-    if (n < 0 || n > a.f) n = n < 0 ? 0 : a.f;
-    const int NG = (a.d + kCols - 1) / kCols;
-    const int NKB = (n + kKB - 1) / kKB;
-    const long long U = (long long)NG * NKB;
-    const int g = m / kCols;
-    float sum = 0.f;
-    if (U > 0) {
-        const int c_lo = sk_owner((long long)g * NKB, U, P), c_hi = sk_owner((long long)(g + 1) * NKB - 1, U, P);
-        for (int c = c_lo; c <= c_hi; ++c) {
-            const long long st = sk_start(c, U, P);
-            if (sk_start(c + 1, U, P) == st) continue;  // an empty range wrote no slot
-            const int seg = g - (int)(st / NKB);
-            sum += __ldcg(a.part + ((size_t)(c * 2 + seg) * a.B + b) * kCols + (m - g * kCols));
+    // a CTA's 256 outputs lie in one column group (kCols = 256): its slots
+    // are found once, by one warp, instead of by every thread
+    const int g = blockIdx.x * 256 / kCols, b = blockIdx.y;
+    if (threadIdx.x < 32) {
+        int n = *a.count;
+        if (n < 0 || n > a.f) n = n < 0 ? 0 : a.f;
+        const int NG = (a.d + kCols - 1) / kCols;
+        const int NKB = (n + kKB - 1) / kKB;
+        const long long U = (long long)NG * NKB;
+        int cnt = 0;
+        if (U > 0) {
+            const int c_lo = sk_owner((long long)g * NKB, U, P), c_hi = sk_owner((long long)(g + 1) * NKB - 1, U, P);
+            for (int c0 = c_lo; c0 <= c_hi; c0 += 32) {
+                const int c = c0 + (int)threadIdx.x;
+                bool has = false;
+                int slot = 0;
+                if (c <= c_hi) {
+                    const long long st = sk_start(c, U, P);
+                    has = sk_start(c + 1, U, P) != st;   // an empty range wrote no slot
+                    slot = c * 2 + (g - (int)(st / NKB));
+                }
+                const unsigned m = __ballot_sync(kFull, has);
+                if (has) {
+                    const int pos = cnt + __popc(m & ((1u << threadIdx.x) - 1u));
+                    if (pos < kMaxSlots) s_slot[pos] = slot;
+                }
+                cnt += __popc(m);
+            }
         }
+        if (threadIdx.x == 0) s_n = cnt < kMaxSlots ? cnt : kMaxSlots;
     }
+    __syncthreads();
+    const int m = blockIdx.x * 256 + threadIdx.x;
+    if (m >= a.d) return;
+    float sum = 0.f;
+    const int ns = s_n;
+    for (int i = 0; i < ns; ++i)
+        sum += __ldcg(a.part + ((size_t)s_slot[i] * a.B + b) * kCols + (m - g * kCols));
     const size_t o = (size_t)b * a.d + m;
     y[o] = resid ? fmaf(scale, sum, resid[o]) : sum;
 }
@@ -833,7 +857,7 @@ bool tc_path_applies(const FfnArgs &f) {
     // down GEMM: stream-K partials (2 slots x 256 columns per CTA and token)
     // fit the workspace's partial-sum region, and a CTA's range spans <= 2
     // column groups; gate GEMM: at most 2P tiles, so a range spans <= 3 tiles
-    if (f.d < 512 || (f.d + 255) / 256 > f.G) return false;
+    if (f.d < 512 || (f.d + 255) / 256 > f.G || f.G > 256) return false;
     if ((f.f + kTileM - 1) / kTileM > 2 * f.G) return false;
     return true;
 }
