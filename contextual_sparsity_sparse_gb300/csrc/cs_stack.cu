@@ -277,6 +277,13 @@ struct CacheEntry {
 // nodes do not report their functions): host I/O then uses copies.
 bool g_io_nodes_unusable = false;
 
+// CS_GRAPH_IO=0 stages host x / y with copies around the graph launch
+// instead of the graph's own copy kernels (read at every call).
+bool graph_io_enabled() {
+    const char *v = getenv("CS_GRAPH_IO");
+    return !(v && v[0] == '0');
+}
+
 std::mutex g_mu;
 std::unordered_map<std::string, CacheEntry> g_cache;
 constexpr size_t kMaxCached = 64;
@@ -577,7 +584,7 @@ cs_status cs_decode_stack(const cs_ffn_layer *layers, const cs_predictor *preds,
         Events E;
         return enqueue_stack(p, sm, two ? sp : sm, E);
     };
-    if (x_host && xm) {
+    if (x_host && xm && graph_io_enabled()) {
         // the graph's first and last nodes read and write it in place
         p.io_src = static_cast<const float *>(xm);
         p.io_dst = static_cast<float *>(xm);
@@ -648,7 +655,7 @@ cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, c
 
     cudaStream_t s = (cudaStream_t)stream;
     auto enq = [&]() { return enqueue_layer(p, s); };
-    if ((x_host || y_host) && (!x_host || xm) && (!y_host || ym)) {
+    if ((x_host || y_host) && (!x_host || xm) && (!y_host || ym) && graph_io_enabled()) {
         // the graph's first and last nodes read x and write y in place
         p.io_src = x_host ? static_cast<const float *>(xm) : nullptr;
         p.io_dst = y_host ? static_cast<float *>(ym) : nullptr;

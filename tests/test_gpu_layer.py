@@ -56,9 +56,12 @@ def three_calls(layer, pred, X, params, f, d, s):
     return idx.cpu().numpy()[0, :n], y.cpu().numpy()[0]
 
 
-@pytest.mark.parametrize("io", ["device", "pinned"])
+@pytest.mark.parametrize("io", ["device", "pinned", "pinned-copies"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_layer_topk(case, io):
+def test_layer_topk(case, io, monkeypatch):
+    """pinned: the graph's own copy kernels read x and write y; pinned-copies
+    (CS_GRAPH_IO=0): copies around the graph launch."""
+    monkeypatch.setenv("CS_GRAPH_IO", "0" if io == "pinned-copies" else "1")
     name, d, f, r, dt, glu, rho = case
     H = HostLayer(d, f, r, dt, glu=glu, seed=0, rho=rho)
     layer, pred = H.device()

@@ -212,11 +212,15 @@ def test_stack_inside_caller_capture():
     assert np.array_equal(x.cpu().numpy().view(np.uint32), ref.cpu().numpy().view(np.uint32))
 
 
+@pytest.mark.parametrize("graph_io", ["1", "0"])
 @pytest.mark.parametrize("L", [3, 4])
-def test_stack_with_pinned_host_x(L):
-    """x_0 in page-locked host memory: copied in and x_L copied back by the
-    call; the result is the device-x call's, bit for bit, and several host
-    buffers replay one cached graph.  Pageable host memory is refused."""
+def test_stack_with_pinned_host_x(L, graph_io, monkeypatch):
+    """x_0 in page-locked host memory: read and x_L written back by the
+    call (by the graph's own copy kernels, or with CS_GRAPH_IO=0 by copies
+    around the launch); the result is the device-x call's, bit for bit, and
+    several host buffers replay one cached graph.  Pageable host memory is
+    refused."""
+    monkeypatch.setenv("CS_GRAPH_IO", graph_io)
     d, f, r = 512, 2048, 64
     Hs, layers, preds = stack_inputs(L, d, f, r, synth.BF16, glu=True)
     ws = cs.Workspace(d, f, r)
