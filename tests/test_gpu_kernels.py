@@ -318,7 +318,7 @@ def test_exact_ffn(dt, glu, shape):
 
 # -------------------------------------------------------------------- union
 
-@pytest.mark.parametrize("f", [1, 31, 33, 2048, 32768, 40000])
+@pytest.mark.parametrize("f", [1, 31, 33, 2048, 32768, 40000, 262145])
 @pytest.mark.parametrize("B", [1, 2, 7, 32])
 def test_union_bit_exact(f, B):
     M = synth.union_masks(3, B, f, 0.1)
@@ -334,6 +334,21 @@ def test_union_bit_exact(f, B):
     n = int(ucnt.item())
     assert n == wi.size and np.array_equal(uidx.cpu().numpy()[:n], wi)
     assert np.array_equal(umask.cpu().numpy().view(np.uint32), wm)
+
+
+@pytest.mark.parametrize("f", [4096, 40001])
+def test_union_all_set(f):
+    """Every bit set: each warp's 32 words hold 1,024 ids, the most its
+    staging buffer takes; the ids run 0 .. f-1 across every block."""
+    words = (f + 31) // 32
+    M = np.full((3, words), 0xffffffff, dtype=np.uint32)
+    m = torch.from_numpy(M.view(np.int32)).cuda()
+    umask = torch.zeros(words, dtype=torch.int32, device="cuda")
+    uidx = torch.full((f,), -1, dtype=torch.int32, device="cuda")
+    ucnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cs.cs_union_mask(m, f, umask, uidx, ucnt)
+    assert int(ucnt.item()) == f
+    assert np.array_equal(uidx.cpu().numpy(), np.arange(f, dtype=np.int32))
 
 
 # -------------------------------------------------------------------- layout
