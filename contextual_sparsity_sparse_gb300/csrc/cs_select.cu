@@ -10,7 +10,9 @@
 // Ranking: larger score first, equal scores by lower id, -0 == +0, NaN below
 // -inf (as order-preserving 32-bit keys).  Top-k needs the k-th key K and the
 // number of ties at K to take:
-//   1. min / max of the finite scores;
+//   1. bounds of the finite scores: their min / max (one CTA), or on a
+//      cluster the range of a fixed sample of the row, widened (scores past
+//      it share the end buckets);
 //   2. a 4096-bucket histogram of a monotone linear map of the score (NaN,
 //      -inf and +inf get their own end buckets), so buckets hold a handful of
 //      scores for any smooth distribution;
@@ -349,25 +351,31 @@ select_row_kernel(const float *scores, int f, int k, float tau,
 }
 
 // ---------------------------------------------------------------------------
-// Cluster row kernel: one cluster of kCl CTAs x 256 threads per token row.
+// Cluster row kernel: one cluster of kCl CTAs x 512 threads per token row.
 // CTA r owns the 32-aligned id slice [r*SL, r*SL + SL); thread t of it the
 // contiguous ids [t*E, t*E + E) of that slice, in registers.  The four steps
-// of the row kernel run with the per-element passes split kCl ways.  Small
-// data is pushed into every CTA's shared memory before a cluster barrier, so
-// that after it each CTA finds it locally: min / max, per-slice histogram
-// totals, the pivot bucket's members, and the (greater, tie) totals behind the
-// output offsets.  The one pull is the pivot slice's 512 bins from every CTA
-// (all loads in flight together).  Three cluster barriers when the pivot
-// bucket is small (every CTA then derives all CTAs' totals from the exchanged
-// members and the pushed above-bucket counts), four otherwise; no shared
-// memory is touched remotely after the last one, so CTAs may leave at once.
+// of the row kernel run with the per-element passes split kCl ways.  The
+// bucket map's bounds come from a fixed sample of the row that every CTA
+// reads alike, so they need no exchange.  Small data is pushed into every
+// CTA's shared memory before a cluster barrier, so that after it each CTA
+// finds it locally: per-slice histogram totals, the pivot bucket's members,
+// and the (greater, tie) totals behind the output offsets.  The one pull is
+// the pivot slice's 512 bins from every CTA (all loads in flight together).
+// Two cluster barriers when the sample has spread and the pivot bucket is
+// small (every CTA then derives all CTAs' totals from the exchanged members
+// and the pushed above-bucket counts); one more for a sample without spread
+// (the exact min / max exchanged) and one more for a crowded pivot bucket.
+// No shared memory is touched remotely after the last one, so CTAs may leave
+// at once.  Half an SM's threads per CTA: the per-element loops are short
+// and the block-wide steps still cheap (measured against 256 and 1024).
 // ---------------------------------------------------------------------------
 constexpr int kCl = 8;
-constexpr int kClT = 256;
-constexpr int kClW = kClT / 32;
 constexpr int kClBins = kBuckets / kCl;     // bins per CTA slice
 constexpr int kClMaxSlice = kSelectMaxF / kCl;
-static_assert(kClW == kCl, "warp w of a CTA handles histogram slice w");
+constexpr int kClT = 512;
+constexpr int kClW = kClT / 32;
+static_assert(kClW % kCl == 0, "whole warps per histogram slice");
+static_assert((((kSelectMaxF / kCl) + 31) / 32 * 32 + kClT - 1) / kClT <= 12, "ET covers the largest row");
 
 struct ClSmem {
     uint32_t hist[kBuckets];                  // local histogram
@@ -379,6 +387,7 @@ struct ClSmem {
     uint32_t pgt[kCl], peq[kCl];            // (greater, tie) totals from each CTA
     uint32_t pabove[kCl];                   // scores above the pivot bucket in each CTA
     uint32_t wab[kClW];
+    uint32_t wsl[kClW];                     // per-warp histogram sums
     uint32_t lkey[kCandSmall], lid[kCandSmall];
     uint32_t rhist[256];                      // radix digits (crowded bucket)
     uint32_t akey[kCandSmall], aid[kCandSmall];
@@ -389,7 +398,7 @@ struct ClSmem {
     uint32_t bucket, rem, ncand, pivot, need;
 };
 
-// Exclusive scan over a 256-thread block (unsigned, wraps modulo 2^32).
+// Exclusive scan over one CTA of the cluster kernel (unsigned, wraps modulo 2^32).
 __device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t *wsum, uint32_t *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t inc = v;
@@ -459,36 +468,64 @@ select_cl_kernel(const float *scores, int f, int k, float tau,
         }
     }
 
+    // one score of a fixed sample of the whole row per thread: the same ids
+    // in every CTA (f >= 2048 > kClT, so the ids are distinct and in range)
+    const float smp = KIND == SEL_TOPK ? ld_dep(s + (int)(((long long)tid * f) / kClT)) : 0.f;
+
     const int kk = k < 0 ? 0 : (k > f ? f : k);
     float pv = 0.f;
     bool pnan = false;
     int need = 0;
     bool fast = false;   // the per-CTA totals come from the exchanged candidates (no 4th barrier)
     if (KIND == SEL_TOPK && kk > 0 && kk < f) {
-        // 1. min / max of the finite scores, pushed to every CTA
-        float lo = INFINITY, hi = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < ET; ++e)
-            if (e < ne && fabsf(v[e]) < INFINITY) { lo = fminf(lo, v[e]); hi = fmaxf(hi, v[e]); }
-        lo = warp_min(lo);
-        hi = warp_max(hi);
+        // 1. bounds of the bucket map: the finite range of the sample widened
+        //    by half its width on either side, identical in every CTA (same
+        //    ids, exact min / max), so no exchange.  Scores beyond the bounds
+        //    fall into the end buckets; the map stays monotone, so the result
+        //    is exact whatever the bounds, which only set how many scores
+        //    share the pivot bucket.  A sample without spread (or a range
+        //    near overflow) takes the exact min / max of the row instead,
+        //    pushed to every CTA.
+        const bool sf = fabsf(smp) < INFINITY;
+        float lo = warp_min(sf ? smp : INFINITY), hi = warp_max(sf ? smp : -INFINITY);
         if (lane == 0) { S.wlo[warp] = lo; S.whi[warp] = hi; }
         __syncthreads();
-        if (warp == 0) {
-            lo = warp_min(lane < kClW ? S.wlo[lane] : INFINITY);
-            hi = warp_max(lane < kClW ? S.whi[lane] : -INFINITY);
-            if (lane < kCl) {
-                *cl.map_shared_rank(&S.plo[rank], lane) = lo;
-                *cl.map_shared_rank(&S.phi[rank], lane) = hi;
+        float smin = warp_min(lane < kClW ? S.wlo[lane] : INFINITY);
+        float smax = warp_max(lane < kClW ? S.whi[lane] : -INFINITY);
+        const float half = 0.5f * (smax - smin);
+        const float wlo_ = smin - half, whi_ = smax + half;
+        if (smax > smin && fabsf(wlo_) < INFINITY && fabsf(whi_) < INFINITY &&
+            (float)(kBuckets - 4) / (whi_ - wlo_) < INFINITY) {
+            smin = wlo_;
+            smax = whi_;
+        } else {
+            lo = INFINITY;
+            hi = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < ET; ++e)
+                if (e < ne && fabsf(v[e]) < INFINITY) { lo = fminf(lo, v[e]); hi = fmaxf(hi, v[e]); }
+            lo = warp_min(lo);
+            hi = warp_max(hi);
+            __syncthreads();   // every warp has read the sample's partials
+            if (lane == 0) { S.wlo[warp] = lo; S.whi[warp] = hi; }
+            __syncthreads();
+            if (warp == 0) {
+                lo = warp_min(lane < kClW ? S.wlo[lane] : INFINITY);
+                hi = warp_max(lane < kClW ? S.whi[lane] : -INFINITY);
+                if (lane < kCl) {
+                    *cl.map_shared_rank(&S.plo[rank], lane) = lo;
+                    *cl.map_shared_rank(&S.phi[rank], lane) = hi;
+                }
             }
+            cl.sync();                                                    // (1)
+            smin = warp_min(lane < kCl ? S.plo[lane] : INFINITY);
+            smax = warp_max(lane < kCl ? S.phi[lane] : -INFINITY);
         }
-        cl.sync();                                                        // (1)
-        const float smin = warp_min(lane < kCl ? S.plo[lane] : INFINITY);
-        const float smax = warp_max(lane < kCl ? S.phi[lane] : -INFINITY);
         const float scale = smax > smin ? (float)(kBuckets - 4) / (smax - smin) : 0.f;
         const float off = -smin * scale;
-        // 2. local histogram; warp w pushes this CTA's total of slice w
-        //    (bins [w*512, w*512 + 512)) to every CTA
+        // 2. local histogram; this CTA's total of each slice w (bins
+        //    [w*512, w*512 + 512), summed by kClW / kCl warps) pushed to
+        //    every CTA
         int bk[ET];  // each score's bucket, kept for the candidate pass
 #pragma unroll
         for (int e = 0; e < ET; ++e) {
@@ -497,8 +534,9 @@ select_cl_kernel(const float *scores, int f, int k, float tau,
         }
         __syncthreads();
         {
-            constexpr int BPL = kClBins / 32;      // 16 bins per lane
-            const int bin0 = warp * kClBins + lane * BPL;
+            constexpr int WPS = kClW / kCl;                 // warps per slice
+            constexpr int BPL = kClBins / (32 * WPS);       // bins per lane
+            const int bin0 = warp * (kClBins / WPS) + lane * BPL;
             uint32_t sum = 0;
 #pragma unroll
             for (int q = 0; q < BPL; q += 4) {
@@ -506,7 +544,18 @@ select_cl_kernel(const float *scores, int f, int k, float tau,
                 sum += h4.x + h4.y + h4.z + h4.w;
             }
             sum = (uint32_t)warp_isum((int)sum);
-            if (lane < kCl) *cl.map_shared_rank(&S.ptot[rank][warp], lane) = sum;
+            if (WPS == 1) {
+                if (lane < kCl) *cl.map_shared_rank(&S.ptot[rank][warp], lane) = sum;
+            } else {
+                if (lane == 0) S.wsl[warp] = sum;
+                __syncthreads();
+                if (warp < kCl && lane < kCl) {
+                    uint32_t t = 0;
+#pragma unroll
+                    for (int q = 0; q < WPS; ++q) t += S.wsl[warp * WPS + q];
+                    *cl.map_shared_rank(&S.ptot[rank][warp], lane) = t;
+                }
+            }
         }
         cl.sync();                                                        // (2)
         // 3. the slice holding the kk-th largest (slice w holds higher scores
@@ -526,20 +575,28 @@ select_cl_kernel(const float *scores, int f, int k, float tau,
             above += t;
         }
         {
-            const int bin = owner * kClBins + 2 * tid;
-            uint2 got[kCl];
+            // BPT of the slice's bins per thread (threads past the slice idle)
+            constexpr int BPT = kClBins >= kClT ? kClBins / kClT : 1;
+            const int bin = owner * kClBins + BPT * tid;
+            const bool has = BPT * tid < kClBins;
+            uint32_t got[kCl][BPT];
 #pragma unroll
             for (int r = 0; r < kCl; ++r)
-                got[r] = *cl.map_shared_rank(reinterpret_cast<const uint2 *>(&S.hist[bin]), r);
-            uint32_t cb[2] = {0u, 0u};
 #pragma unroll
-            for (int r = 0; r < kCl; ++r) { cb[0] += got[r].x; cb[1] += got[r].y; }
-            const uint32_t own = cb[0] + cb[1];
+                for (int q = 0; q < BPT; ++q) got[r][q] = has ? *cl.map_shared_rank(&S.hist[bin + q], r) : 0u;
+            uint32_t cb[BPT], own = 0;
+#pragma unroll
+            for (int q = 0; q < BPT; ++q) {
+                cb[q] = 0u;
+#pragma unroll
+                for (int r = 0; r < kCl; ++r) cb[q] += got[r][q];
+                own += cb[q];
+            }
             uint32_t tot_o;
             const uint32_t pre = cta_excl_scan(own, S.usum, &tot_o);
             uint32_t run = above_owner + (tot_o - pre - own);
 #pragma unroll
-            for (int q = 1; q >= 0; --q) {
+            for (int q = BPT - 1; q >= 0; --q) {
                 if (run < (uint32_t)kk && run + cb[q] >= (uint32_t)kk) {
                     S.bucket = (uint32_t)(bin + q);
                     S.rem = (uint32_t)kk - run;
@@ -793,12 +850,10 @@ cudaError_t run_select_cl_kind(const SelectArgs &a, cudaStream_t s) {
 
 cudaError_t launch_select_cl(const SelectArgs &a, cudaStream_t s) {
     const int SL = (((a.f + kCl - 1) / kCl) + 31) & ~31;
-    const int E = (SL + kClT - 1) / kClT;
+    const int E = (SL + kClT - 1) / kClT;     // <= 12 for f <= kSelectMaxF
     if (E <= 4) return run_select_cl_kind<4>(a, s);
     if (E <= 8) return run_select_cl_kind<8>(a, s);
-    if (E <= 12) return run_select_cl_kind<12>(a, s);
-    if (E <= 16) return run_select_cl_kind<16>(a, s);
-    return run_select_cl_kind<24>(a, s);
+    return run_select_cl_kind<12>(a, s);
 }
 
 template <int ET, int KIND>
@@ -817,15 +872,9 @@ cudaError_t run_select_kind(const SelectArgs &a, cudaStream_t s) {
 
 cudaError_t launch_select_row(const SelectArgs &a, cudaStream_t s) {
     const int E = (a.f + kRowThreads - 1) / kRowThreads;
+    // rows of f < 2048 only (longer rows run on a cluster): E <= 2
     if (E <= 4) return run_select_kind<4>(a, s);
-    if (E <= 8) return run_select_kind<8>(a, s);
-    if (E <= 12) return run_select_kind<12>(a, s);
-    if (E <= 16) return run_select_kind<16>(a, s);
-    if (E <= 20) return run_select_kind<20>(a, s);
-    if (E <= 24) return run_select_kind<24>(a, s);
-    if (E <= 28) return run_select_kind<28>(a, s);
-    if (E <= 32) return run_select_kind<32>(a, s);
-    return run_select_kind<48>(a, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace

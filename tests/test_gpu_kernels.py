@@ -100,6 +100,40 @@ def test_topk_bit_exact(f):
             assert np.array_equal(M[b], synth.bits_from_bool(np.isin(np.arange(f), want)))
 
 
+def _tail_rows(f, seed):
+    """Rows that stress the bounds of the selection's bucket map: heavy tails,
+    a few huge outliers, a mostly-zero row, and a row whose every fourth score
+    is one constant (a sample of ids on any grid of multiples of 4 sees no
+    spread there)."""
+    rng = np.random.default_rng(seed)
+    cauchy = rng.standard_cauchy(f).astype(np.float32)
+    outl = rng.standard_normal(f).astype(np.float32)
+    outl[rng.choice(f, 5, replace=False)] = np.array([1e30, -1e30, 3e29, 1e20, -7e25], np.float32)
+    sparse = np.zeros(f, np.float32)
+    sparse[rng.choice(f, 100, replace=False)] = rng.random(100).astype(np.float32) + 0.25
+    grid = rng.standard_normal(f).astype(np.float32)
+    grid[::4] = 0.5
+    return np.stack([cauchy, outl, sparse, grid])
+
+
+@pytest.mark.parametrize("f", [2048, 28672, 49152])
+def test_topk_heavy_tails_bit_exact(f):
+    S = _tail_rows(f, 31 + f)
+    B = S.shape[0]
+    s = torch.from_numpy(S).cuda()
+    idx = torch.full((B, f), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(B, dtype=torch.int32, device="cuda")
+    mask = torch.zeros((B, (f + 31) // 32), dtype=torch.int32, device="cuda")
+    for k in sorted({1, 3, 5, 6, 50, 100, 101, f // 100, f // 7, f // 4, f // 2, f - 2}):
+        cs.cs_select(s, cs.select_params(cs.CS_SEL_TOPK, k), idx, cnt, mask)
+        I, N, M = idx.cpu().numpy(), cnt.cpu().numpy(), mask.cpu().numpy().view(np.uint32)
+        for b in range(B):
+            want = oracle.select_topk(S[b], k)
+            assert N[b] == want.size, (f, k, b)
+            assert np.array_equal(I[b, :N[b]], want), (f, k, b)
+            assert np.array_equal(M[b], synth.bits_from_bool(np.isin(np.arange(f), want))), (f, k, b)
+
+
 @pytest.mark.parametrize("f", SEL_F)
 def test_threshold_bit_exact(f):
     B = 2
