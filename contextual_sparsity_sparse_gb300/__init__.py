@@ -32,7 +32,8 @@ EXPORTS = ["cs_version", "cs_status_string", "cs_last_error", "cs_workspace_size
            "cs_workspace_init", "cs_get_device_error", "cs_pack_transpose", "cs_predict",
            "cs_select", "cs_sparse_ffn", "cs_exact_ffn", "cs_union_mask", "cs_decode_stack",
            "cs_stack_release", "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows",
-           "cs_hot_order", "cs_fit_scratch_size", "cs_fit_predictor", "cs_sparse_attention"]
+           "cs_hot_order", "cs_fit_scratch_size", "cs_fit_predictor", "cs_sparse_attention",
+           "cs_decode_attention"]
 
 
 class CsError(RuntimeError):
@@ -99,6 +100,8 @@ def lib():
             L.cs_permute_rows.argtypes = [P, I, I, P, I, I, I, P, I, P]
             L.cs_hot_order.argtypes = [P, I, P]
             L.cs_sparse_attention.argtypes = [C.POINTER(_Attn), P, P, P, P, P, I, P, P, S, P]
+            L.cs_decode_attention.argtypes = [C.POINTER(_Attn), C.POINTER(_Pred), P, P, C.POINTER(_Sel),
+                                              P, P, I, P, S, P, P, P]
             L.cs_fit_scratch_size.argtypes = [I, I, I, I]
             L.cs_fit_scratch_size.restype = S
             L.cs_fit_predictor.argtypes = [C.POINTER(_Layer), C.POINTER(_Pred), P, I, C.c_double, P, S, P]
@@ -106,7 +109,7 @@ def lib():
                          "cs_predict", "cs_select", "cs_sparse_ffn", "cs_exact_ffn",
                          "cs_union_mask", "cs_decode_stack", "cs_stack_release",
                          "cs_sparse_ffn_noalloc", "cs_decode_layer", "cs_permute_rows", "cs_hot_order",
-                         "cs_fit_predictor", "cs_sparse_attention"):
+                         "cs_fit_predictor", "cs_sparse_attention", "cs_decode_attention"):
                 getattr(L, name).restype = I
             _lib = L
     return _lib
@@ -332,6 +335,18 @@ def cs_sparse_attention(layer: AttnLayer, x, heads, count, k_cache, v_cache, y, 
     _check(lib().cs_sparse_attention(C.byref(layer.c), _ptr(x), _ptr(heads), _ptr(count), _ptr(k_cache),
                                      _ptr(v_cache), int(k_cache.shape[1]), _ptr(y), ws.ptr, ws.nbytes,
                                      _stream(stream)))
+
+
+def cs_decode_attention(layer: AttnLayer, pred, x, y, params, k_cache, v_cache, ws: Workspace, stream=None,
+                        heads=None, count=None):
+    """One token's head-sparse attention step: the predictor scores the heads,
+    the selection picks them, y = their attention over the KV cache (see
+    include/cs.h).  x and y may live on the GPU or in pinned host memory;
+    k_cache / v_cache are [n_heads, seq_len, d_head] CUDA tensors."""
+    d = layer.d
+    _check(lib().cs_decode_attention(C.byref(layer.c), C.byref(pred.c), _io_ptr(x, d), _io_ptr(y, d),
+                                     C.byref(params), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[1]),
+                                     ws.ptr, ws.nbytes, _stream(stream), _ptr(heads), _ptr(count)))
 
 
 def cs_fit_predictor(layer: FfnLayer, pred: Predictor, X, lam, stream=None):

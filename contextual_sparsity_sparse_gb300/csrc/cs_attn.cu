@@ -401,6 +401,108 @@ cudaError_t run_attn(const AttnK &k, cudaStream_t s) {
 
 }  // namespace
 
+namespace cs {
+
+// The launch geometry of one call: the split of the positions and where the
+// partial rows, queries and split records sit inside the workspace's G x dp
+// partial values (H partial rows, the H queries, then per head its splits'
+// (max, sum, o)).
+struct AttnGeom {
+    WsLayout WL;
+    int esz, nvk, sc, ns;
+    size_t need;
+};
+
+static AttnGeom attn_geom(const AttnCall &c) {
+    const cs_attn_layer &L = c.layer;
+    AttnGeom g;
+    g.WL = ws_layout(L.d, 1, 1, 1, device_sm_count());
+    g.esz = (int)dtype_size(L.dtype);
+    g.nvk = L.d_head * g.esz / 16;
+    g.sc = kSplitVec / g.nvk;
+    g.ns = (c.seq_len + g.sc - 1) / g.sc;
+    g.need = (size_t)L.n_heads * g.WL.dp + (size_t)L.n_heads * L.d_head + (size_t)L.n_heads * g.ns * (L.d_head + 2);
+    return g;
+}
+
+cs_status attn_check(const AttnCall &c, const char *who) {
+    const cs_attn_layer &L = c.layer;
+    if (L.dtype != CS_F32 && L.dtype != CS_F16 && L.dtype != CS_BF16) {
+        set_error("%s: bad dtype %d", who, (int)L.dtype);
+        return CS_ERR_INVALID;
+    }
+    const int esz = (int)dtype_size(L.dtype), V = 16 / esz;
+    const bool dh_ok = L.d_head >= V && L.d_head <= kAttnThreads && (L.d_head & (L.d_head - 1)) == 0;
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (L.d < V || L.d % V || L.n_heads < 1 || !dh_ok || !L.w_q || !L.w_o_t || !al16(L.w_q) || !al16(L.w_o_t) ||
+        !c.k_cache || !c.v_cache || !al16(c.k_cache) || !al16(c.v_cache)) {
+        set_error("%s: d a multiple of %d, d_head a power of two in [%d, %d], and 16-byte aligned weights and "
+                  "caches", who, V, V, kAttnThreads);
+        return CS_ERR_INVALID;
+    }
+    if (c.seq_len < 1 || c.seq_len > kAttnMaxS) {
+        set_error("%s: seq_len=%d outside [1, %d]", who, c.seq_len, kAttnMaxS);
+        return c.seq_len < 1 ? CS_ERR_INVALID : CS_ERR_UNSUPPORTED;
+    }
+    return CS_OK;
+}
+
+cs_status attn_check_ws(const AttnCall &c, const char *who) {
+    const cs_attn_layer &L = c.layer;
+    const int V = 16 / (int)dtype_size(L.dtype);
+    if (!c.ws || (reinterpret_cast<uintptr_t>(c.ws) & 255u)) {
+        set_error("%s: workspace is null or not 256-byte aligned", who);
+        return CS_ERR_WORKSPACE;
+    }
+    const AttnGeom g = attn_geom(c);
+    if (c.ws_bytes < g.WL.total) {
+        set_error("%s: workspace too small: %zu bytes given, %zu needed", who, c.ws_bytes, g.WL.total);
+        return CS_ERR_WORKSPACE;
+    }
+    if (g.need > (size_t)g.WL.G * g.WL.dp || L.d / V > 8 * kAttnThreads) {
+        set_error("%s: %d heads of %d over %d positions (d=%d) need more than the %d x %d partial values of "
+                  "the workspace, or d is too wide", who, L.n_heads, L.d_head, c.seq_len, L.d, g.WL.G, g.WL.dp);
+        return CS_ERR_UNSUPPORTED;
+    }
+    return CS_OK;
+}
+
+cudaError_t attn_launch(const AttnCall &c, const float *x, const int32_t *heads, const int32_t *count, float *y,
+                        cudaStream_t s) {
+    const cs_attn_layer &L = c.layer;
+    const AttnGeom g = attn_geom(c);
+    AttnK k;
+    k.w_q = static_cast<const uint8_t *>(L.w_q);
+    k.w_o_t = static_cast<const uint8_t *>(L.w_o_t);
+    k.k = static_cast<const uint8_t *>(c.k_cache);
+    k.v = static_cast<const uint8_t *>(c.v_cache);
+    k.x = x;
+    k.idx = heads;
+    k.count = count;
+    k.part = reinterpret_cast<float *>(static_cast<char *>(c.ws) + g.WL.part);
+    k.qbuf = k.part + (size_t)L.n_heads * g.WL.dp;
+    k.split = k.qbuf + (size_t)L.n_heads * L.d_head;
+    k.nvk = g.nvk;
+    k.sc = g.sc;
+    k.ns = g.ns;
+    k.err = static_cast<uint32_t *>(c.ws);
+    k.d = L.d;
+    k.H = L.n_heads;
+    k.dh = L.d_head;
+    k.S = c.seq_len;
+    k.dp = g.WL.dp;
+    k.row_bytes = (size_t)L.d * g.esz;
+    cudaError_t e = L.dtype == CS_F32 ? run_attn<float>(k, s)
+                    : L.dtype == CS_F16 ? run_attn<__half>(k, s)
+                                        : run_attn<__nv_bfloat16>(k, s);
+    // the reduction adds the partial rows of the selected slots only (the
+    // count is read on the device and clamped to the head count)
+    if (e == cudaSuccess) e = launch_ffn_reduce(k.part, L.n_heads, 1, L.d, g.WL.dp, nullptr, 1.f, y, s, count);
+    return e;
+}
+
+}  // namespace cs
+
 extern "C" {
 
 cs_status cs_sparse_attention(const cs_attn_layer *layer, const float *x, const int32_t *heads,
@@ -410,76 +512,18 @@ cs_status cs_sparse_attention(const cs_attn_layer *layer, const float *x, const 
         set_error("cs_sparse_attention: layer, x, heads, count, k_cache, v_cache and y are required");
         return CS_ERR_INVALID;
     }
-    const cs_attn_layer &L = *layer;
-    if (L.dtype != CS_F32 && L.dtype != CS_F16 && L.dtype != CS_BF16) {
-        set_error("cs_sparse_attention: bad dtype %d", (int)L.dtype);
-        return CS_ERR_INVALID;
-    }
-    const int esz = (int)dtype_size(L.dtype), V = 16 / esz;
-    const bool dh_ok = L.d_head >= V && L.d_head <= kAttnThreads && (L.d_head & (L.d_head - 1)) == 0;
-    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if (L.d < V || L.d % V || L.n_heads < 1 || !dh_ok || !L.w_q || !L.w_o_t || !al16(L.w_q) || !al16(L.w_o_t) ||
-        !al16(x) || !al16(k_cache) || !al16(v_cache) || (reinterpret_cast<uintptr_t>(heads) & 3u) ||
+    const AttnCall c{*layer, k_cache, v_cache, seq_len, ws, ws_bytes};
+    cs_status st = attn_check(c, "cs_sparse_attention");
+    if (st != CS_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(heads) & 3u) ||
         (reinterpret_cast<uintptr_t>(count) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u) || x == y) {
-        set_error("cs_sparse_attention: d a multiple of %d, d_head a power of two in [%d, %d], 16-byte aligned "
-                  "weights, caches and x, and y not aliasing x", V, V, kAttnThreads);
+        set_error("cs_sparse_attention: x 16-byte aligned, heads, count and y 4-byte aligned, and y not "
+                  "aliasing x");
         return CS_ERR_INVALID;
     }
-    if (seq_len < 1 || seq_len > kAttnMaxS) {
-        set_error("cs_sparse_attention: seq_len=%d outside [1, %d]", seq_len, kAttnMaxS);
-        return seq_len < 1 ? CS_ERR_INVALID : CS_ERR_UNSUPPORTED;
-    }
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) {
-        set_error("cs_sparse_attention: workspace is null or not 256-byte aligned");
-        return CS_ERR_WORKSPACE;
-    }
-    // the partial outputs use the workspace's per-CTA partial rows (one per head)
-    const WsLayout WL = ws_layout(L.d, 1, 1, 1, device_sm_count());
-    if (ws_bytes < WL.total) {
-        set_error("cs_sparse_attention: workspace too small: %zu bytes given, %zu needed", ws_bytes, WL.total);
-        return CS_ERR_WORKSPACE;
-    }
-    // inside the workspace's G partial rows: H partial rows, the H queries,
-    // then per head its splits' (max, sum, o)
-    const int nvk = L.d_head * esz / 16;
-    const int sc = kSplitVec / nvk;
-    const int ns = (seq_len + sc - 1) / sc;
-    const size_t need = (size_t)L.n_heads * WL.dp + (size_t)L.n_heads * L.d_head +
-                        (size_t)L.n_heads * ns * (L.d_head + 2);
-    if (need > (size_t)WL.G * WL.dp || L.d / V > 8 * kAttnThreads) {
-        set_error("cs_sparse_attention: %d heads of %d over %d positions (d=%d) need more than the %d x %d "
-                  "partial values of the workspace, or d is too wide", L.n_heads, L.d_head, seq_len, L.d, WL.G,
-                  WL.dp);
-        return CS_ERR_UNSUPPORTED;
-    }
-    AttnK k;
-    k.w_q = static_cast<const uint8_t *>(L.w_q);
-    k.w_o_t = static_cast<const uint8_t *>(L.w_o_t);
-    k.k = static_cast<const uint8_t *>(k_cache);
-    k.v = static_cast<const uint8_t *>(v_cache);
-    k.x = x;
-    k.idx = heads;
-    k.count = count;
-    k.part = reinterpret_cast<float *>(static_cast<char *>(ws) + WL.part);
-    k.qbuf = k.part + (size_t)L.n_heads * WL.dp;
-    k.split = k.qbuf + (size_t)L.n_heads * L.d_head;
-    k.nvk = nvk;
-    k.sc = sc;
-    k.ns = ns;
-    k.err = static_cast<uint32_t *>(ws);
-    k.d = L.d;
-    k.H = L.n_heads;
-    k.dh = L.d_head;
-    k.S = seq_len;
-    k.dp = WL.dp;
-    k.row_bytes = (size_t)L.d * esz;
-    cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = L.dtype == CS_F32 ? run_attn<float>(k, s)
-                    : L.dtype == CS_F16 ? run_attn<__half>(k, s)
-                                        : run_attn<__nv_bfloat16>(k, s);
-    // the reduction adds the partial rows of the selected slots only (the
-    // count is read on the device and clamped to the head count)
-    if (e == cudaSuccess) e = launch_ffn_reduce(k.part, L.n_heads, 1, L.d, WL.dp, nullptr, 1.f, y, s, count);
+    st = attn_check_ws(c, "cs_sparse_attention");
+    if (st != CS_OK) return st;
+    const cudaError_t e = attn_launch(c, x, heads, count, y, (cudaStream_t)stream);
     return e == cudaSuccess ? CS_OK : cuda_fail(e, "cs_sparse_attention");
 }
 

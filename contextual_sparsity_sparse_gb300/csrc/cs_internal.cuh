@@ -357,6 +357,23 @@ struct FfnArgs {
 };
 cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s);
 
+// Head-sparse attention (cs_attn.cu) over one layer's KV cache, with the
+// workspace whose partial rows it uses.
+struct AttnCall {
+    cs_attn_layer layer;
+    const void *k_cache, *v_cache;
+    int seq_len;
+    void *ws;
+    size_t ws_bytes;
+};
+// Checks the layer, the caches and the length (host only), then the
+// workspace (its size depends on the device's SM count); both set the error.
+cs_status attn_check(const AttnCall &c, const char *who);
+cs_status attn_check_ws(const AttnCall &c, const char *who);
+// Enqueues y = the listed heads' attention (x 16-byte aligned, y not x).
+cudaError_t attn_launch(const AttnCall &c, const float *x, const int32_t *heads, const int32_t *count, float *y,
+                        cudaStream_t s);
+
 // Arguments of the gather kernels (one CTA per SM over a chunk of the list).
 struct FfnK {
     const uint8_t *w_gate, *w_up, *w_down_t;

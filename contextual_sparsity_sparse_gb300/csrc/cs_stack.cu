@@ -59,6 +59,10 @@ struct StackPlan {
     // first) and host y (or the stack's x, written from p.y / p.x last)
     const float *io_src = nullptr;
     float *io_dst = nullptr;
+    // one token's head-sparse attention instead of the FFN layers: the
+    // predictor scores the heads, the selection picks them (into
+    // trace_idx / trace_count when given), y = the attention
+    const AttnCall *attn = nullptr;
 };
 
 constexpr int kIoThreads = 256;
@@ -252,6 +256,28 @@ cudaError_t enqueue_stack(const StackPlan &p, cudaStream_t sm, cudaStream_t sp, 
     return cudaSuccess;
 }
 
+// Enqueue one token's head-sparse attention: y = attention(x, select(P(x))).
+cudaError_t enqueue_attention(const StackPlan &p, cudaStream_t s) {
+    const Bufs b = bufs_of(p);
+    if (p.io_src) TRY(launch_io(0, IoCopy{p.io_src, p.x, p.d}, s));
+    const cs_predictor &P = p.preds[0];
+    PredictArgs a;
+    a.d = P.d; a.r = P.r; a.f = P.f; a.B = 1; a.dtype = P.dtype;
+    a.ld_down = P.ld_down; a.ld_up = P.ld_up; a.p_down = P.p_down; a.p_up = P.p_up;
+    a.x = p.x; a.h = b.h; a.scores = b.scores; a.err = b.err;
+    TRY(launch_predict(a, s));
+    SelectArgs sa;
+    sa.scores = b.scores; sa.B = 1; sa.f = p.f;
+    sa.kind = p.sel.mode == CS_SEL_TOPK ? SEL_TOPK : SEL_THRESHOLD;
+    sa.k = p.sel.k; sa.tau = p.sel.tau; sa.hot = 0;
+    sel_out(p, b, 0, &sa.idx, &sa.count);
+    sa.ld_idx = p.f; sa.mask = nullptr;
+    TRY(launch_select(sa, s));
+    TRY(attn_launch(*p.attn, p.x, sa.idx, sa.count, p.y, s));
+    if (p.io_dst) TRY(launch_io(1, IoCopy{p.y, p.io_dst, p.d}, s));
+    return cudaSuccess;
+}
+
 // Enqueue one layer's step for one token: y = FFN(x, select(P(x))).
 cudaError_t enqueue_layer(const StackPlan &p, cudaStream_t s) {
     const Bufs b = bufs_of(p);
@@ -293,7 +319,16 @@ std::string plan_key(const StackPlan &p, cudaStream_t sp, int dev) {
     auto put = [&](const void *v, size_t n) { k.append(static_cast<const char *>(v), n); };
     put(&dev, sizeof dev);
     put(&p.L, sizeof p.L);
-    put(p.layers, sizeof(cs_ffn_layer) * p.L);
+    const bool attn = p.attn != nullptr;
+    put(&attn, sizeof attn);
+    if (attn) {
+        put(&p.attn->layer, sizeof p.attn->layer);
+        put(&p.attn->k_cache, sizeof p.attn->k_cache);
+        put(&p.attn->v_cache, sizeof p.attn->v_cache);
+        put(&p.attn->seq_len, sizeof p.attn->seq_len);
+    } else {
+        put(p.layers, sizeof(cs_ffn_layer) * p.L);
+    }
     if (p.sel.mode != CS_SEL_EXACT) put(p.preds, sizeof(cs_predictor) * p.L);
     put(&p.x, sizeof p.x);
     put(&p.scale, sizeof p.scale);
@@ -373,6 +408,17 @@ cudaError_t update_io(CacheEntry &ce, const StackPlan &p) {
     return cudaSuccess;
 }
 
+// A predictor scoring f outputs from d inputs through rank r, with valid
+// pointers, pitches and dtype.
+bool pred_ok(const cs_predictor &P, int d, int f, int r) {
+    const int ldd = P.ld_down ? P.ld_down : P.d, ldu = P.ld_up ? P.ld_up : P.r;
+    const size_t ep = dtype_size(P.dtype);
+    return !(P.d != d || P.f != f || P.r != r || P.r < 1 || !P.p_down || !P.p_up || ldd < d || ldu < r ||
+             (ldd * ep) % 16 || (ldu * ep) % 16 || (reinterpret_cast<uintptr_t>(P.p_down) & 15u) ||
+             (reinterpret_cast<uintptr_t>(P.p_up) & 15u) || P.r > 8192 ||
+             (P.dtype != CS_F32 && P.dtype != CS_F16 && P.dtype != CS_BF16));
+}
+
 // Shape and layout checks shared by the stack and the single-layer step.
 cs_status check_models(const cs_ffn_layer *layers, const cs_predictor *preds, int L, bool exact,
                        int hot, const char *who) {
@@ -399,13 +445,7 @@ cs_status check_models(const cs_ffn_layer *layers, const cs_predictor *preds, in
             return CS_ERR_INVALID;
         }
         if (!exact) {
-            const cs_predictor &P = preds[l];
-            const int ldd = P.ld_down ? P.ld_down : P.d, ldu = P.ld_up ? P.ld_up : P.r;
-            const size_t ep = dtype_size(P.dtype);
-            if (P.d != d || P.f != f - hot || P.r != r || !P.p_down || !P.p_up || ldd < d || ldu < r ||
-                (ldd * ep) % 16 || (ldu * ep) % 16 || (reinterpret_cast<uintptr_t>(P.p_down) & 15u) ||
-                (reinterpret_cast<uintptr_t>(P.p_up) & 15u) || P.r > 8192 ||
-                (P.dtype != CS_F32 && P.dtype != CS_F16 && P.dtype != CS_BF16)) {
+            if (!pred_ok(preds[l], d, f - hot, r)) {
                 set_error("%s: predictor %d does not match the layers or is invalid (it must score the "
                           "f - hot = %d tail neurons)", who, l, f - hot);
                 return CS_ERR_INVALID;
@@ -675,6 +715,92 @@ cs_status cs_decode_layer(const cs_ffn_layer *layer, const cs_predictor *pred, c
     if (y_host) {
         cudaError_t e = cudaMemcpyAsync(y, p.y, xy_bytes, cudaMemcpyDeviceToHost, s);
         if (e != cudaSuccess) return cuda_fail(e, "cs_decode_layer(y copy)");
+    }
+    return CS_OK;
+}
+
+cs_status cs_decode_attention(const cs_attn_layer *layer, const cs_predictor *pred, const float *x, float *y,
+                              const cs_select_params *params, const void *k_cache, const void *v_cache,
+                              int seq_len, void *ws, size_t ws_bytes, cs_stream_t stream, int32_t *heads,
+                              int32_t *count) {
+    const char *who = "cs_decode_attention";
+    if (!layer || !pred || !params || !x || !y || x == y || (reinterpret_cast<uintptr_t>(x) & 3u) ||
+        (reinterpret_cast<uintptr_t>(y) & 3u) || (!heads) != (!count) ||
+        (reinterpret_cast<uintptr_t>(heads) & 3u) || (reinterpret_cast<uintptr_t>(count) & 3u)) {
+        set_error("cs_decode_attention: layer, pred, params, x and y are required (4-byte aligned, y not x); "
+                  "heads and count are given together or not at all");
+        return CS_ERR_INVALID;
+    }
+    cs_status st = check_params(params, who);
+    if (st != CS_OK) return st;
+    if (params->mode == CS_SEL_EXACT || params->hot != 0) {
+        set_error("cs_decode_attention: the heads are chosen by top-k or a threshold on the predictor's "
+                  "scores, without a hot prefix");
+        return CS_ERR_INVALID;
+    }
+    const AttnCall c{*layer, k_cache, v_cache, seq_len, ws, ws_bytes};
+    st = attn_check(c, who);
+    if (st != CS_OK) return st;
+    const int d = layer->d, H = layer->n_heads;
+    if (pred->d != d || pred->f != H) {
+        set_error("cs_decode_attention: the predictor must score the %d heads from the d = %d inputs", H, d);
+        return CS_ERR_INVALID;
+    }
+    st = attn_check_ws(c, who);
+    if (st != CS_OK) return st;
+    if (!pred_ok(*pred, d, H, pred->r)) {
+        set_error("cs_decode_attention: the predictor must score the %d heads from the d = %d inputs, with "
+                  "16-byte aligned weights and pitches", H, d);
+        return CS_ERR_INVALID;
+    }
+    bool x_host = false, y_host = false;
+    void *xm = nullptr, *ym = nullptr;
+    st = io_kind(x, &x_host, &xm, who, "x");
+    if (st != CS_OK) return st;
+    st = io_kind(y, &y_host, &ym, who, "y");
+    if (st != CS_OK) return st;
+    if (!x_host && (reinterpret_cast<uintptr_t>(x) & 15u)) {
+        set_error("cs_decode_attention: a device x must be 16-byte aligned");
+        return CS_ERR_INVALID;
+    }
+
+    StackPlan p;
+    p.layers = nullptr; p.preds = pred; p.L = 1; p.d = d; p.f = H; p.r = pred->r;
+    p.scale = 1.f; p.sel = *params; p.mode = CS_STACK_SEQUENTIAL;
+    p.ws = static_cast<char *>(ws);
+    p.lay = ws_layout(d, H, pred->r, 1, device_sm_count());
+    p.trace_count = count; p.trace_idx = heads;
+    p.layer_only = true;
+    p.attn = &c;
+    if (ws_bytes < p.lay.total) {
+        set_error("cs_decode_attention: workspace too small: %zu bytes given, %zu needed", ws_bytes, p.lay.total);
+        return CS_ERR_WORKSPACE;
+    }
+    // host x and y go through the workspace's x row and y staging row
+    p.x = x_host ? reinterpret_cast<float *>(p.ws + p.lay.st_x) : const_cast<float *>(x);
+    p.y = y_host ? reinterpret_cast<float *>(p.ws + p.lay.io_y) : y;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    auto enq = [&]() { return enqueue_attention(p, s); };
+    if ((x_host || y_host) && (!x_host || xm) && (!y_host || ym) && graph_io_enabled()) {
+        p.io_src = x_host ? static_cast<const float *>(xm) : nullptr;
+        p.io_dst = y_host ? static_cast<float *>(ym) : nullptr;
+        bool refused = false;
+        st = run_cached(p, s, nullptr, who, enq, &refused);
+        if (st != CS_OK || !refused) return st;
+        p.io_src = nullptr;
+        p.io_dst = nullptr;
+    }
+    const size_t xy_bytes = sizeof(float) * (size_t)d;
+    if (x_host) {
+        cudaError_t e = cudaMemcpyAsync(p.x, x, xy_bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_attention(x copy)");
+    }
+    st = run_cached(p, s, nullptr, who, enq);
+    if (st != CS_OK) return st;
+    if (y_host) {
+        cudaError_t e = cudaMemcpyAsync(y, p.y, xy_bytes, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cs_decode_attention(y copy)");
     }
     return CS_OK;
 }

@@ -350,6 +350,31 @@ cs_status cs_sparse_attention(const cs_attn_layer *layer, const float *x, const 
                               float *y, void *ws, size_t ws_bytes, cs_stream_t stream);
 
 /*
+ * One token's head-sparse attention step in one call, [P1] first section (a
+ * small, input-dependent set of heads) and [P2] "Implications for System
+ * Design" (predict the heads, compute only those):
+ *     H_sel = select(P(x)),  y = cs_sparse_attention(x, H_sel).
+ *   pred: rank r, d = layer->d inputs, f = layer->n_heads outputs (one score
+ *      per head).
+ *   params: CS_SEL_TOPK or CS_SEL_THRESHOLD over the head scores, hot = 0
+ *      (else CS_ERR_INVALID).
+ *   x, y: [d] fp32, device memory (x 16-byte aligned) or page-locked host
+ *      memory, read and written as in cs_decode_layer; y must not be x.
+ *   k_cache, v_cache, seq_len: as cs_sparse_attention.
+ *   heads: [n_heads] int32 device or NULL; count: int32 device scalar or NULL
+ *      (both or neither) -- the chosen heads, ascending, and their number.
+ * Predictor, selection and attention are captured into one CUDA graph per
+ * argument set and replayed, as in cs_decode_layer (same capture and
+ * host-buffer rules).  The workspace must hold cs_workspace_size(d, n_heads,
+ * r, 1) bytes and meet cs_sparse_attention's bound on partial values; it
+ * uses the same regions as cs_decode_layer and cs_decode_stack.
+ */
+cs_status cs_decode_attention(const cs_attn_layer *layer, const cs_predictor *pred, const float *x, float *y,
+                              const cs_select_params *params, const void *k_cache, const void *v_cache,
+                              int seq_len, void *ws, size_t ws_bytes, cs_stream_t stream, int32_t *heads,
+                              int32_t *count);
+
+/*
  * Fits a predictor's up map to its layer, [P2] "The Prediction Problem" (the
  * predictor is trained to reproduce which neurons the layer activates) and
  * [P1] "Precision, recall, and which error hurts".  With pred->p_down fixed,

@@ -145,6 +145,23 @@ def test_attention_and_fit_validation_without_gpu(lib):
     assert lib.cs_sparse_attention(C.byref(A), fake, fake, fake, fake, fake, 20000, y, fake, 1 << 20, None) == 3
     # x aliasing y
     assert lib.cs_sparse_attention(C.byref(A), fake, fake, fake, fake, fake, 16, fake, fake, 1 << 20, None) == 1
+    # the one-call attention step: heads without a count, an exact or hot
+    # selection, a predictor that does not score one output per head
+    P8 = cs._Pred(512, 16, 8, cs.CS_F16, 512, 16, fake, fake)
+    top = cs.select_params(cs.CS_SEL_TOPK, 2)
+    args = (fake, fake, 16, fake, 1 << 20, None)
+    assert lib.cs_decode_attention(None, C.byref(P8), fake, y, C.byref(top), *args, None, None) == 1
+    assert lib.cs_decode_attention(C.byref(A), C.byref(P8), fake, fake, C.byref(top), *args, None, None) == 1
+    assert lib.cs_decode_attention(C.byref(A), C.byref(P8), fake, y, C.byref(top), *args, fake, None) == 1
+    for bad_sel in (cs.select_params(cs.CS_SEL_EXACT), cs.select_params(cs.CS_SEL_TOPK, 2, hot=32)):
+        assert lib.cs_decode_attention(C.byref(A), C.byref(P8), fake, y, C.byref(bad_sel), *args,
+                                       None, None) == 1
+    assert b"top-k or a threshold" in lib.cs_last_error()
+    P9 = cs._Pred(512, 16, 9, cs.CS_F16, 512, 16, fake, fake)
+    assert lib.cs_decode_attention(C.byref(A), C.byref(P9), fake, y, C.byref(top), *args, None, None) == 1
+    assert b"heads" in lib.cs_last_error()
+    assert lib.cs_decode_attention(C.byref(bad), C.byref(P8), fake, y, C.byref(top), *args, None, None) == 1
+    assert b"d_head" in lib.cs_last_error()
     # the fit: negative ridge, a predictor for another layer
     L = cs._Layer(128, 64, cs.CS_F16, 128, 256, 0, 256, 0)
     P = cs._Pred(128, 8, 64, cs.CS_F16, 0, 0, 256, 256)

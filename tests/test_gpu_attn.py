@@ -117,3 +117,98 @@ def test_attention_step_with_predicted_heads():
     assert np.array_equal(got, oracle.select_topk(s32, k))
     assert rel_err(y.cpu().numpy(), oracle.attention(A, x[0], got, kc, vc)) < TOL
     assert cs.cs_get_device_error(ws) == 0
+
+
+def _predicted_heads_case():
+    d, H, dh, S, r = 2048, 32, 64, 512, 64
+    A, dev, kc, vc = attn_case(d, H, dh, S, synth.BF16, seed=11)
+    sd = 1 / math.sqrt(d)
+    pd = synth.normal_matrix(12, 0, r, d, sd, synth.BF16)
+    pu = synth.normal_matrix(12, 1, H, r, 1 / math.sqrt(r), synth.BF16)
+    P = oracle.Predictor(d, r, H, synth.BF16, pd, pu)
+    pred = cs.Predictor(upload(pd, synth.BF16), upload(pu, synth.BF16))
+    return d, H, r, A, dev, kc, vc, P, pred
+
+
+def _widest_gap_k(s_ref, lo, hi):
+    order = np.sort(s_ref)[::-1]
+    gaps = order[:-1] - order[1:]
+    return int(np.argmax(gaps[lo - 1:hi - 1])) + lo
+
+
+@pytest.mark.parametrize("io", ["device", "pinned", "pinned_x", "pinned_y"])
+@pytest.mark.parametrize("mode", ["topk", "threshold"])
+def test_decode_attention_one_call(io, mode):
+    """cs_decode_attention (predictor, head selection and attention as one
+    cached graph, x and y on the device or in pinned host memory): the same
+    heads and bit for bit the same y as the three calls, over tokens that
+    re-point the graph's copy kernels; heads against the oracle's selection
+    and y against the oracle's attention."""
+    d, H, r, A, dev, kc, vc, P, pred = _predicted_heads_case()
+    layer = cs.AttnLayer(dev["wq"], dev["wo"], H)
+    ws = cs.Workspace(d, H, r)
+    X = synth.x_normal(21, 3, d)
+    xs_d = torch.from_numpy(X).cuda()
+    xs_h = torch.from_numpy(X).pin_memory()
+    ys_h = torch.full((3, d), float("nan")).pin_memory()
+    ys_d = torch.full((3, d), float("nan"), device="cuda")
+    sc = torch.empty((1, H), device="cuda")
+    hd3 = torch.empty((1, H), dtype=torch.int32, device="cuda")
+    cnt3 = torch.empty(1, dtype=torch.int32, device="cuda")
+    y3 = torch.empty(d, device="cuda")
+    hd = torch.full((H,), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for t in range(3):
+        _, s_ref = oracle.predict(P, X[t])
+        s32 = s_ref.astype(np.float32)
+        if mode == "topk":
+            k = _widest_gap_k(s_ref, 5, 12)
+            params = cs.select_params(cs.CS_SEL_TOPK, k)
+            want = oracle.select_topk(s32, k)
+        else:
+            k = _widest_gap_k(s_ref, 4, 16)
+            order = np.sort(s32)[::-1]
+            tau = float((order[k - 1] + order[k]) / 2)
+            params = cs.select_params(cs.CS_SEL_THRESHOLD, 0, tau)
+            want = oracle.select_threshold(s32, np.float32(tau))
+        cs.cs_predict(pred, xs_d[t:t + 1], sc, ws)
+        cs.cs_select(sc, params, hd3, cnt3, ws=ws)
+        cs.cs_sparse_attention(layer, xs_d[t], hd3[0], cnt3, dev["k"], dev["v"], y3, ws)
+        x_in = xs_h[t] if io in ("pinned", "pinned_x") else xs_d[t]
+        y_out = ys_h[t] if io in ("pinned", "pinned_y") else ys_d[t]
+        cs.cs_decode_attention(layer, pred, x_in, y_out, params, dev["k"], dev["v"], ws, heads=hd, count=cnt)
+        torch.cuda.synchronize()
+        n = int(cnt.item())
+        assert n == int(cnt3.item()) == want.size, (t, n, want.size)
+        got = hd.cpu().numpy()[:n]
+        assert np.array_equal(got, hd3.cpu().numpy()[0, :n])
+        assert np.array_equal(got, want)
+        y = y_out.cpu().numpy()
+        assert np.array_equal(y, y3.cpu().numpy())
+        assert rel_err(y, oracle.attention(A, X[t], got, kc, vc)) < TOL
+    assert cs.cs_get_device_error(ws) == 0
+
+
+def test_decode_attention_without_head_outputs():
+    """Without heads / count the workspace holds them; y is unchanged."""
+    d, H, r, A, dev, kc, vc, P, pred = _predicted_heads_case()
+    layer = cs.AttnLayer(dev["wq"], dev["wo"], H)
+    ws = cs.Workspace(d, H, r)
+    x = synth.x_normal(22, 1, d)
+    _, s_ref = oracle.predict(P, x[0])
+    k = _widest_gap_k(s_ref, 5, 12)
+    params = cs.select_params(cs.CS_SEL_TOPK, k)
+    xt = torch.from_numpy(x[0]).cuda()
+    y1 = torch.empty(d, device="cuda")
+    y2 = torch.empty(d, device="cuda")
+    hd = torch.empty(H, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(1, dtype=torch.int32, device="cuda")
+    cs.cs_decode_attention(layer, pred, xt, y1, params, dev["k"], dev["v"], ws)
+    cs.cs_decode_attention(layer, pred, xt, y2, params, dev["k"], dev["v"], ws, heads=hd, count=cnt)
+    torch.cuda.synchronize()
+    assert np.array_equal(y1.cpu().numpy(), y2.cpu().numpy())
+    want = oracle.select_topk(s_ref.astype(np.float32), k)
+    assert np.array_equal(hd.cpu().numpy()[:int(cnt.item())], want)
+    assert rel_err(y1.cpu().numpy(), oracle.attention(A, x[0], want, kc, vc)) < TOL
+    with pytest.raises(cs.CsError):
+        cs.cs_decode_attention(layer, pred, xt, xt, params, dev["k"], dev["v"], ws)
