@@ -381,8 +381,10 @@ struct ClSmem {
     uint32_t hist[kBuckets];                  // local histogram
     uint32_t ptot[kCl][kCl];                // [source CTA][slice] partial slice totals
     float plo[kCl], phi[kCl];               // min / max from each CTA
-    uint32_t ckey[kCl][kCandSmall];          // [source CTA] pivot-bucket members
-    uint32_t cid[kCl][kCandSmall];
+    // [source CTA] pivot-bucket members; rows padded by one word so that lanes
+    // walking different CTAs' rows at one position hit different banks
+    uint32_t ckey[kCl][kCandSmall + 1];
+    uint32_t cid[kCl][kCandSmall + 1];
     uint32_t ccnt[kCl];
     uint32_t pgt[kCl], peq[kCl];            // (greater, tie) totals from each CTA
     uint32_t pabove[kCl];                   // scores above the pivot bucket in each CTA
