@@ -27,7 +27,8 @@
 //
 // Rows of f >= 2048 scores run on a cluster of 8 CTAs (the per-element passes
 // split 8 ways, the CTAs exchanging through distributed shared memory);
-// shorter rows on one CTA.  Neither takes a global atomic or a grid-wide
+// shorter rows on one CTA, and rows of at most 64 scores on one warp (exact
+// ranks by pairwise comparison).  None takes a global atomic or a grid-wide
 // barrier.
 #include <cooperative_groups.h>
 
@@ -879,10 +880,82 @@ cudaError_t launch_select_row(const SelectArgs &a, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------------------
+// Warp row kernel: rows of f <= 64 scores (one score per attention head, say)
+// on one warp each; lane l holds ids l and l + 32.  Top-k ranks every score
+// exactly: its rank is the number of scores ahead of it (a larger key, or an
+// equal key at a lower id), found by broadcasting each key in turn; the
+// scores of rank < k are taken.  Ballots compact the taken ids in ascending
+// order.  No shared memory and no barrier.
+// ---------------------------------------------------------------------------
+constexpr int kWarpRowMaxF = 64;
+
+template <int KIND>
+__global__ void __launch_bounds__(32) select_warp_kernel(const float *scores, int f, int k, float tau,
+                                                         int32_t *__restrict__ idx, int ld_idx,
+                                                         int32_t *__restrict__ count, uint32_t *__restrict__ mask,
+                                                         int hot) {
+    const int lane = threadIdx.x, b = blockIdx.x;
+    const float *s = scores + (size_t)b * f;
+    int32_t *const row = idx + (size_t)b * ld_idx;
+    int32_t *out = row + hot;
+    pdl_launch_dependents();
+    pdl_wait();  // scores come from the previous kernel
+    const bool in0 = lane < f, in1 = lane + 32 < f;
+    const float v0 = in0 ? ld_dep(s + lane) : 0.f, v1 = in1 ? ld_dep(s + lane + 32) : 0.f;
+    bool t0, t1;
+    if (KIND == SEL_TOPK) {
+        const int kk = k < 0 ? 0 : (k > f ? f : k);
+        const uint32_t k0 = score_key(v0), k1 = score_key(v1);
+        int r0 = 0, r1 = 0;
+        for (int j = 0; j < f; ++j) {
+            const uint32_t kj = __shfl_sync(kFull, j < 32 ? k0 : k1, j & 31);
+            r0 += (kj > k0) || (kj == k0 && j < lane);
+            r1 += (kj > k1) || (kj == k1 && j < lane + 32);
+        }
+        t0 = in0 && r0 < kk;
+        t1 = in1 && r1 < kk;
+    } else if (KIND == SEL_THRESHOLD) {
+        t0 = in0 && v0 >= tau;
+        t1 = in1 && v1 >= tau;
+    } else if (KIND == SEL_SILU_MAG) {
+        t0 = in0 && fabsf(gate_act(CS_ACT_SILU, v0)) > tau;
+        t1 = in1 && fabsf(gate_act(CS_ACT_SILU, v1)) > tau;
+    } else {   // SEL_POSITIVE
+        t0 = in0 && v0 > tau;
+        t1 = in1 && v1 > tau;
+    }
+    const uint32_t m0 = __ballot_sync(kFull, t0), m1 = __ballot_sync(kFull, t1);
+    const uint32_t below = (1u << lane) - 1u;
+    const int n0 = __popc(m0);
+    if (t0) out[__popc(m0 & below)] = hot + lane;
+    if (t1) out[n0 + __popc(m1 & below)] = hot + lane + 32;
+    if (lane == 0) count[b] = hot + n0 + __popc(m1);
+    for (int i = lane; i < hot; i += 32) row[i] = i;
+    if (mask) {
+        uint32_t *mrow = mask + (size_t)b * ((hot + f + 31) >> 5);
+        for (int w = lane; w < (hot >> 5); w += 32) mrow[w] = 0xffffffffu;
+        if (lane == 0 && f > 0) mrow[hot >> 5] = m0;
+        if (lane == 1 && f > 32) mrow[(hot >> 5) + 1] = m1;
+    }
+}
+
+cudaError_t launch_select_warp(const SelectArgs &a, cudaStream_t s) {
+    auto go = [&](auto kern) {
+        return launch(kern, dim3(a.B), dim3(32), 0, s, pdl_enabled(), a.scores, a.f, a.k, a.tau, a.idx, a.ld_idx,
+                      a.count, a.mask, a.hot);
+    };
+    if (a.kind == SEL_TOPK) return go(select_warp_kernel<SEL_TOPK>);
+    if (a.kind == SEL_THRESHOLD) return go(select_warp_kernel<SEL_THRESHOLD>);
+    if (a.kind == SEL_SILU_MAG) return go(select_warp_kernel<SEL_SILU_MAG>);
+    return go(select_warp_kernel<SEL_POSITIVE>);
+}
+
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs &a, cudaStream_t s) {
     if (a.f >= 2048) return launch_select_cl(a, s);
+    if (a.f <= kWarpRowMaxF) return launch_select_warp(a, s);
     return launch_select_row(a, s);
 }
 

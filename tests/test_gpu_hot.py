@@ -43,7 +43,7 @@ def host_bits(a, dt):
 
 # ---------------------------------------------------------------- selection
 
-@pytest.mark.parametrize("f_tail,hot", [(1000, 32), (2047, 1024), (19456, 1024), (27648, 1024)])
+@pytest.mark.parametrize("f_tail,hot", [(40, 64), (1000, 32), (2047, 1024), (19456, 1024), (27648, 1024)])
 @pytest.mark.parametrize("B", [1, 3])
 def test_select_hot_bit_exact(f_tail, hot, B):
     S = np.stack([synth.score_vector(50 + b, f_tail, ties=f_tail // 10, specials=bool(b % 2))

@@ -77,7 +77,7 @@ def test_predict(dt, shape, B):
 
 # --------------------------------------------------------------- selection
 
-SEL_F = [1, 7, 64, 1000, 2048, 20480, 32768, 49152]
+SEL_F = [1, 7, 33, 40, 64, 65, 1000, 2048, 20480, 32768, 49152]
 
 
 @pytest.mark.parametrize("f", SEL_F)
