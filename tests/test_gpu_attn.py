@@ -212,3 +212,30 @@ def test_decode_attention_without_head_outputs():
     assert rel_err(y1.cpu().numpy(), oracle.attention(A, x[0], want, kc, vc)) < TOL
     with pytest.raises(cs.CsError):
         cs.cs_decode_attention(layer, pred, xt, xt, params, dev["k"], dev["v"], ws)
+
+
+@pytest.mark.parametrize("sel", ["k0", "tau_inf", "all"])
+def test_decode_attention_edge_selections(sel):
+    """No head chosen (k = 0, or a threshold above every score): y = 0 and
+    count 0; every head chosen: the full attention, against the oracle."""
+    d, H, r, A, dev, kc, vc, P, pred = _predicted_heads_case()
+    layer = cs.AttnLayer(dev["wq"], dev["wo"], H)
+    ws = cs.Workspace(d, H, r)
+    x = synth.x_normal(23, 1, d)
+    params = {"k0": cs.select_params(cs.CS_SEL_TOPK, 0),
+              "tau_inf": cs.select_params(cs.CS_SEL_THRESHOLD, 0, float("inf")),
+              "all": cs.select_params(cs.CS_SEL_TOPK, H + 3)}[sel]
+    y = torch.full((d,), float("nan")).pin_memory()
+    hd = torch.full((H,), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    cs.cs_decode_attention(layer, pred, torch.from_numpy(x[0]).pin_memory(), y, params, dev["k"], dev["v"], ws,
+                           heads=hd, count=cnt)
+    torch.cuda.synchronize()
+    n = int(cnt.item())
+    if sel == "all":
+        assert n == H and np.array_equal(hd.cpu().numpy(), np.arange(H))
+        assert rel_err(y.numpy(), oracle.attention(A, x[0], list(range(H)), kc, vc)) < TOL
+    else:
+        assert n == 0
+        assert np.all(y.numpy() == 0)
+    assert cs.cs_get_device_error(ws) == 0
