@@ -49,7 +49,7 @@ typedef enum cs_status {
     CS_OK = 0,
     CS_ERR_INVALID = 1,     /* bad argument; nothing was enqueued              */
     CS_ERR_CUDA = 2,        /* a CUDA runtime call failed (see cs_last_error)  */
-    CS_ERR_UNSUPPORTED = 3, /* valid, but outside what this build handles      */
+    CS_ERR_UNSUPPORTED = 3, /* valid, but outside the supported sizes          */
     CS_ERR_TIMEOUT = 4,     /* a bounded device wait gave up                   */
     CS_ERR_WORKSPACE = 5    /* workspace missing, misaligned or too small      */
 } cs_status;
